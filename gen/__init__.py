@@ -1,0 +1,156 @@
+"""Seeded synthetic inputs for the fused norm/act -> FP8 ops.
+
+This module is shared by the tests, the smoke check and the benchmark, and
+serves both the oracle and the CUDA path with the same bytes.  It contains
+none of the method's arithmetic: it draws random numbers (numpy PCG64 streams
+keyed by ``(seed, tensor id, row block)``) and converts them to bf16 with
+PyTorch's CPU cast, which rounds to nearest even.
+
+Distributions follow the workloads in the design notes:
+  x, residual, gate_up ~ N(0, 1)
+  weight               ~ 1 + 0.1 * N(0, 1)
+  prefill x            ~ Student-t(3) with 0.1 % of the elements scaled by 100
+Each tensor is split into blocks of rows generated independently, so a
+tensor's values do not depend on the number of threads used.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+TENSOR_X, TENSOR_RESIDUAL, TENSOR_WEIGHT, TENSOR_GATE_UP = 1, 2, 3, 4
+_ROW_BLOCK = 64
+
+STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
+MODE_NAMES = {STATIC: "static", PER_TOKEN: "per_token", PER_GROUP: "per_group"}
+
+
+def _threads() -> int:
+    return max(1, min(16, os.cpu_count() or 1))
+
+
+def _rng(seed: int, tensor_id: int, block: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tensor_id, block])))
+
+
+def _draw(kind: str, rng: np.random.Generator, shape) -> np.ndarray:
+    if kind == "normal":
+        return rng.standard_normal(shape, dtype=np.float32)
+    if kind == "weight":
+        return (1.0 + 0.1 * rng.standard_normal(shape, dtype=np.float64)).astype(np.float32)
+    if kind == "t3_outliers":
+        t = rng.standard_t(3, size=shape)
+        hit = rng.random(shape) < 0.001
+        t[hit] *= 100.0
+        return t.astype(np.float32)
+    raise ValueError(f"unknown distribution {kind!r}")
+
+
+def to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float32 array -> uint16 bf16 bit patterns (PyTorch's RNE cast)."""
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_tensor(kind: str, seed: int, tensor_id: int, rows: int, cols: int) -> np.ndarray:
+    """A [rows, cols] bf16 tensor (uint16 bits) of distribution ``kind``."""
+    out = np.empty((rows, cols), np.uint16)
+    nblocks = (rows + _ROW_BLOCK - 1) // _ROW_BLOCK
+
+    def work(b):
+        r0 = b * _ROW_BLOCK
+        r1 = min(rows, r0 + _ROW_BLOCK)
+        vals = _draw(kind, _rng(seed, tensor_id, b), (r1 - r0, cols))
+        out[r0:r1] = to_bf16_bits(vals)
+
+    if nblocks <= 2:
+        for b in range(nblocks):
+            work(b)
+    else:
+        with ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(work, range(nblocks)))
+    return out
+
+
+def norm_inputs(T: int, H: int, seed: int = 0, x_dist: str = "normal"):
+    """x [T,H], residual [T,H], weight [H] as uint16 bf16 bits."""
+    return {
+        "x": bf16_tensor(x_dist, seed, TENSOR_X, T, H),
+        "residual": bf16_tensor("normal", seed, TENSOR_RESIDUAL, T, H),
+        "weight": bf16_tensor("weight", seed, TENSOR_WEIGHT, 1, H).reshape(H),
+    }
+
+
+def silu_inputs(T: int, I: int, seed: int = 0):
+    """gate_up [T, 2I] (gate half, then up half) as uint16 bf16 bits."""
+    return {"gate_up": bf16_tensor("normal", seed, TENSOR_GATE_UP, T, 2 * I)}
+
+
+# ----------------------------------------------------------------- workloads
+
+@dataclass(frozen=True)
+class Workload:
+    """One op invocation: which op, its shape, scale mode and inputs."""
+    name: str
+    op: str                  # "norm" or "silu"
+    T: int
+    n: int                   # hidden (norm) or intermediate (silu)
+    mode: int
+    group_size: int = 128
+    eps: float = 1e-5
+    static_scale: float = 0.05
+    x_dist: str = "normal"
+    residual: bool = True
+    seed: int = 0
+    note: str = field(default="", compare=False)
+
+    def inputs(self):
+        if self.op == "norm":
+            return norm_inputs(self.T, self.n, self.seed, self.x_dist)
+        return silu_inputs(self.T, self.n, self.seed)
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes the op must move: every row read once and written once; the
+        weight and a static scale read once per launch."""
+        s_row = {STATIC: 0, PER_TOKEN: 4, PER_GROUP: 4 * (self.n // self.group_size)}[self.mode]
+        s0 = 4 if self.mode == STATIC else 0
+        if self.op == "norm":
+            per_row = (7 if self.residual else 3) * self.n + s_row
+            return self.T * per_row + 2 * self.n + s0
+        return self.T * (5 * self.n + s_row) + s0
+
+
+# The named shapes: a small static case, a Llama-3-8B-shaped decode step, the
+# SiLU-and-mul 2048 x 14336 case in two modes, a 70B-shaped prefill with
+# heavy-tailed activations, and the bandwidth sweep.
+CFG0 = Workload("norm_static_16x1024", "norm", 16, 1024, STATIC, eps=1e-6, static_scale=0.05)
+CFG1 = Workload("norm_per_token_256x4096", "norm", 256, 4096, PER_TOKEN, eps=1e-5)
+CFG2A = Workload("silu_static_2048x14336", "silu", 2048, 14336, STATIC, static_scale=0.1)
+CFG2B = Workload("silu_per_group128_2048x14336", "silu", 2048, 14336, PER_GROUP, group_size=128)
+CFG3 = Workload("norm_per_group128_16384x8192_t3", "norm", 16384, 8192, PER_GROUP,
+                group_size=128, eps=1e-5, x_dist="t3_outliers")
+# The SiLU half of the Llama-3-8B decode step: intermediate 14336 pairs with
+# hidden 4096 in the sweep's shape list.
+CFG1_ACT = Workload("silu_per_token_256x14336", "silu", 256, 14336, PER_TOKEN)
+
+NAMED = {w.name: w for w in (CFG0, CFG1, CFG2A, CFG2B, CFG3, CFG1_ACT)}
+
+SWEEP_T = (1, 8, 64, 512, 4096, 32768)
+SWEEP_SHAPES = ((4096, 14336), (8192, 28672))
+
+
+def sweep():
+    """Both ops x three scale modes x T x (hidden, intermediate)."""
+    out = []
+    for H, I in SWEEP_SHAPES:
+        for mode in (STATIC, PER_TOKEN, PER_GROUP):
+            for T in SWEEP_T:
+                out.append(Workload(f"norm_{MODE_NAMES[mode]}_{T}x{H}", "norm", T, H, mode,
+                                    eps=1e-5, static_scale=0.05))
+                out.append(Workload(f"silu_{MODE_NAMES[mode]}_{T}x{I}", "silu", T, I, mode,
+                                    static_scale=0.1))
+    return out

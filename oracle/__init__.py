@@ -1,0 +1,225 @@
+"""Plain fp64 CPU oracle for fused residual-add + RMSNorm -> FP8 and
+SiLU-and-mul -> FP8 (numpy front end over ``oracle.c``).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product
+package never imports it and shares no code with it.
+
+What each function computes is documented in ``oracle.c`` with the passages
+it follows ("Fusion torch.compile passes", sections "RMSNorm + Quantization
+(fuse_norm_quant)" and "SiLU+Mul + Quantization (fuse_act_quant)"; OCP OFP8
+for the E4M3 format).
+
+Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
+  bf16 / e4m3 codecs ........ pinned (spec points, exhaustive round trips,
+                              brute-force nearest value)
+  fused_add_rms_norm_fp8 .... pinned (closed forms, invariants, library
+                              bf16 add, exact-arithmetic brute force)
+  silu_mul_fp8 .............. pinned (closed forms, library sigmoid,
+                              exact-arithmetic brute force)
+  NaN / Inf inputs .......... parity unpinned (no workload contains them)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lock = threading.Lock()
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile one C source file into a shared library with the oracle's flags."""
+    tmp = out + f".tmp{os.getpid()}"
+    cc = os.environ.get("CC", "gcc")
+    subprocess.check_call([cc, *_CFLAGS, "-o", tmp, src, "-lm"])
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``_build/liboracle.so`` (gcc, no GPU needed)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        compile_source(_SRC, _LIB_PATH)
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) the oracle's shared library."""
+    lib = ctypes.CDLL(path or build())
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    lib.orc_fused_add_rms_norm_fp8.argtypes = [P, P, P, P, P, P, P, i64, i64,
+                                               ctypes.c_float, ctypes.c_int, i64]
+    lib.orc_fused_add_rms_norm_fp8.restype = ctypes.c_int
+    lib.orc_silu_mul_fp8.argtypes = [P, P, P, P, i64, i64, ctypes.c_int, i64]
+    lib.orc_silu_mul_fp8.restype = ctypes.c_int
+    for name in ("orc_bf16_decode_n", "orc_bf16_encode_n",
+                 "orc_e4m3_decode_n", "orc_e4m3_encode_n"):
+        getattr(lib, name).argtypes = [P, P, i64]
+        getattr(lib, name).restype = None
+    lib.orc_amax_floor.argtypes = []
+    lib.orc_amax_floor.restype = ctypes.c_double
+    return lib
+
+
+class Oracle:
+    """The oracle's functions bound to one loaded copy of its library (the
+    tests also load deliberately broken copies to show the pins catch them)."""
+
+    def __init__(self, lib: ctypes.CDLL):
+        self.lib = lib
+
+    # -------------------------------------------------------------- codecs
+    def bf16_decode(self, bits) -> np.ndarray:
+        b = _u16(bits)
+        out = np.empty(b.shape, np.float64)
+        self.lib.orc_bf16_decode_n(_ptr(out), _ptr(b), b.size)
+        return out
+
+    def bf16_encode(self, values) -> np.ndarray:
+        v = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(v.shape, np.uint16)
+        self.lib.orc_bf16_encode_n(_ptr(out), _ptr(v), v.size)
+        return out
+
+    def e4m3_decode(self, codes) -> np.ndarray:
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, np.float64)
+        self.lib.orc_e4m3_decode_n(_ptr(out), _ptr(c), c.size)
+        return out
+
+    def e4m3_encode(self, values) -> np.ndarray:
+        v = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(v.shape, np.uint8)
+        self.lib.orc_e4m3_encode_n(_ptr(out), _ptr(v), v.size)
+        return out
+
+    def amax_floor(self) -> float:
+        """A_MIN, the floor on a dynamic amax (the fp32 number nearest 1e-10)."""
+        return float(self.lib.orc_amax_floor())
+
+    # ----------------------------------------------------------------- ops
+    def fused_add_rms_norm_fp8(self, x, residual, weight, eps: float, mode: int,
+                               group_size: int = 128, scale=None, want_v: bool = True):
+        """fused_add_rms_norm(x, residual) -> quant_fp8, or with ``residual``
+        None the plain rms_norm(x) -> quant_fp8 variant.
+
+        x, residual: uint16 bf16 bits [T, H]; weight: uint16 [H].
+        Returns dict(q uint8 [T,H], residual_out uint16 [T,H] or None,
+        scale float32 ([1] static / [T] / [T,H/G]), v float64 [T,H] = y/s)."""
+        x = _u16(x)
+        T, H = x.shape
+        w = _u16(weight).reshape(H)
+        res = None if residual is None else _u16(residual).reshape(T, H)
+        q = np.empty((T, H), np.uint8)
+        r_out = None if res is None else np.empty((T, H), np.uint16)
+        s = _scale_buffer(mode, T, H, group_size, scale)
+        v = np.empty((T, H), np.float64) if want_v else None
+        rc = self.lib.orc_fused_add_rms_norm_fp8(
+            _ptr(q), _ptr(r_out), _ptr(s), _ptr(v), _ptr(x), _ptr(res), _ptr(w),
+            T, H, ctypes.c_float(eps), mode, group_size)
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (rc={rc})")
+        return {"q": q, "residual_out": r_out, "scale": s, "v": v}
+
+    def silu_mul_fp8(self, gate_up, mode: int, group_size: int = 128, scale=None,
+                     want_v: bool = True):
+        """silu_and_mul(gate_up) -> quant_fp8.
+
+        gate_up: uint16 bf16 bits [T, 2I], gate = columns [0, I), up = [I, 2I).
+        Returns dict(q uint8 [T,I], scale, v float64 [T,I])."""
+        gu = _u16(gate_up)
+        T, two_i = gu.shape
+        if two_i % 2:
+            raise ValueError("gate_up must have an even number of columns")
+        I = two_i // 2
+        q = np.empty((T, I), np.uint8)
+        s = _scale_buffer(mode, T, I, group_size, scale)
+        v = np.empty((T, I), np.float64) if want_v else None
+        rc = self.lib.orc_silu_mul_fp8(_ptr(q), _ptr(s), _ptr(v), _ptr(gu), T, I, mode,
+                                       group_size)
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (rc={rc})")
+        return {"q": q, "scale": s, "v": v}
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.int16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected bf16 bit patterns as uint16, got {a.dtype}")
+    return a
+
+
+def _scale_buffer(mode: int, rows: int, n: int, group_size: int, scale):
+    if mode == STATIC:
+        if scale is None:
+            raise ValueError("static mode needs the fp32 scale")
+        return np.array([np.asarray(scale, np.float32).reshape(-1)[0]], np.float32)
+    if mode == PER_TOKEN:
+        return np.zeros((rows,), np.float32)
+    if mode == PER_GROUP:
+        if group_size <= 0 or n % group_size:
+            raise ValueError("per-group mode needs a group size dividing the row")
+        return np.zeros((rows, n // group_size), np.float32)
+    raise ValueError(f"bad scale mode {mode}")
+
+
+def default() -> Oracle:
+    """The oracle built from ``oracle.c`` as committed."""
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(load_library())
+    return _default
+
+
+_default = None
+
+
+def bf16_decode(bits):
+    return default().bf16_decode(bits)
+
+
+def bf16_encode(values):
+    return default().bf16_encode(values)
+
+
+def e4m3_decode(codes):
+    return default().e4m3_decode(codes)
+
+
+def e4m3_encode(values):
+    return default().e4m3_encode(values)
+
+
+def amax_floor():
+    return default().amax_floor()
+
+
+def fused_add_rms_norm_fp8(*args, **kwargs):
+    return default().fused_add_rms_norm_fp8(*args, **kwargs)
+
+
+def silu_mul_fp8(*args, **kwargs):
+    return default().silu_mul_fp8(*args, **kwargs)

@@ -1,0 +1,294 @@
+/*
+ * oracle.c -- plain, slow, scalar fp64 CPU oracle for the two fused ops
+ *
+ *   fused_add_rms_norm -> quant_fp8   (fuse_norm_quant)
+ *   silu_and_mul       -> quant_fp8   (fuse_act_quant)
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this file's library.  It shares no
+ * code, header, table or constant with the CUDA library; it has its own bf16
+ * and e4m3 codecs and keeps every intermediate in fp64.
+ *
+ * Sources, cited by page title and section:
+ *  [FUS]  "Fusion torch.compile passes" (data-sketchers.com wiki, vLLM
+ *         design-fusions page): section "RMSNorm + Quantization
+ *         (fuse_norm_quant)" -- the two norm variants, the in-place residual
+ *         update, and the three FP8 scale modes (static per-tensor, dynamic
+ *         per-token, dynamic per-token-group of 128/64 columns); section
+ *         "SiLU+Mul + Quantization (fuse_act_quant)" -- SiLU(gate)*up then
+ *         FP8 quant without materialising the activation; "Quick Reference"
+ *         table rows fuse_norm_quant / fuse_act_quant.
+ *  [OFP8] OCP 8-bit Floating Point Specification (OFP8), E4M3 encoding:
+ *         bias 7, no infinities, S.1111.111 is NaN, max normal 448
+ *         (S.1111.110), min normal 2^-6, min subnormal 2^-9.
+ *
+ * The pages never write the RMSNorm, SiLU or quantisation formulas out.  The
+ * readings taken here (each the plainest one the pages support):
+ *  - RMSNorm: y_j = r_j / sqrt(mean_j(r_j^2) + eps) * w_j, eps inside the
+ *    square root, the mean over the whole hidden dimension.
+ *  - The fused-add variant normalises the bf16-rounded sum r = bf16(x + res),
+ *    which is also the residual it writes back.
+ *  - y is NOT rounded to bf16 before quantising: the fusion exists to avoid
+ *    materialising that full-precision intermediate.
+ *  - Scales are dequantisation scales: q = e4m3(y / s), so y ~= q * s.
+ *    Dynamic scales are s = fp32(max(amax, A_MIN) / 448), the division uses
+ *    the stored fp32 scale, and A_MIN is the fp32 number nearest 1e-10
+ *    (it only keeps an all-zero row or group away from 0/0).
+ *  - Per-group scales cover G contiguous columns; the scale tensor is
+ *    [T, n/G] fp32, row-major.
+ *  - silu(g) = g / (1 + exp(-g)); the gate is columns [0, I) and the up
+ *    projection columns [I, 2I) of one [T, 2I] row.
+ *  - e4m3 conversion rounds to nearest, ties to even mantissa, saturates
+ *    finite overflow (and infinity) to +-448, keeps the sign of zero, and
+ *    maps NaN to 0x7F.
+ *
+ * Build: plain C11, -ffp-contract=off so that no multiply-add is fused and
+ * the results are the same on every host architecture.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_STATIC = 0, ORC_PER_TOKEN = 1, ORC_PER_GROUP = 2 };
+
+#define ORC_E4M3_MAX 448.0
+
+/* ------------------------------------------------------------------ codecs */
+
+/* Round a finite v to the nearest number with `p` significant bits whose
+ * exponent is at least `emin` (below it the spacing stays 2^(emin-p+1), i.e.
+ * gradual underflow), ties to even.  Division and multiplication by the power
+ * of two `quantum` are exact, and nearbyint rounds half to even under the
+ * default rounding mode, so the only rounding is the one intended. */
+static double round_to_precision(double v, int p, int emin)
+{
+    if (v == 0.0 || !isfinite(v))
+        return v;
+    int e = ilogb(v);
+    if (e < emin)
+        e = emin;
+    double quantum = ldexp(1.0, e - (p - 1));
+    double m = v / quantum;
+    return nearbyint(m) * quantum;
+}
+
+/* bf16 is the upper half of an IEEE binary32, so decoding is exact. */
+double orc_bf16_decode(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* bf16: 8 significant bits, emin -126, overflow to infinity (IEEE RNE). */
+uint16_t orc_bf16_encode(double v)
+{
+    if (isnan(v))
+        return (uint16_t)(signbit(v) ? 0xFFC0u : 0x7FC0u);
+    double r = round_to_precision(v, 8, -126);
+    const double bf16_max = ldexp(255.0, 120); /* (2 - 2^-7) * 2^127 */
+    if (fabs(r) > bf16_max)
+        r = signbit(r) ? -INFINITY : INFINITY;
+    float f = (float)r; /* exact: r is a bf16 value or an infinity */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+double orc_e4m3_decode(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 0xF, m = c & 0x7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double mag = (e == 0) ? ldexp((double)m, -9)           /* 0.m * 2^-6 */
+                          : ldexp((double)(8 + m), e - 10); /* 1.m * 2^(e-7) */
+    return s ? -mag : mag;
+}
+
+/* e4m3 (OCP E4M3FN): 4 significant bits, emin -6, satfinite at 448. */
+uint8_t orc_e4m3_encode(double v)
+{
+    if (isnan(v))
+        return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    double a = fabs(v);
+    double r = isinf(a) ? ORC_E4M3_MAX : round_to_precision(a, 4, -6);
+    if (r > ORC_E4M3_MAX)
+        r = ORC_E4M3_MAX;
+    if (r == 0.0)
+        return sign;
+    int e = ilogb(r);
+    if (e < -6) /* subnormal: r = k * 2^-9, k = 1..7 */
+        return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9)));
+    int mant = (int)((r / ldexp(1.0, e) - 1.0) * 8.0);
+    return (uint8_t)(sign | (uint8_t)(((e + 7) << 3) | mant));
+}
+
+void orc_bf16_decode_n(double *out, const uint16_t *in, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_bf16_decode(in[i]);
+}
+
+void orc_bf16_encode_n(uint16_t *out, const double *in, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_bf16_encode(in[i]);
+}
+
+void orc_e4m3_decode_n(double *out, const uint8_t *in, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_decode(in[i]);
+}
+
+void orc_e4m3_encode_n(uint8_t *out, const double *in, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_encode(in[i]);
+}
+
+/* ------------------------------------------------------------ quantisation */
+
+/* The fp32 number nearest 1e-10: floor on a dynamic amax. */
+double orc_amax_floor(void) { return (double)1e-10f; }
+
+static float dynamic_scale(double amax)
+{
+    double a = amax > orc_amax_floor() ? amax : orc_amax_floor();
+    return (float)(a / ORC_E4M3_MAX);
+}
+
+/* quant_fp8 of one row y[0..n) ([FUS] "RMSNorm + Quantization": static
+ * per-tensor, dynamic per-token, dynamic per-token-group).
+ *   STATIC    : s = scale[0] (input)
+ *   PER_TOKEN : s = fp32(max(amax_j |y_j|, A_MIN) / 448), written to scale[t]
+ *   PER_GROUP : same over columns [g*G, (g+1)*G), written to scale[t*n/G + g]
+ * then v_j = y_j / s (fp64, with the stored fp32 s) and q_j = e4m3(v_j).
+ * v (optional) receives v_j for the tolerance checker. */
+static void quantize_row(uint8_t *q, double *v, float *scale, const double *y,
+                         int64_t t, int64_t n, int mode, int64_t G)
+{
+    if (mode == ORC_STATIC) {
+        double s = (double)scale[0];
+        for (int64_t j = 0; j < n; ++j) {
+            double vj = y[j] / s;
+            q[j] = orc_e4m3_encode(vj);
+            if (v)
+                v[j] = vj;
+        }
+        return;
+    }
+    int64_t width = (mode == ORC_PER_TOKEN) ? n : G;
+    int64_t ngroups = n / width;
+    for (int64_t g = 0; g < ngroups; ++g) {
+        const double *yg = y + g * width;
+        double amax = 0.0;
+        for (int64_t j = 0; j < width; ++j)
+            if (fabs(yg[j]) > amax)
+                amax = fabs(yg[j]);
+        float s32 = dynamic_scale(amax);
+        scale[t * ngroups + g] = s32;
+        double s = (double)s32;
+        for (int64_t j = 0; j < width; ++j) {
+            double vj = yg[j] / s;
+            q[g * width + j] = orc_e4m3_encode(vj);
+            if (v)
+                v[g * width + j] = vj;
+        }
+    }
+}
+
+static int check_mode(int mode, int64_t n, int64_t G)
+{
+    if (mode == ORC_STATIC || mode == ORC_PER_TOKEN)
+        return 0;
+    if (mode == ORC_PER_GROUP && G > 0 && n % G == 0)
+        return 0;
+    return -1;
+}
+
+/* ------------------------------------------------------------------ ops */
+
+/* fused_add_rms_norm(x, residual) -> quant_fp8(y), rows t = 0..T-1, each
+ * of H columns ([FUS] "RMSNorm + Quantization", fused-add variant; with
+ * residual == NULL the plain rms_norm(x) -> quant_fp8(y) variant):
+ *   r_j  = bf16(x_j + res_j)   (the fp64 sum is exact unless the exponents
+ *                               are more than 45 apart, and then the smaller
+ *                               addend is far below half a bf16 ulp, so the
+ *                               RNE result is the same as for the exact sum)
+ *   residual_out_j = r_j       (the residual is updated in place)
+ *   inv  = 1 / sqrt((sum_j r_j^2) / H + eps)
+ *   y_j  = r_j * inv * w_j     (fp64, never rounded to bf16)
+ *   q    = quant_fp8(y)
+ * Layouts: x, residual, residual_out, v: [T, H]; weight [H]; q [T, H];
+ * scale as in quantize_row.  Returns 0, or -1 on a bad mode/shape. */
+int orc_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *scale,
+                               double *v, const uint16_t *x,
+                               const uint16_t *residual, const uint16_t *weight,
+                               int64_t T, int64_t H, float eps, int mode,
+                               int64_t G)
+{
+    if (T < 0 || H <= 0 || check_mode(mode, H, G) != 0)
+        return -1;
+    double *r = (double *)malloc((size_t)H * sizeof(double));
+    double *y = (double *)malloc((size_t)H * sizeof(double));
+    if (!r || !y) {
+        free(r);
+        free(y);
+        return -2;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t *xt = x + t * H;
+        for (int64_t j = 0; j < H; ++j) {
+            if (residual) {
+                double sum = orc_bf16_decode(xt[j]) + orc_bf16_decode(residual[t * H + j]);
+                uint16_t rb = orc_bf16_encode(sum);
+                residual_out[t * H + j] = rb;
+                r[j] = orc_bf16_decode(rb);
+            } else {
+                r[j] = orc_bf16_decode(xt[j]);
+            }
+        }
+        double ss = 0.0;
+        for (int64_t j = 0; j < H; ++j)
+            ss += r[j] * r[j];
+        double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
+        for (int64_t j = 0; j < H; ++j)
+            y[j] = r[j] * inv * orc_bf16_decode(weight[j]);
+        quantize_row(q + t * H, v ? v + t * H : NULL, scale, y, t, H, mode, G);
+    }
+    free(r);
+    free(y);
+    return 0;
+}
+
+/* silu_and_mul(gate_up) -> quant_fp8(a), rows t = 0..T-1 ([FUS] "SiLU+Mul +
+ * Quantization"):
+ *   g_j = gate_up[t, j], u_j = gate_up[t, I + j]   (gate half, then up half)
+ *   a_j = g_j / (1 + exp(-g_j)) * u_j              (fp64, never materialised)
+ *   q   = quant_fp8(a)
+ * Layouts: gate_up [T, 2I]; q and v [T, I]; scale as in quantize_row. */
+int orc_silu_mul_fp8(uint8_t *q, float *scale, double *v,
+                     const uint16_t *gate_up, int64_t T, int64_t I, int mode,
+                     int64_t G)
+{
+    if (T < 0 || I <= 0 || check_mode(mode, I, G) != 0)
+        return -1;
+    double *a = (double *)malloc((size_t)I * sizeof(double));
+    if (!a)
+        return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t *row = gate_up + t * 2 * I;
+        for (int64_t j = 0; j < I; ++j) {
+            double g = orc_bf16_decode(row[j]);
+            double u = orc_bf16_decode(row[I + j]);
+            a[j] = g / (1.0 + exp(-g)) * u;
+        }
+        quantize_row(q + t * I, v ? v + t * I : NULL, scale, a, t, I, mode, G);
+    }
+    free(a);
+    return 0;
+}

@@ -1,0 +1,372 @@
+"""Pins for the oracle: checks against what the E4M3/bf16 definitions, closed
+forms, invariants, library routines and exact-arithmetic brute force fix.
+
+Every ``check_*`` takes an ``oracle.Oracle`` and raises AssertionError on a
+mismatch.  ``tests/test_oracle_pins.py`` runs them on the committed oracle;
+``tests/test_oracle_mutants.py`` runs them on copies of the oracle with a
+planted mistake and requires that at least one check fails for each.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import exact
+
+STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(vals) -> np.ndarray:
+    """float values -> bf16 bits (torch RNE cast; all values used here are
+    exactly representable)."""
+    t = torch.tensor(np.asarray(vals, np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def _rand_bf16(rng, shape, scale=1.0) -> np.ndarray:
+    return _bits(rng.standard_normal(shape).astype(np.float32) * scale)
+
+
+def _weight(rng, H) -> np.ndarray:
+    return _bits((1.0 + 0.1 * rng.standard_normal(H)).astype(np.float32))
+
+
+# ----------------------------------------------------------------- e4m3
+
+def load_e4m3_points():
+    pts = []
+    with open(os.path.join(GOLDEN, "e4m3_ofp8_points.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            code, val, *_ = line.split()
+            pts.append((int(code, 16), float(val)))
+    return pts
+
+
+def check_e4m3_spec_points(orc):
+    for code, val in load_e4m3_points():
+        got = orc.e4m3_decode(np.array([code], np.uint8))[0]
+        if np.isnan(val):
+            assert np.isnan(got), (hex(code), got)
+            assert orc.e4m3_encode(np.array([np.nan]))[0] == 0x7F
+            continue
+        assert got == val and np.signbit(got) == np.signbit(val), (hex(code), got, val)
+        enc = orc.e4m3_encode(np.array([val]))[0]
+        assert enc == code, (val, hex(enc), hex(code))
+
+
+def check_e4m3_all_codes(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    dec = orc.e4m3_decode(codes)
+    nan = np.isnan(dec)
+    assert list(np.flatnonzero(nan)) == [0x7F, 0xFF]
+    # positive codes enumerate exactly the format's value set, in order
+    assert np.array_equal(dec[:0x7F], exact.E4M3_POS_F64)
+    assert np.array_equal(dec[0x80:0xFF], -exact.E4M3_POS_F64)
+    assert np.signbit(dec[0x80]) and not np.signbit(dec[0x00])
+    enc = orc.e4m3_encode(dec)
+    fin = ~nan
+    assert np.array_equal(enc[fin], codes[fin])
+
+
+def check_e4m3_encoder_brute_force(orc):
+    vals = exact.E4M3_POS_F64
+    mids = (vals[:-1] + vals[1:]) / 2.0
+    pts = [vals, mids, np.nextafter(mids, np.inf), np.nextafter(mids, -np.inf),
+           np.nextafter(vals, np.inf), np.nextafter(vals, -np.inf),
+           np.array([448.0, 460.0, 463.99, 464.0, 464.01, 479.0, 480.0, 1e6, 1e300,
+                     2.0 ** -10, 2.0 ** -10 * (1 + 2 ** -40), 2.0 ** -11, 1e-300])]
+    rng = np.random.default_rng(7)
+    pts.append(np.exp2(rng.uniform(-13, 10, 200_000)))
+    v = np.concatenate(pts)
+    v = np.concatenate([v, -v])
+    got = orc.e4m3_encode(v)
+    want = exact.e4m3_nearest_code_vec(v)
+    bad = np.flatnonzero(got != want)
+    assert bad.size == 0, [(v[i], hex(got[i]), hex(want[i])) for i in bad[:5]]
+    # the vectorised search agrees with the plain exhaustive one
+    for x in list(mids[::9]) + [460.0, 2.0 ** -10, 0.3, 17.0]:
+        assert exact.e4m3_nearest_code(x) == orc.e4m3_encode(np.array([x]))[0], x
+
+
+def check_e4m3_special_values(orc):
+    enc = orc.e4m3_encode(np.array([np.inf, -np.inf, np.nan, -0.0, -1e-30, 1e-30, 0.0]))
+    assert list(enc) == [0x7E, 0xFE, 0x7F, 0x80, 0x80, 0x00, 0x00], [hex(c) for c in enc]
+
+
+# ----------------------------------------------------------------- bf16
+
+def check_bf16_all_patterns(orc):
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    dec = orc.bf16_decode(codes)
+    ref = exact.bf16_bits_to_f64(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(dec), nan)
+    assert np.array_equal(dec[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(dec[~nan]), np.signbit(ref[~nan]))
+    enc = orc.bf16_encode(dec)
+    assert np.array_equal(enc[~nan], codes[~nan])
+    assert np.all(np.isnan(exact.bf16_bits_to_f64(enc[nan])))
+
+
+def check_bf16_encoder_brute_force(orc):
+    rng = np.random.default_rng(11)
+    vals = exact.BF16_POS_VALUES[:-1]
+    mids = (vals[:-1] + vals[1:]) / 2.0   # exact in fp64
+    pick = rng.choice(mids.size, 4000, replace=False)
+    pts = np.concatenate([
+        mids[pick], np.nextafter(mids[pick], np.inf), np.nextafter(mids[pick], -np.inf),
+        rng.standard_normal(3000) * np.exp2(rng.integers(-140, 127, 3000)),
+        np.array([3.3895313892515355e38, 3.4e38, 1e39, 1e-45, 2.0 ** -134, 2.0 ** -133 * 1.5]),
+    ])
+    pts = np.concatenate([pts, -pts])
+    got = orc.bf16_encode(pts)
+    for v, g in zip(pts, got):
+        want = exact.bf16_nearest_code(v)
+        assert int(g) == want, (v, hex(g), hex(want))
+    # library cross-check: torch's float32 -> bfloat16 cast rounds to nearest even
+    f32 = (rng.standard_normal(100_000) * np.exp2(rng.integers(-60, 60, 100_000))).astype(np.float32)
+    lib = torch.from_numpy(f32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(orc.bf16_encode(f32.astype(np.float64)), lib)
+
+
+# ------------------------------------------------------------- RMSNorm
+
+def check_norm_constant_row(orc):
+    """RMSNorm of a constant row c is c / sqrt(c^2 + eps) * w, which is
+    sign(c) * w when eps = 0 (to the rounding of c * (1/|c|))."""
+    rng = np.random.default_rng(1)
+    H = 256
+    w = _weight(rng, H)
+    wf = exact.bf16_bits_to_f64(w)
+    for c in (1.5, -0.375, 3.0e-3, 96.0):
+        x = _bits(np.full((1, H), c))
+        c = float(exact.bf16_bits_to_f64(x[0, 0]))
+        for eps in (0.0, 1e-6, 1e-2):
+            out = orc.fused_add_rms_norm_fp8(x, None, w, eps, STATIC, scale=1.0)
+            eps32 = float(np.float32(eps))
+            want = c / np.sqrt(c * c + eps32) * wf
+            if eps == 0.0:
+                np.testing.assert_allclose(out["v"][0], np.sign(c) * wf, rtol=1e-15)
+            np.testing.assert_allclose(out["v"][0], want, rtol=1e-14)
+
+
+def check_norm_h1_closed_form(orc):
+    rng = np.random.default_rng(2)
+    x = _rand_bf16(rng, (64, 1))
+    res = _rand_bf16(rng, (64, 1))
+    w = _bits([0.8125])
+    out = orc.fused_add_rms_norm_fp8(x, res, w, 1e-3, STATIC, scale=0.5)
+    r = exact.bf16_bits_to_f64(out["residual_out"])[:, 0]
+    eps32 = float(np.float32(1e-3))
+    want = r / np.sqrt(r * r + eps32) * 0.8125 / 0.5
+    np.testing.assert_allclose(out["v"][:, 0], want, rtol=1e-14)
+
+
+def check_norm_invariants(orc):
+    """eps = 0: the row's RMS of y/w is exactly 1 (up to fp64 rounding), and
+    scaling the input by 2 (exact in bf16) leaves y unchanged bit for bit."""
+    rng = np.random.default_rng(3)
+    T, H = 8, 384
+    x = _rand_bf16(rng, (T, H))
+    w = _weight(rng, H)
+    wf = exact.bf16_bits_to_f64(w)
+    out = orc.fused_add_rms_norm_fp8(x, None, w, 0.0, STATIC, scale=1.0)
+    y_over_w = out["v"] / wf
+    np.testing.assert_allclose(np.sqrt(np.mean(y_over_w ** 2, axis=1)), 1.0, rtol=1e-13)
+    # y_j / w_j is proportional to x_j within a row
+    xf = exact.bf16_bits_to_f64(x)
+    ratio = y_over_w / xf
+    np.testing.assert_allclose(ratio, ratio[:, :1] * np.ones_like(ratio), rtol=1e-13)
+    x2 = _bits(2.0 * xf)
+    out2 = orc.fused_add_rms_norm_fp8(x2, None, w, 0.0, STATIC, scale=1.0)
+    assert np.array_equal(out2["v"], out["v"])
+
+
+def check_norm_residual_add_library(orc):
+    """residual_out = bf16(x + residual): a float32 add followed by torch's RNE
+    cast gives the correctly rounded sum of two bf16 numbers; the normalised
+    row is that stored residual (plain variant run on residual_out)."""
+    rng = np.random.default_rng(4)
+    T, H = 16, 512
+    x = _rand_bf16(rng, (T, H), scale=np.exp2(rng.integers(-8, 8, (T, H))))
+    res = _rand_bf16(rng, (T, H))
+    w = _weight(rng, H)
+    out = orc.fused_add_rms_norm_fp8(x, res, w, 1e-5, PER_TOKEN)
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float()
+    rt = torch.from_numpy(res.view(np.int16)).view(torch.bfloat16).float()
+    lib = (xt + rt).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out["residual_out"], lib)
+    plain = orc.fused_add_rms_norm_fp8(out["residual_out"], None, w, 1e-5, PER_TOKEN)
+    assert np.array_equal(plain["q"], out["q"]) and np.array_equal(plain["scale"], out["scale"])
+    # a zero residual changes nothing against the plain variant
+    zero = np.zeros_like(res)
+    pz = orc.fused_add_rms_norm_fp8(x, zero, w, 1e-5, PER_TOKEN)
+    p0 = orc.fused_add_rms_norm_fp8(x, None, w, 1e-5, PER_TOKEN)
+    assert np.array_equal(pz["q"], p0["q"]) and np.array_equal(pz["v"], p0["v"])
+    assert np.array_equal(pz["residual_out"], x)
+
+
+def check_norm_brute_force(orc):
+    """Tiny random rows against exact rational arithmetic (60-digit sqrt)."""
+    rng = np.random.default_rng(5)
+    floor = orc.amax_floor()
+    for H, mode, G in ((8, STATIC, 0), (16, PER_TOKEN, 0), (16, PER_GROUP, 8),
+                       (12, PER_GROUP, 4), (1, PER_TOKEN, 0)):
+        T = 3
+        x = _rand_bf16(rng, (T, H))
+        res = _rand_bf16(rng, (T, H), scale=3.0)
+        w = _weight(rng, H)
+        s_static = 0.0625 if mode == STATIC else None
+        for residual in (res, None):
+            out = orc.fused_add_rms_norm_fp8(x, residual, w, 1e-5, mode, G or 128,
+                                             scale=s_static)
+            for t in range(T):
+                ex = exact.exact_norm_row(x[t], None if residual is None else residual[t],
+                                          w, 1e-5, mode, G, s_static, floor)
+                if residual is not None:
+                    assert list(out["residual_out"][t]) == ex["residual_out"]
+                s_row = out["scale"] if mode == STATIC else np.atleast_1d(out["scale"][t])
+                assert np.array_equal(s_row, ex["scale"]), (s_row, ex["scale"])
+                np.testing.assert_allclose(out["v"][t], [float(v) for v in ex["v"]], rtol=1e-13)
+                assert list(out["q"][t]) == ex["q"], (H, mode, t)
+
+
+# ------------------------------------------------------------- quant modes
+
+def check_per_token_max_code(orc):
+    """Dynamic per-token: every row reaches |q| = 448 (code 0x7E/0xFE), the
+    scale is fp32(amax/448), and dequantisation q*s is within half an E4M3
+    step of y."""
+    rng = np.random.default_rng(6)
+    T, H = 32, 640
+    x = _rand_bf16(rng, (T, H), scale=np.exp2(rng.integers(-6, 6, (T, 1))))
+    res = _rand_bf16(rng, (T, H))
+    w = _weight(rng, H)
+    out = orc.fused_add_rms_norm_fp8(x, res, w, 1e-5, PER_TOKEN)
+    assert np.all(np.max(out["q"] & 0x7F, axis=1) == 0x7E)
+    ref = orc.fused_add_rms_norm_fp8(x, res, w, 1e-5, STATIC, scale=1.0)
+    y = ref["v"]
+    amax = np.max(np.abs(y), axis=1)
+    np.testing.assert_allclose(out["scale"], (amax / 448.0).astype(np.float32), rtol=1e-7)
+    deq = exact.E4M3_POS_F64[out["q"] & 0x7F] * np.where(out["q"] & 0x80, -1, 1)
+    deq = deq * out["scale"][:, None]
+    step = np.maximum(np.abs(y) / 8.0, 2.0 ** -9 * out["scale"][:, None])
+    assert np.all(np.abs(deq - y) <= step * 0.5 + 1e-12 * np.abs(y))
+
+
+def check_per_group_layout(orc):
+    """Per-group: each group's scale is fp32(max|y| over its G columns / 448),
+    stored at [t, g]; every group reaches 448; G = H equals per-token; and a
+    static run with the per-token scale of each row gives the same codes."""
+    rng = np.random.default_rng(8)
+    T, H = 6, 512
+    x = _rand_bf16(rng, (T, H), scale=np.exp2(rng.integers(-4, 4, (1, H))))
+    res = _rand_bf16(rng, (T, H))
+    w = _weight(rng, H)
+    ref = orc.fused_add_rms_norm_fp8(x, res, w, 1e-5, STATIC, scale=1.0)
+    for G in (64, 128):
+        out = orc.fused_add_rms_norm_fp8(x, res, w, 1e-5, PER_GROUP, G)
+        assert out["scale"].shape == (T, H // G)
+        amax = np.max(np.abs(ref["v"]).reshape(T, H // G, G), axis=2)
+        np.testing.assert_allclose(out["scale"], (amax / 448.0).astype(np.float32), rtol=1e-7)
+        assert np.all(np.max((out["q"] & 0x7F).reshape(T, H // G, G), axis=2) == 0x7E)
+    full = orc.fused_add_rms_norm_fp8(x, res, w, 1e-5, PER_GROUP, H)
+    tok = orc.fused_add_rms_norm_fp8(x, res, w, 1e-5, PER_TOKEN)
+    assert np.array_equal(full["q"], tok["q"])
+    assert np.array_equal(full["scale"].reshape(T), tok["scale"])
+    for t in range(T):
+        st = orc.fused_add_rms_norm_fp8(x[t:t + 1], res[t:t + 1], w, 1e-5, STATIC,
+                                        scale=tok["scale"][t])
+        assert np.array_equal(st["q"][0], tok["q"][t])
+
+
+def check_zero_row_and_saturation(orc):
+    H = 256
+    w = _bits(np.ones(H))
+    z = np.zeros((2, H), np.uint16)
+    out = orc.fused_add_rms_norm_fp8(z, z, w, 1e-5, PER_TOKEN)
+    assert np.all(out["q"] == 0)
+    assert np.all(out["scale"] == np.float32(orc.amax_floor() / 448.0))
+    rng = np.random.default_rng(9)
+    x = _rand_bf16(rng, (2, H))
+    sat = orc.fused_add_rms_norm_fp8(x, None, w, 1e-5, STATIC, scale=1e-6)
+    v = sat["v"]
+    big = np.abs(v) >= 448
+    assert big.mean() > 0.9
+    assert np.all((sat["q"][big] & 0x7F) == 0x7E)
+    assert np.array_equal(sat["q"][big] >> 7, np.signbit(v[big]).astype(np.uint8))
+
+
+# ------------------------------------------------------------------ SiLU
+
+def check_silu_closed_forms(orc):
+    """silu(0) = 0; silu(g) = g for g >= 40 (e^-40 is below half an fp64 ulp);
+    silu(g) - silu(-g) = g; silu(g) -> -0 for g <= -745; silu(g)*u against
+    scipy's logistic function."""
+    from scipy.special import expit
+    I = 8
+    g = np.array([0.0, 40.0, 64.0, 1024.0, -746.0, -1024.0, 2.5, -2.5])
+    u = np.array([1.0, 1.0, 0.5, 1.0, 1.0, 1.0, 1.0, 1.0])
+    gu = _bits(np.concatenate([g, u])[None, :])
+    out = orc.silu_mul_fp8(gu, STATIC, scale=1.0)
+    v = out["v"][0]
+    assert v[0] == 0.0 and v[1] == 40.0 and v[2] == 32.0 and v[3] == 1024.0
+    assert v[4] == 0.0 and np.signbit(v[4]) and out["q"][0, 4] == 0x80
+    assert abs((v[6] - v[7]) - 2.5) <= 1e-15
+    rng = np.random.default_rng(10)
+    T, I = 4, 512
+    gate = rng.standard_normal((T, I)) * 4
+    up = rng.standard_normal((T, I))
+    gu = _bits(np.concatenate([gate, up], axis=1))
+    gf = exact.bf16_bits_to_f64(gu[:, :I])
+    uf = exact.bf16_bits_to_f64(gu[:, I:])
+    out = orc.silu_mul_fp8(gu, STATIC, scale=1.0)
+    np.testing.assert_allclose(out["v"], gf * expit(gf) * uf, rtol=1e-14, atol=1e-300)
+
+
+def check_silu_brute_force(orc):
+    rng = np.random.default_rng(12)
+    floor = orc.amax_floor()
+    for I, mode, G in ((8, STATIC, 0), (16, PER_TOKEN, 0), (16, PER_GROUP, 8)):
+        T = 3
+        gu = _rand_bf16(rng, (T, 2 * I), scale=3.0)
+        s_static = 0.1 if mode == STATIC else None
+        out = orc.silu_mul_fp8(gu, mode, G or 128, scale=s_static)
+        for t in range(T):
+            ex = exact.exact_silu_row(gu[t], mode, G, s_static, floor)
+            s_row = out["scale"] if mode == STATIC else np.atleast_1d(out["scale"][t])
+            assert np.array_equal(s_row, ex["scale"]), (s_row, ex["scale"])
+            np.testing.assert_allclose(out["v"][t], [float(v) for v in ex["v"]], rtol=1e-13)
+            assert list(out["q"][t]) == ex["q"], (I, mode, t)
+
+
+def check_silu_modes(orc):
+    """SiLU per-token rows reach 448; per-group G = I equals per-token."""
+    rng = np.random.default_rng(13)
+    T, I = 8, 256
+    gu = _rand_bf16(rng, (T, 2 * I))
+    tok = orc.silu_mul_fp8(gu, PER_TOKEN)
+    assert np.all(np.max(tok["q"] & 0x7F, axis=1) == 0x7E)
+    full = orc.silu_mul_fp8(gu, PER_GROUP, I)
+    assert np.array_equal(full["q"], tok["q"])
+    ref = orc.silu_mul_fp8(gu, STATIC, scale=1.0)
+    G = 128
+    grp = orc.silu_mul_fp8(gu, PER_GROUP, G)
+    amax = np.max(np.abs(ref["v"]).reshape(T, I // G, G), axis=2)
+    np.testing.assert_allclose(grp["scale"], (amax / 448.0).astype(np.float32), rtol=1e-7)
+
+
+ALL_CHECKS = [
+    check_e4m3_spec_points, check_e4m3_all_codes, check_e4m3_encoder_brute_force,
+    check_e4m3_special_values, check_bf16_all_patterns, check_bf16_encoder_brute_force,
+    check_norm_constant_row, check_norm_h1_closed_form, check_norm_invariants,
+    check_norm_residual_add_library, check_norm_brute_force, check_per_token_max_code,
+    check_per_group_layout, check_zero_row_and_saturation, check_silu_closed_forms,
+    check_silu_brute_force, check_silu_modes,
+]

@@ -1,0 +1,61 @@
+"""Planted mistakes in the oracle must be caught by its pins (CPU only).
+
+Each mutant is a copy of ``oracle/oracle.c`` with one plausible error (a
+dropped term, a wrong sign, index or operand, a wrong rounding rule), built
+into a temporary library; at least one pin must fail on it.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTANTS = {
+    "eps_outside_sqrt": ("sqrt(ss / (double)H + (double)eps)", "(sqrt(ss / (double)H) + (double)eps)"),
+    "sum_not_mean": ("sqrt(ss / (double)H + (double)eps)", "sqrt(ss + (double)eps)"),
+    "eps_dropped": ("sqrt(ss / (double)H + (double)eps)", "sqrt(ss / (double)H)"),
+    "weight_dropped": ("y[j] = r[j] * inv * orc_bf16_decode(weight[j]);", "y[j] = r[j] * inv;"),
+    "sum_not_rounded": ("r[j] = orc_bf16_decode(rb);", "r[j] = sum;"),
+    "residual_not_added": ("orc_bf16_decode(xt[j]) + orc_bf16_decode(residual[t * H + j])",
+                           "orc_bf16_decode(xt[j])"),
+    "scale_multiplied": ("double vj = yg[j] / s;", "double vj = yg[j] * s;"),
+    "static_scale_multiplied": ("double vj = y[j] / s;", "double vj = y[j] * s;"),
+    "amax_not_abs": ("if (fabs(yg[j]) > amax)\n                amax = fabs(yg[j]);",
+                     "if (yg[j] > amax)\n                amax = yg[j];"),
+    "fp8_max_480": ("#define ORC_E4M3_MAX 448.0", "#define ORC_E4M3_MAX 480.0"),
+    "scale_layout_transposed": ("scale[t * ngroups + g] = s32;", "scale[g * 1 + t * 1] = s32;"),
+    "ties_away_from_zero": ("return nearbyint(m) * quantum;", "return round(m) * quantum;"),
+    "truncating_rounding": ("return nearbyint(m) * quantum;", "return trunc(m) * quantum;"),
+    "no_subnormals": ("if (e < emin)\n        e = emin;", "if (e < emin)\n        return 0.0 * v;"),
+    "sign_of_zero_lost": ("if (r == 0.0)\n        return sign;", "if (r == 0.0)\n        return 0;"),
+    "silu_sign": ("a[j] = g / (1.0 + exp(-g)) * u;", "a[j] = g / (1.0 + exp(g)) * u;"),
+    "silu_gate_up_swapped": ("double g = orc_bf16_decode(row[j]);\n            double u = orc_bf16_decode(row[I + j]);",
+                             "double g = orc_bf16_decode(row[I + j]);\n            double u = orc_bf16_decode(row[j]);"),
+    "silu_up_dropped": ("a[j] = g / (1.0 + exp(-g)) * u;", "a[j] = g / (1.0 + exp(-g));"),
+    "e4m3_bias_8": ("return (uint8_t)(sign | (uint8_t)(((e + 7) << 3) | mant));",
+                    "return (uint8_t)(sign | (uint8_t)(((e + 8) << 3) | mant));"),
+    "amax_floor_dropped": ("double a = amax > orc_amax_floor() ? amax : orc_amax_floor();",
+                           "double a = amax;"),
+    "bf16_decode_shift": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mutated = tmp_path / f"oracle_{name}.c"
+    mutated.write_text(src.replace(old, new))
+    lib_path = oracle.compile_source(str(mutated), str(tmp_path / f"lib_{name}.so"))
+    orc = oracle.Oracle(oracle.load_library(lib_path))
+    caught = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(orc)
+        except Exception as exc:  # noqa: BLE001 - any failure counts as caught
+            caught.append(f"{check.__name__}: {type(exc).__name__}")
+    assert caught, f"no pin catches the planted mistake {name!r}"
