@@ -1,0 +1,130 @@
+/*
+ * vg_fused.h -- C ABI of libvg_fused.so: fused residual-add + RMSNorm -> FP8
+ * and SiLU-and-mul -> FP8 quantisation on one GB300 (sm_103a).
+ *
+ * Operations (cited by page title and section):
+ *   "Fusion torch.compile passes" (data-sketchers.com wiki, vLLM
+ *   design-fusions page), section "RMSNorm + Quantization (fuse_norm_quant)":
+ *   rms_norm(x) -> quant_fp8(y) and fused_add_rms_norm(x, residual) ->
+ *   quant_fp8(y) in one kernel, the residual updated in place, with FP8
+ *   static per-tensor, dynamic per-token and dynamic per-token-group (128/64)
+ *   scales.  Section "SiLU+Mul + Quantization (fuse_act_quant)":
+ *   silu_and_mul of the gate-up projection -> quant_fp8 in one kernel,
+ *   without materialising the post-activation tensor.  "Quick Reference"
+ *   table: both fusions apply for every num_tokens.
+ *
+ * Numerics (the pages give no formulas; these are the readings the library
+ * implements):
+ *   r   = bf16(x + residual)                       (fp32 add, RNE to bf16)
+ *   y   = r / sqrt(mean(r^2) + eps) * weight       (fp32, never rounded to bf16)
+ *   a   = gate / (1 + exp(-gate)) * up             (fp32, never rounded to bf16)
+ *   q   = e4m3(y / s)    RNE, saturating to +-448, OCP E4M3FN encoding
+ *   s   = static: the given fp32 scale
+ *         per-token: fp32(max(amax over the row, 1e-10f) / 448)
+ *         per-group: fp32(max(amax over G columns, 1e-10f) / 448)
+ *   The kernels multiply by 1/s, computed once per row or group.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library allocates nothing, keeps no per-call state, never
+ *     synchronises, and launches only on `stream` (NULL = legacy default
+ *     stream).  Calls are asynchronous and may be captured in a CUDA graph.
+ *   - bf16 tensors are passed as uint16_t bit patterns, fp8 outputs as
+ *     uint8_t E4M3 codes.  All tensors are dense and row-major.
+ *   - Every argument is validated on the host before any launch; a
+ *     validation error returns its status and launches nothing.  A launch
+ *     failure returns VG_ERR_CUDA.  num_tokens == 0 returns VG_OK without
+ *     launching.
+ *   - Alignment: every bf16 / fp8 tensor pointer must be 16-byte aligned,
+ *     `scale` 4-byte aligned.  The row length (hidden or inter) must be a
+ *     multiple of 8 and at most VG_MAX_ROW.
+ *   - Aliasing: residual_out may equal residual exactly (in-place update).
+ *     Any other overlap between an output and any other tensor is undefined.
+ *   - Device: compute capability 10.3 (GB300) only; other devices return
+ *     VG_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef VG_FUSED_H
+#define VG_FUSED_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t from cuda_runtime.h. */
+struct CUstream_st;
+typedef struct CUstream_st *vg_stream_t;
+
+#define VG_ABI_VERSION 1
+#define VG_MAX_ROW 32768 /* largest hidden / inter a row-resident kernel holds */
+
+typedef enum {
+    VG_SCALE_STATIC = 0,    /* s given: scale[0], fp32, read on the device         */
+    VG_SCALE_PER_TOKEN = 1, /* s computed per row: scale[T] written                 */
+    VG_SCALE_PER_GROUP = 2  /* s per G columns: scale[T, n/G] written, row-major    */
+} vg_scale_mode;
+
+typedef enum {
+    VG_OK = 0,
+    VG_ERR_NULL_PTR = 1,           /* a required pointer is NULL, or residual_out
+                                      and residual are not both set or both NULL  */
+    VG_ERR_BAD_SHAPE = 2,          /* num_tokens < 0, row length not a multiple
+                                      of 8, < 8, or > VG_MAX_ROW                  */
+    VG_ERR_MISALIGNED = 3,         /* a tensor pointer breaks the alignment rule */
+    VG_ERR_BAD_MODE = 4,           /* mode is not a vg_scale_mode                 */
+    VG_ERR_BAD_GROUP = 5,          /* per-group with group_size not 64 or 128, or
+                                      not dividing the row length                 */
+    VG_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 */
+    VG_ERR_CUDA = 7                /* a CUDA runtime call or launch failed        */
+} vg_status;
+
+/*
+ * Residual add + RMSNorm -> FP8 ("RMSNorm + Quantization (fuse_norm_quant)").
+ *
+ *   q            out  uint8  [T, H]  E4M3 codes of y / s
+ *   residual_out out  uint16 [T, H]  bf16 r = bf16(x + residual); may equal
+ *                                    `residual` (in place).  NULL iff residual
+ *                                    is NULL.
+ *   scale        STATIC: in fp32 [1]; PER_TOKEN: out fp32 [T];
+ *                PER_GROUP: out fp32 [T, H / group_size]
+ *   x            in   uint16 [T, H]  bf16
+ *   residual     in   uint16 [T, H]  bf16, or NULL for the plain
+ *                                    rms_norm(x) -> quant_fp8 variant (r = x)
+ *   weight       in   uint16 [H]     bf16
+ *   num_tokens T >= 0; hidden H: multiple of 8, 8 <= H <= VG_MAX_ROW
+ *   eps          added to mean(r^2) inside the square root
+ *   mode         vg_scale_mode; group_size 64 or 128 (PER_GROUP only,
+ *                ignored otherwise)
+ */
+vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *scale,
+                                    const uint16_t *x, const uint16_t *residual,
+                                    const uint16_t *weight, int64_t num_tokens,
+                                    int64_t hidden, float eps, int32_t mode,
+                                    int32_t group_size, vg_stream_t stream);
+
+/*
+ * SiLU(gate) * up -> FP8 ("SiLU+Mul + Quantization (fuse_act_quant)").
+ *
+ *   q        out uint8  [T, I]  E4M3 codes of a / s
+ *   scale    STATIC: in fp32 [1]; PER_TOKEN: out fp32 [T];
+ *            PER_GROUP: out fp32 [T, I / group_size]
+ *   gate_up  in  uint16 [T, 2I] bf16: gate = columns [0, I), up = [I, 2I)
+ *   num_tokens T >= 0; inter I: multiple of 8, 8 <= I <= VG_MAX_ROW
+ *   mode, group_size as above.  SiLU has no epsilon, so there is none here.
+ */
+vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up,
+                          int64_t num_tokens, int64_t inter, int32_t mode,
+                          int32_t group_size, vg_stream_t stream);
+
+/* Static English text for a status code (never NULL). */
+const char *vg_status_string(vg_status status);
+
+/* VG_ABI_VERSION of the library that is loaded. */
+int32_t vg_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VG_FUSED_H */

@@ -1,0 +1,198 @@
+"""Fused residual-add + RMSNorm -> FP8 and SiLU-and-mul -> FP8 on GB300.
+
+Thin Python binding over the C ABI of ``libvg_fused.so`` (declared in
+``include/vg_fused.h``).  Every step of both ops runs in the library's CUDA
+kernels; this module only marshals arguments: it checks dtypes, devices and
+contiguity of torch tensors, passes their device pointers and the current
+CUDA stream, and turns a non-zero status into ``VgError``.  There is no CPU
+fallback: if the library has not been built, every call raises.
+
+Entry points (same names and argument order as the C ABI):
+  vg_fused_add_rms_norm_fp8(q, residual_out, scale, x, residual, weight,
+                            eps, mode, group_size=128, stream=None)
+  vg_silu_mul_fp8(q, scale, gate_up, mode, group_size=128, stream=None)
+Convenience wrappers that allocate the outputs with torch:
+  fused_add_rms_norm_fp8(x, residual, weight, eps, mode, ...)
+  silu_mul_fp8(gate_up, mode, ...)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
+MAX_ROW = 32768
+
+STATUS_NAMES = {
+    0: "VG_OK", 1: "VG_ERR_NULL_PTR", 2: "VG_ERR_BAD_SHAPE", 3: "VG_ERR_MISALIGNED",
+    4: "VG_ERR_BAD_MODE", 5: "VG_ERR_BAD_GROUP", 6: "VG_ERR_UNSUPPORTED_DEVICE", 7: "VG_ERR_CUDA",
+}
+
+EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_status_string",
+                    "vg_abi_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class VgError(RuntimeError):
+    """A non-zero vg_status returned by the library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (built by ``build.build()``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or os.environ.get("VG_FUSED_LIB", LIB_PATH)
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"CUDA library {p} is missing: build it with "
+                "`python -m norm_activation_fp8_gb300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(p)
+        P, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        lib.vg_fused_add_rms_norm_fp8.argtypes = [P, P, P, P, P, P, i64, i64, ctypes.c_float,
+                                                  i32, i32, P]
+        lib.vg_fused_add_rms_norm_fp8.restype = ctypes.c_int
+        lib.vg_silu_mul_fp8.argtypes = [P, P, P, i64, i64, i32, i32, P]
+        lib.vg_silu_mul_fp8.restype = ctypes.c_int
+        lib.vg_status_string.argtypes = [ctypes.c_int]
+        lib.vg_status_string.restype = ctypes.c_char_p
+        lib.vg_abi_version.argtypes = []
+        lib.vg_abi_version.restype = i32
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().vg_status_string(status).decode()
+
+
+def _check(status: int):
+    if status != 0:
+        raise VgError(status, status_string(status))
+
+
+# ----------------------------------------------------------- marshalling
+
+def _ptr(t, dtypes, name):
+    """Device pointer of a torch tensor (or pass an int pointer / None)."""
+    if t is None or isinstance(t, int):
+        return t
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, an int pointer or None")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (there is no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtypes():
+    import torch
+    bf16 = (torch.bfloat16, torch.int16, torch.uint16)
+    fp8 = (torch.float8_e4m3fn, torch.uint8, torch.int8)
+    return bf16, fp8, (torch.float32,)
+
+
+def _rows(t, name):
+    if isinstance(t, int) or t is None:
+        raise ValueError(f"{name}: shapes cannot be taken from a raw pointer; pass num_tokens")
+    if t.dim() != 2:
+        raise ValueError(f"{name}: expected a 2-D [T, n] tensor")
+    return t.shape[0], t.shape[1]
+
+
+def vg_fused_add_rms_norm_fp8(q, residual_out, scale, x, residual, weight, eps: float,
+                              mode: int, group_size: int = 128, stream=None,
+                              num_tokens: int | None = None, hidden: int | None = None):
+    """Residual add + RMSNorm -> FP8 through the C ABI (outputs preallocated).
+
+    q [T,H] fp8/uint8; residual_out [T,H] bf16 (may be ``residual`` itself)
+    or None with residual None; scale fp32 ([1] static input, [T] or
+    [T,H/G] output); x [T,H] bf16; residual [T,H] bf16 or None; weight [H]."""
+    bf16, fp8, f32 = _dtypes()
+    if num_tokens is None or hidden is None:
+        num_tokens, hidden = _rows(x, "x")
+    st = load().vg_fused_add_rms_norm_fp8(
+        _ptr(q, fp8, "q"), _ptr(residual_out, bf16, "residual_out"), _ptr(scale, f32, "scale"),
+        _ptr(x, bf16, "x"), _ptr(residual, bf16, "residual"), _ptr(weight, bf16, "weight"),
+        num_tokens, hidden, ctypes.c_float(eps), mode, group_size, _stream(stream))
+    _check(st)
+
+
+def vg_silu_mul_fp8(q, scale, gate_up, mode: int, group_size: int = 128, stream=None,
+                    num_tokens: int | None = None, inter: int | None = None):
+    """SiLU(gate) * up -> FP8 through the C ABI (outputs preallocated).
+
+    q [T,I] fp8/uint8; scale fp32 ([1] static input, [T] or [T,I/G]
+    output); gate_up [T,2I] bf16 with gate = columns [0,I), up = [I,2I)."""
+    bf16, fp8, f32 = _dtypes()
+    if num_tokens is None or inter is None:
+        num_tokens, two_i = _rows(gate_up, "gate_up")
+        if two_i % 2:
+            raise ValueError("gate_up must have an even number of columns")
+        inter = two_i // 2
+    st = load().vg_silu_mul_fp8(_ptr(q, fp8, "q"), _ptr(scale, f32, "scale"),
+                                _ptr(gate_up, bf16, "gate_up"), num_tokens, inter, mode,
+                                group_size, _stream(stream))
+    _check(st)
+
+
+# ------------------------------------------------- allocating wrappers
+
+def _scale_out(mode, T, n, group_size, scale, device):
+    import torch
+    if mode == STATIC:
+        if scale is None:
+            raise ValueError("static mode needs a scale tensor")
+        return scale
+    if mode == PER_TOKEN:
+        return torch.empty((T,), dtype=torch.float32, device=device)
+    return torch.empty((T, n // group_size), dtype=torch.float32, device=device)
+
+
+def fused_add_rms_norm_fp8(x, residual, weight, eps: float, mode: int, group_size: int = 128,
+                           scale=None, inplace: bool = True, stream=None):
+    """Returns (q float8_e4m3fn [T,H], scale, residual_out).  With
+    ``inplace`` the residual is updated in place, as the fused op does."""
+    import torch
+    T, H = x.shape
+    q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device=x.device)
+    s = _scale_out(mode, T, H, group_size, scale, x.device)
+    r_out = None
+    if residual is not None:
+        r_out = residual if inplace else torch.empty_like(residual)
+    vg_fused_add_rms_norm_fp8(q, r_out, s, x, residual, weight, eps, mode, group_size, stream)
+    return q, s, r_out
+
+
+def silu_mul_fp8(gate_up, mode: int, group_size: int = 128, scale=None, stream=None):
+    """Returns (q float8_e4m3fn [T,I], scale)."""
+    import torch
+    T, two_i = gate_up.shape
+    q = torch.empty((T, two_i // 2), dtype=torch.float8_e4m3fn, device=gate_up.device)
+    s = _scale_out(mode, T, two_i // 2, group_size, scale, gate_up.device)
+    vg_silu_mul_fp8(q, s, gate_up, mode, group_size, stream)
+    return q, s

@@ -1,0 +1,118 @@
+// common.cuh -- device helpers shared by the fused norm / SiLU -> FP8 kernels.
+//
+// bf16 pairs travel packed in 32-bit words (element 0 in the low half), fp8
+// codes packed four to a word (element 0 in the lowest byte), so every global
+// access is a 16-byte (inputs) or 8-byte (fp8 outputs) vector.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace vg {
+
+constexpr float kE4M3Max = 448.0f;   // largest finite OCP E4M3FN value
+constexpr float kAmaxFloor = 1e-10f; // floor on a dynamic amax (no 0/0 on zero rows)
+constexpr int kElemsPerChunk = 8;    // bf16 elements per 16-byte vector
+
+enum ScaleMode : int { kStatic = 0, kPerToken = 1, kPerGroup = 2 };
+
+// ------------------------------------------------------------------ bf16
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round two fp32 values to bf16 (RNE) and pack them, `lo` in the low half.
+// cvt...bf16x2.f32 d, a, b puts a in the upper half and b in the lower half.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// ------------------------------------------------------------------ fp8
+
+// Two fp32 -> two E4M3 codes, RNE with saturation to +-448 (NaN -> 0x7F),
+// `lo` in the low byte.  Same operand order rule as the bf16x2 form.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// Eight fp32 -> eight E4M3 codes packed into 8 bytes, element 0 first.
+__device__ __forceinline__ uint2 quant8(const float (&v)[8]) {
+  uint2 o;
+  o.x = cvt_e4m3x2(v[0], v[1]) | (cvt_e4m3x2(v[2], v[3]) << 16);
+  o.y = cvt_e4m3x2(v[4], v[5]) | (cvt_e4m3x2(v[6], v[7]) << 16);
+  return o;
+}
+
+// -------------------------------------------------------------- memory ops
+
+// Read-only data streamed once: non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream_ro(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Data streamed once that this kernel may also overwrite (the residual when
+// updated in place): coherent load, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Read-only data shared by every row (the RMSNorm weight): keep it cached.
+__device__ __forceinline__ uint4 ld_keep(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::evict_last.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Outputs written once: streaming stores (evict-first in L2).
+__device__ __forceinline__ void st_stream(void *p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_stream(void *p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// --------------------------------------------------------------- reductions
+
+// Butterfly reductions: every participating lane ends with the bit-identical
+// result (each level combines the same two operands on both partners).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Max over aligned sets of `width` lanes (width a power of two <= 32).
+__device__ __forceinline__ float lanes_max(float v, int width) {
+  for (int o = width >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+// Dequantisation scale of a dynamic row or group: fp32(max(amax, floor)/448).
+__device__ __forceinline__ float dynamic_scale(float amax) {
+  return fmaxf(amax, kAmaxFloor) / kE4M3Max;
+}
+
+}  // namespace vg

@@ -1,0 +1,58 @@
+// launch.h -- internal (non-ABI) declarations shared by the library's .cu files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace vg {
+
+// How a row-wise kernel covers a [T, n] tensor: each row is split into
+// nch = n/8 chunks of 16 bytes; `ntr` threads (a multiple of 32) own a row,
+// thread i holding chunks i, i + ntr, ..., i + (vpt-1)*ntr; a CTA carries
+// `rpc` rows, so it has ntr * rpc threads.
+struct RowPlan {
+  int vpt;
+  int ntr;
+  int rpc;
+  int64_t grid;
+  int block() const { return ntr * rpc; }
+};
+
+// Picks the plan for nch chunks per row (nch <= 4096).
+RowPlan plan_rows(int64_t T, int nch);
+
+struct NormArgs {
+  uint8_t *q;
+  uint16_t *res_out;
+  float *scale;
+  const uint16_t *x;
+  const uint16_t *res;
+  const uint16_t *w;
+  int64_t T;
+  int32_t H;
+  int32_t nch;     // H / 8
+  int32_t ntr;     // threads per row
+  int32_t rpc;     // rows per CTA
+  int32_t gch;     // chunks per scale group (G / 8), per-group mode only
+  int32_t ngroups; // H / G, per-group mode only
+  float eps;
+  float inv_h;     // 1 / H
+};
+
+struct SiluArgs {
+  uint8_t *q;
+  float *scale;
+  const uint16_t *gate_up;
+  int64_t T;
+  int32_t I;
+  int32_t nch;
+  int32_t ntr;
+  int32_t rpc;
+  int32_t gch;
+  int32_t ngroups;
+};
+
+cudaError_t launch_norm_fp8(NormArgs a, int mode, const RowPlan &plan, cudaStream_t stream);
+cudaError_t launch_silu_fp8(SiluArgs a, int mode, const RowPlan &plan, cudaStream_t stream);
+
+}  // namespace vg

@@ -1,0 +1,147 @@
+// silu_fp8.cu -- SiLU(gate) * up -> FP8 e4m3, one pass over HBM.
+//
+// Implements "SiLU+Mul + Quantization (fuse_act_quant)" of the "Fusion
+// torch.compile passes" page: silu_and_mul of the gate-up projection
+// followed by quant_fp8, in one kernel, without materialising the
+// post-activation tensor.
+//
+// Row layout: gate_up[t] = [gate (I) | up (I)].  A thread owns the same
+// chunk index c in both halves, so its 16-byte loads of gate and up are both
+// coalesced across the warp.  a = g * sigmoid(g) * u in fp32:
+//   sigmoid(g) = rcp(1 + __expf(-g))   (rcp.approx: 1 ulp; a huge
+//                denominator flushes the reciprocal to +0 and the product
+//                keeps the sign of g, as the exact -0 would)
+// Static and per-group modes need no row-wide reduction: each chunk is
+// quantised and stored as soon as its group's amax (a butterfly over 8 or 16
+// lanes) is known.  Per-token keeps the row's activations in registers until
+// the row amax is reduced.
+#include "common.cuh"
+#include "launch.h"
+
+namespace vg {
+namespace {
+
+__device__ __forceinline__ float fast_rcp(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g * fast_rcp(1.0f + __expf(-g)) * u;
+}
+
+__device__ __forceinline__ void silu_chunk(const uint4 &gv, const uint4 &uv, float (&v)[8]) {
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = silu_mul(bf16_lo(gw[i]), bf16_lo(uw[i]));
+    v[2 * i + 1] = silu_mul(bf16_hi(gw[i]), bf16_hi(uw[i]));
+  }
+}
+
+__device__ __forceinline__ float amax8(const float (&v)[8]) {
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
+template <int VPT, int MODE>
+__global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
+  __shared__ float red[16];
+
+  const int tid = threadIdx.x;
+  const int slot = tid / a.ntr;
+  const int lr = tid - slot * a.ntr;
+  const int64_t row = (int64_t)blockIdx.x * a.rpc + slot;
+  const bool live = row < a.T;
+  const int64_t in_base = live ? row * 2 * a.I : 0;
+  const int64_t out_base = live ? row * a.I : 0;
+
+  uint4 gv[VPT], uv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int c = lr + k * a.ntr;
+    if (live && c < a.nch) {
+      gv[k] = ld_stream_ro(a.gate_up + in_base + c * kElemsPerChunk);
+      uv[k] = ld_stream_ro(a.gate_up + in_base + a.I + c * kElemsPerChunk);
+    } else {
+      gv[k] = make_uint4(0, 0, 0, 0);
+      uv[k] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  if (MODE != kPerToken) {
+    const float inv_static = (MODE == kStatic) ? __frcp_rn(__ldg(a.scale)) : 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int c = lr + k * a.ntr;
+      float v[8];
+      silu_chunk(gv[k], uv[k], v);
+      float m = inv_static;
+      if (MODE == kPerGroup) {
+        const float s = dynamic_scale(lanes_max(amax8(v), a.gch));
+        if (live && c < a.nch && (c % a.gch) == 0) a.scale[row * a.ngroups + c / a.gch] = s;
+        m = __frcp_rn(s);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] *= m;
+      if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
+    }
+    return;
+  }
+
+  // Per-token: activations stay in registers until the row amax is known.
+  float act[VPT][8];
+  float am = 0.f;
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    silu_chunk(gv[k], uv[k], act[k]);
+    am = fmaxf(am, amax8(act[k]));
+  }
+  am = warp_max(am);
+  if (a.ntr > 32) {
+    const int nw = a.ntr >> 5;
+    if ((lr & 31) == 0) red[slot * nw + (lr >> 5)] = am;
+    __syncthreads();
+    am = 0.f;
+    for (int i = 0; i < nw; ++i) am = fmaxf(am, red[slot * nw + i]);
+  }
+  const float s = dynamic_scale(am);
+  if (live && lr == 0) a.scale[row] = s;
+  const float m = __frcp_rn(s);
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int c = lr + k * a.ntr;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) act[k][i] *= m;
+    if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(act[k]));
+  }
+}
+
+template <int VPT>
+cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStream_t s) {
+  switch (mode) {
+    case kStatic: silu_fp8_kernel<VPT, kStatic><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
+    case kPerToken: silu_fp8_kernel<VPT, kPerToken><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
+    default: silu_fp8_kernel<VPT, kPerGroup><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_silu_fp8(SiluArgs a, int mode, const RowPlan &p, cudaStream_t s) {
+  a.ntr = p.ntr;
+  a.rpc = p.rpc;
+  switch (p.vpt) {
+    case 1: return launch_mode<1>(a, mode, p, s);
+    case 2: return launch_mode<2>(a, mode, p, s);
+    case 4: return launch_mode<4>(a, mode, p, s);
+    default: return launch_mode<8>(a, mode, p, s);
+  }
+}
+
+}  // namespace vg

@@ -1,0 +1,144 @@
+// vg_fused.cu -- the C ABI declared in include/vg_fused.h.
+//
+// Host side only: validates every argument before launching anything,
+// checks the device once per device, picks a row plan from the shape and
+// launches on the caller's stream.  No allocation, no synchronisation, no
+// per-call state, so every call can be captured in a CUDA graph.
+#include <atomic>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "vg_fused.h"
+
+namespace vg {
+namespace {
+
+constexpr int kMaxDevices = 64;
+// 0 = not checked yet, 1 = supported (cc 10.3), 2 = unsupported.
+std::atomic<int> g_device_state[kMaxDevices];
+
+vg_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VG_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return VG_ERR_UNSUPPORTED_DEVICE;
+  int st = g_device_state[dev].load(std::memory_order_relaxed);
+  if (st == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return VG_ERR_CUDA;
+    st = (major == 10 && minor == 3) ? 1 : 2;
+    g_device_state[dev].store(st, std::memory_order_relaxed);
+  }
+  return st == 1 ? VG_OK : VG_ERR_UNSUPPORTED_DEVICE;
+}
+
+inline bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
+
+vg_status check_row(int64_t num_tokens, int64_t n, int32_t mode, int32_t group_size) {
+  if (mode != VG_SCALE_STATIC && mode != VG_SCALE_PER_TOKEN && mode != VG_SCALE_PER_GROUP)
+    return VG_ERR_BAD_MODE;
+  if (num_tokens < 0 || num_tokens > INT32_MAX || n < 8 || n % 8 != 0 || n > VG_MAX_ROW)
+    return VG_ERR_BAD_SHAPE;
+  if (mode == VG_SCALE_PER_GROUP && ((group_size != 64 && group_size != 128) || n % group_size != 0))
+    return VG_ERR_BAD_GROUP;
+  return VG_OK;
+}
+
+}  // namespace
+
+RowPlan plan_rows(int64_t T, int nch) {
+  RowPlan p;
+  if (nch <= 128) {  // one warp per row, eight rows per CTA
+    p.ntr = 32;
+    p.vpt = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
+    p.rpc = 8;
+  } else {
+    p.vpt = nch <= 1024 ? 2 : (nch <= 2048 ? 4 : 8);
+    const int per = (nch + p.vpt - 1) / p.vpt;
+    p.ntr = (per + 31) / 32 * 32;
+    p.rpc = p.ntr <= 128 ? 2 : 1;
+  }
+  p.grid = (T + p.rpc - 1) / p.rpc;
+  return p;
+}
+
+}  // namespace vg
+
+extern "C" {
+
+vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *scale,
+                                    const uint16_t *x, const uint16_t *residual,
+                                    const uint16_t *weight, int64_t num_tokens, int64_t hidden,
+                                    float eps, int32_t mode, int32_t group_size,
+                                    vg_stream_t stream) {
+  vg_status st = vg::check_row(num_tokens, hidden, mode, group_size);
+  if (st != VG_OK || num_tokens == 0) return st;
+  if (!q || !scale || !x || !weight || ((residual == nullptr) != (residual_out == nullptr)))
+    return VG_ERR_NULL_PTR;
+  if (vg::misaligned(q, 16) || vg::misaligned(x, 16) || vg::misaligned(weight, 16) ||
+      vg::misaligned(residual, 16) || vg::misaligned(residual_out, 16) || vg::misaligned(scale, 4))
+    return VG_ERR_MISALIGNED;
+  if ((st = vg::check_device()) != VG_OK) return st;
+
+  vg::NormArgs a{};
+  a.q = q;
+  a.res_out = residual_out;
+  a.scale = scale;
+  a.x = x;
+  a.res = residual;
+  a.w = weight;
+  a.T = num_tokens;
+  a.H = (int32_t)hidden;
+  a.nch = (int32_t)(hidden / 8);
+  a.gch = mode == VG_SCALE_PER_GROUP ? group_size / 8 : 1;
+  a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(hidden / group_size) : 1;
+  a.eps = eps;
+  a.inv_h = 1.0f / (float)hidden;
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch);
+  return vg::launch_norm_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
+                                                                                   : VG_ERR_CUDA;
+}
+
+vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int64_t num_tokens,
+                          int64_t inter, int32_t mode, int32_t group_size, vg_stream_t stream) {
+  vg_status st = vg::check_row(num_tokens, inter, mode, group_size);
+  if (st != VG_OK || num_tokens == 0) return st;
+  if (!q || !scale || !gate_up) return VG_ERR_NULL_PTR;
+  if (vg::misaligned(q, 16) || vg::misaligned(gate_up, 16) || vg::misaligned(scale, 4))
+    return VG_ERR_MISALIGNED;
+  if ((st = vg::check_device()) != VG_OK) return st;
+
+  vg::SiluArgs a{};
+  a.q = q;
+  a.scale = scale;
+  a.gate_up = gate_up;
+  a.T = num_tokens;
+  a.I = (int32_t)inter;
+  a.nch = (int32_t)(inter / 8);
+  a.gch = mode == VG_SCALE_PER_GROUP ? group_size / 8 : 1;
+  a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(inter / group_size) : 1;
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch);
+  return vg::launch_silu_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
+                                                                                 : VG_ERR_CUDA;
+}
+
+const char *vg_status_string(vg_status s) {
+  switch (s) {
+    case VG_OK: return "ok";
+    case VG_ERR_NULL_PTR: return "a required pointer is NULL (or residual/residual_out not paired)";
+    case VG_ERR_BAD_SHAPE: return "bad shape: num_tokens < 0 or row length not a multiple of 8 in [8, VG_MAX_ROW]";
+    case VG_ERR_MISALIGNED: return "misaligned pointer: tensors need 16-byte, scale 4-byte alignment";
+    case VG_ERR_BAD_MODE: return "unknown scale mode";
+    case VG_ERR_BAD_GROUP: return "per-group mode needs group_size 64 or 128 dividing the row length";
+    case VG_ERR_UNSUPPORTED_DEVICE: return "current device is not compute capability 10.3 (GB300)";
+    case VG_ERR_CUDA: return "CUDA runtime or launch error";
+  }
+  return "unknown status";
+}
+
+int32_t vg_abi_version(void) { return VG_ABI_VERSION; }
+
+}  // extern "C"

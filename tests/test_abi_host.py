@@ -1,0 +1,128 @@
+"""The C-ABI library on the host (no GPU): it loads, exports every symbol the
+headers declare, and rejects bad arguments before making any CUDA call.
+
+Every call here returns from host-side validation (or from num_tokens == 0)
+before the library touches the CUDA runtime, so fake pointers are safe."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import norm_activation_fp8_gb300 as vg
+from norm_activation_fp8_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, NULL, SHAPE, ALIGN, MODE, GROUP = 0, 1, 2, 3, 4, 5
+A = 0x10000  # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return vg.load()
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(vg_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert {"vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8"} <= names
+    assert names == set(vg.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(vg_\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+    assert lib.vg_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.vg_status_string(s)
+    assert lib.vg_status_string(0) == b"ok"
+
+
+def norm(lib, q=A, r_out=A, scale=A, x=A, res=A, w=A, T=4, H=1024, eps=1e-5, mode=0, G=128):
+    return lib.vg_fused_add_rms_norm_fp8(q, r_out, scale, x, res, w, T, H, ctypes.c_float(eps),
+                                         mode, G, None)
+
+
+def silu(lib, q=A, scale=A, gu=A, T=4, I=1024, mode=0, G=128):
+    return lib.vg_silu_mul_fp8(q, scale, gu, T, I, mode, G, None)
+
+
+@pytest.mark.parametrize("fn", [norm, silu])
+def test_bad_mode(lib, fn):
+    assert fn(lib, mode=3) == MODE
+    assert fn(lib, mode=-1) == MODE
+
+
+@pytest.mark.parametrize("fn,key", [(norm, "H"), (silu, "I")])
+def test_bad_shape(lib, fn, key):
+    for n in (0, 4, 12, 1030, 32776, 65536):
+        assert fn(lib, **{key: n}) == SHAPE, n
+    assert fn(lib, T=-1) == SHAPE
+    assert fn(lib, T=2 ** 31) == SHAPE
+
+
+@pytest.mark.parametrize("fn,key", [(norm, "H"), (silu, "I")])
+def test_bad_group(lib, fn, key):
+    assert fn(lib, mode=2, G=32) == GROUP
+    assert fn(lib, mode=2, G=256) == GROUP
+    assert fn(lib, mode=2, G=0) == GROUP
+    assert fn(lib, mode=2, G=128, **{key: 1088}) == GROUP  # 1088 = 8.5 * 128
+    # group_size is ignored outside per-group mode (T = 0 stops before launch)
+    assert fn(lib, mode=0, G=7, T=0) == OK
+
+
+@pytest.mark.parametrize("fn", [norm, silu])
+def test_zero_tokens_is_ok_without_pointers(lib, fn):
+    if fn is norm:
+        assert norm(lib, q=None, r_out=None, scale=None, x=None, res=None, w=None, T=0) == OK
+    else:
+        assert silu(lib, q=None, scale=None, gu=None, T=0) == OK
+
+
+def test_null_pointers(lib):
+    for k in ("q", "scale", "x", "w"):
+        assert norm(lib, **{k: None}) == NULL, k
+    assert norm(lib, res=None) == NULL          # residual_out without residual
+    assert norm(lib, r_out=None) == NULL        # residual without residual_out
+    for k in ("q", "scale", "gu"):
+        assert silu(lib, **{k: None}) == NULL, k
+
+
+def test_misaligned(lib):
+    for k in ("q", "r_out", "x", "res", "w"):
+        assert norm(lib, **{k: A + 8}) == ALIGN, k
+    assert norm(lib, scale=A + 2) == ALIGN
+    assert silu(lib, q=A + 4) == ALIGN
+    assert silu(lib, gu=A + 8) == ALIGN
+    assert silu(lib, scale=A + 1) == ALIGN
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        vg.vg_silu_mul_fp8(torch.zeros(2, 32, dtype=torch.uint8), torch.ones(1), x, 0)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        vg.load(str(tmp_path / "absent.so"))

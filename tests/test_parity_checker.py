@@ -1,0 +1,88 @@
+"""The tolerance checker accepts exactly what the tolerance allows (CPU)."""
+import numpy as np
+import pytest
+
+import oracle
+import parity
+
+
+def _case(n=20000, seed=0):
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal(n) * 50
+    return v, oracle.e4m3_encode(v)
+
+
+def test_identical_codes_pass():
+    v, q = _case()
+    assert parity.compare_codes(q, q, v)["mismatch"] == 0
+
+
+def test_near_midpoint_flip_passes():
+    v, q = _case()
+    g = q.copy()
+    # a value sitting just above the midpoint of codes 0x50 and 0x51
+    lo, hi = oracle.e4m3_decode(np.array([0x50, 0x51], np.uint8))
+    v[0] = (lo + hi) / 2 * (1 + 1e-7)
+    q[0] = 0x51
+    g[0] = 0x50
+    st = parity.compare_codes(g, q, v)
+    assert st["flips"] == 1 and st["max_flip_rel_dist"] < 1e-6
+
+
+def test_flip_far_from_midpoint_fails():
+    v, q = _case()
+    g = q.copy()
+    k = int(np.flatnonzero((q & 0x7F) > 0x20)[0])
+    g[k] = q[k] + 1 if (q[k] & 0x7F) < 0x7E else q[k] - 1
+    with pytest.raises(parity.ParityError, match="outside tolerance"):
+        parity.compare_codes(g, q, v)
+
+
+def test_non_adjacent_or_sign_flip_fails():
+    v, q = _case()
+    lo, hi = oracle.e4m3_decode(np.array([0x50, 0x51], np.uint8))
+    v[0] = (lo + hi) / 2
+    q[0] = 0x51
+    for bad in (0x4F, 0xD1, 0xD0):
+        g = q.copy()
+        g[0] = bad
+        with pytest.raises(parity.ParityError):
+            parity.compare_codes(g, q, v)
+
+
+def test_saturated_values_must_agree():
+    v, q = _case()
+    v[0], q[0] = 1000.0, 0x7E
+    g = q.copy()
+    g[0] = 0x7D
+    with pytest.raises(parity.ParityError):
+        parity.compare_codes(g, q, v)
+
+
+def test_too_many_flips_fail():
+    n = 20000
+    lo, hi = oracle.e4m3_decode(np.array([0x50, 0x51], np.uint8))
+    v = np.full(n, (lo + hi) / 2 * (1 + 1e-7))
+    q = np.full(n, 0x51, np.uint8)
+    g = q.copy()
+    g[:2] = 0x50            # 2 flips = 0.01 % of 20000: allowed
+    parity.compare_codes(g, q, v)
+    g[:3] = 0x50            # 3 flips: over the budget
+    with pytest.raises(parity.ParityError, match="near-midpoint flips"):
+        parity.compare_codes(g, q, v)
+
+
+def test_scale_tolerance():
+    s = np.array([1.0, 2.5e-3, 7.0], np.float32)
+    parity.compare_scales(s * np.float32(1 + 5e-7), s)
+    with pytest.raises(parity.ParityError):
+        parity.compare_scales(s * np.float32(1 + 3e-6), s)
+
+
+def test_residual_bit_exact():
+    a = np.arange(10, dtype=np.uint16)
+    parity.compare_exact(a, a.copy(), "residual_out")
+    b = a.copy()
+    b[3] ^= 1
+    with pytest.raises(parity.ParityError):
+        parity.compare_exact(b, a, "residual_out")
