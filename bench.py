@@ -13,10 +13,14 @@ Timing (device, CUDA events on the launching stream):
     input and output) rotate so that R * bytes >= 3 x L2 and no step reads
     data left in L2 by the previous use of its set;
   * the K timed steps are captured once into a CUDA graph (launch cost
-    hidden) with an external event node before and after every kernel, so
-    the per-kernel durations for the roofline come from the timed region;
-  * the timed region is one replay bracketed by a barrier and a
-    torch.cuda.synchronize() on both sides; max over ranks.
+    hidden); the timed region is one replay bracketed by a barrier and a
+    torch.cuda.synchronize() on both sides; max over ranks;
+  * the roofline's per-kernel duration: each op's K launches, over the same
+    rotation of buffer sets, captured in a graph of their own and replayed
+    right after the timed region (event nodes inside a graph would add
+    microseconds per kernel);
+  * clocks are sampled by nvidia-smi over a window of untimed replays of the
+    same graph just before the timed one, through the per-kernel replays.
 e2e repeats the step through the C ABI from pinned HOST buffers: every step
 copies its inputs host->device and reads every output back device->host.
 --impl reference times the fp64 CPU oracle on the host cores instead.
@@ -298,25 +302,21 @@ def run_gpu(args, dist):
                 launch(vg, op)
     torch.cuda.synchronize()
 
-    # K timed steps captured into one graph, with event nodes around kernels
+    # The K timed steps captured once into one graph (hides launch cost).
     nk = len(step)
-    try:
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nk + 1)]
-               for _ in range(args.steps)]
-        in_graph_events = True
-    except TypeError:
-        evs = None
-        in_graph_events = False
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for k in range(args.steps):
-            ops = sets[(args.warmup + k) % n_sets].ops
-            for i, op in enumerate(ops):
-                if in_graph_events:
-                    evs[k][i].record()
+            for op in sets[(args.warmup + k) % n_sets].ops:
                 launch(vg, op)
-            if in_graph_events:
-                evs[k][nk].record()
+    # Per-kernel graphs: the same K launches of one op, for its duration.
+    op_graphs = []
+    for i in range(nk):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(args.steps):
+                launch(vg, sets[(args.warmup + k) % n_sets].ops[i])
+        op_graphs.append(g)
     torch.cuda.synchronize()
 
     clocks = ClockSampler(dist.local)
@@ -336,28 +336,19 @@ def run_gpu(args, dist):
         end.record()
     torch.cuda.synchronize()
     dist.barrier()
-    clk = clocks.stop()
     ms_local = start.elapsed_time(end)
     ms = dist.max(ms_local)
 
     per_kernel = {}
-    if in_graph_events:
-        for i, w in enumerate(step):
-            d = [evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps)]
-            per_kernel[w.name] = sum(d) / len(d)
-    else:  # kernel-only graphs of the same launches, timed right after
-        for i, w in enumerate(step):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for k in range(args.steps):
-                    launch(vg, sets[(args.warmup + k) % n_sets].ops[i])
-            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                s0.record()
-                g.replay()
-                s1.record()
-            torch.cuda.synchronize()
-            per_kernel[w.name] = s0.elapsed_time(s1) / args.steps
+    for w, g in zip(step, op_graphs):
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s0.record()
+            g.replay()
+            s1.record()
+        torch.cuda.synchronize()
+        per_kernel[w.name] = s0.elapsed_time(s1) / args.steps
+    clk = clocks.stop()
 
     total_bytes = nbytes * args.steps * dist.world
     value = total_bytes / (ms * 1e-3) / 1e9
@@ -392,7 +383,8 @@ def run_gpu(args, dist):
                   f"(>= 3x L2 of {l2 / 2**20:.0f} MiB)",
             "timing": "K steps in one CUDA graph replay, CUDA events on the launching stream",
             "per_kernel_ms": {k: round(v, 6) for k, v in per_kernel.items()},
-            "per_kernel_events": "in-graph" if in_graph_events else "kernel-only graphs",
+            "per_kernel_timing": "each op's K launches (same buffer rotation) in its own graph, "
+                                 "replayed right after the timed region",
             "parallelism": f"replicas x{dist.world} (rows sharded, no collective)",
             "gpu": props.name, "sms": props.multi_processor_count,
             "torch": torch.__version__,

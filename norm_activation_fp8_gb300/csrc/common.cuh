@@ -115,4 +115,91 @@ __device__ __forceinline__ float dynamic_scale(float amax) {
   return fmaxf(amax, kAmaxFloor) / kE4M3Max;
 }
 
+// ------------------------------------------------ double-float arithmetic
+//
+// The dynamic-scale path needs the row's 1/sqrt(mean(r^2) + eps) to ~2^-44
+// (fp64 is far too slow on this part), so it is carried as an unevaluated
+// sum hi + lo of two fp32 numbers.
+
+// hi + lo += x with the rounding error of the addition kept exactly in lo
+// (Knuth's TwoSum; no multiply, so no contraction can change it).
+__device__ __forceinline__ void two_sum_acc(float &hi, float &lo, float x) {
+  const float s = hi + x;
+  const float bp = s - hi;
+  const float e = (hi - (s - bp)) + (x - bp);
+  hi = s;
+  lo += e;
+}
+
+// Butterfly sum of (hi, lo) pairs over aligned sets of `width` lanes.
+// TwoSum's error term is exact, so both partners of every exchange get
+// bit-identical results.
+__device__ __forceinline__ void lanes_sum2(float &hi, float &lo, int width) {
+  for (int o = width >> 1; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xFFFFFFFFu, hi, o);
+    const float ol = __shfl_xor_sync(0xFFFFFFFFu, lo, o);
+    const float s = hi + oh;
+    const float bp = s - hi;
+    const float e = (hi - (s - bp)) + (oh - bp);
+    hi = s;
+    lo = (lo + ol) + e;
+  }
+}
+
+// y + dy ~= 1/sqrt(S/n + eps) for S = s_hi + s_lo, to ~2^-44 relative, with
+// |dy| <= half an ulp of y:
+// m = S/n + eps in double-float (the FMA remainder of the division is exact
+// because it spans few bits), y0 = rsqrt(m) to ~2^-22, then one Newton step
+// y = y0 (1 + rho/2 + 3 rho^2/8) with rho = 1 - m y0^2 from exact products.
+__device__ __forceinline__ void rsqrt_df(float s_hi, float s_lo, float n, float inv_n, float eps,
+                                         float &y, float &dy) {
+  const float q = s_hi * inv_n;
+  const float ql = (fmaf(-q, n, s_hi) + s_lo) * inv_n;
+  const float m = q + eps;
+  const float bp = m - q;
+  const float ml = ((q - (m - bp)) + (eps - bp)) + ql;
+  const float y0 = rsqrtf(m);
+  const float p = y0 * y0, pl = fmaf(y0, y0, -p);  // y0^2 = p + pl exactly
+  const float t = m * p, tl = fmaf(m, p, -t);      // m p = t + tl exactly
+  const float rho = (1.0f - t) - (tl + fmaf(m, pl, ml * p));
+  const float c = y0 * rho * fmaf(0.375f, rho, 0.5f);
+  y = y0 + c;               // renormalise: |c| << y0, so Fast2Sum is exact
+  dy = (y0 - y) + c;
+}
+
+// --------------------------------------------------------- packed fp32 x2
+//
+// sm_100+ issues two fp32 operations per instruction (f32x2), each lane
+// rounded exactly like the scalar instruction.
+
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\tfma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+// A bf16 pair (element 0 in the low half) as two fp32 values.
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+
 }  // namespace vg

@@ -27,8 +27,12 @@ __device__ __forceinline__ float fast_rcp(float x) {
   return r;
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) {
-  return g * fast_rcp(1.0f + __expf(-g)) * u;
+// Two elements of silu(g) * u = g * rcp(1 + exp(-g)) * u.
+__device__ __forceinline__ float2 silu_mul2(uint32_t gw, uint32_t uw) {
+  const float2 g = bf16x2_to_f2(gw);
+  const float2 e = make_float2(__expf(-g.x), __expf(-g.y));
+  const float2 d = f2_add(e, make_float2(1.0f, 1.0f));
+  return f2_mul(f2_mul(g, make_float2(fast_rcp(d.x), fast_rcp(d.y))), bf16x2_to_f2(uw));
 }
 
 __device__ __forceinline__ void silu_chunk(const uint4 &gv, const uint4 &uv, float (&v)[8]) {
@@ -36,8 +40,19 @@ __device__ __forceinline__ void silu_chunk(const uint4 &gv, const uint4 &uv, flo
   const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    v[2 * i] = silu_mul(bf16_lo(gw[i]), bf16_lo(uw[i]));
-    v[2 * i + 1] = silu_mul(bf16_hi(gw[i]), bf16_hi(uw[i]));
+    const float2 a = silu_mul2(gw[i], uw[i]);
+    v[2 * i] = a.x;
+    v[2 * i + 1] = a.y;
+  }
+}
+
+__device__ __forceinline__ void scale8(float (&v)[8], float m) {
+  const float2 mm = make_float2(m, m);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = f2_mul(make_float2(v[2 * i], v[2 * i + 1]), mm);
+    v[2 * i] = p.x;
+    v[2 * i + 1] = p.y;
   }
 }
 
@@ -48,7 +63,7 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
   return m;
 }
 
-template <int VPT, int MODE>
+template <int VPT, int MODE, int GCH>
 __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
   __shared__ float red[16];
 
@@ -82,12 +97,11 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
       silu_chunk(gv[k], uv[k], v);
       float m = inv_static;
       if (MODE == kPerGroup) {
-        const float s = dynamic_scale(lanes_max(amax8(v), a.gch));
-        if (live && c < a.nch && (c % a.gch) == 0) a.scale[row * a.ngroups + c / a.gch] = s;
+        const float s = dynamic_scale(lanes_max(amax8(v), GCH));
+        if (live && c < a.nch && (tid & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
         m = __frcp_rn(s);
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] *= m;
+      scale8(v, m);
       if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
     }
     return;
@@ -115,8 +129,7 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int c = lr + k * a.ntr;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) act[k][i] *= m;
+    scale8(act[k], m);
     if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(act[k]));
   }
 }
@@ -124,9 +137,14 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
 template <int VPT>
 cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStream_t s) {
   switch (mode) {
-    case kStatic: silu_fp8_kernel<VPT, kStatic><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
-    case kPerToken: silu_fp8_kernel<VPT, kPerToken><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
-    default: silu_fp8_kernel<VPT, kPerGroup><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
+    case kStatic: silu_fp8_kernel<VPT, kStatic, 1><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
+    case kPerToken: silu_fp8_kernel<VPT, kPerToken, 1><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
+    default:
+      if (a.gch == 8)
+        silu_fp8_kernel<VPT, kPerGroup, 8><<<(unsigned)p.grid, p.block(), 0, s>>>(a);
+      else
+        silu_fp8_kernel<VPT, kPerGroup, 16><<<(unsigned)p.grid, p.block(), 0, s>>>(a);
+      break;
   }
   return cudaGetLastError();
 }
