@@ -57,10 +57,9 @@ CFG3_ACT = gen.Workload("silu_per_group128_16384x28672", "silu", 16384, 28672, g
 STEPS = {
     "llama3_8b_decode": (gen.CFG1, gen.CFG1_ACT),
     "llama3_70b_prefill": (gen.CFG3, CFG3_ACT),
-    "norm_static_16x1024": (gen.CFG0,),
-    "silu_2048x14336_static": (gen.CFG2A,),
-    "silu_2048x14336_per_group128": (gen.CFG2B,),
 }
+# every named single-op workload is also a (one-op) step
+STEPS.update({name: (w,) for name, w in gen.NAMED.items()})
 DEFAULT_STEP = "llama3_8b_decode"
 
 
@@ -77,6 +76,8 @@ def parse_args(argv=None):
                    help="bound on the oracle's CPU-baseline sample")
     p.add_argument("--clock-window", type=float, default=1.0,
                    help="seconds of untimed replays under clock sampling before the timed one")
+    p.add_argument("--tokens", type=int, default=None,
+                   help="override num_tokens of every op of the step (smaller profiling captures)")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -282,7 +283,7 @@ def run_gpu(args, dist):
     if not os.path.exists(vg_build.LIB_PATH):
         vg_build.build()
     vg.load()
-    step = STEPS[args.workload]
+    step = select_step(args)
     nbytes = step_bytes(step)
     host = [w.inputs() for w in step]
     weights = {w.name: torch.from_numpy(h["weight"].view(np.int16)).to(dev)
@@ -376,7 +377,7 @@ def run_gpu(args, dist):
         "ms_per_step": round(ms / args.steps, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
-            "workload": args.workload,
+            "workload": args.workload if args.tokens is None else f"{args.workload}@T{args.tokens}",
             "ops": [describe(w) for w in step],
             "bytes_per_step": nbytes,
             "l2": f"inputs > L2: {n_sets} rotating buffer sets x {resident / 2**20:.1f} MiB "
@@ -396,6 +397,15 @@ def run_gpu(args, dist):
         "clocks": clk,
     }
     return line
+
+
+def select_step(args):
+    import dataclasses
+    step = STEPS[args.workload]
+    if args.tokens is not None:
+        step = tuple(dataclasses.replace(w, T=args.tokens, name=f"{w.name}@T{args.tokens}")
+                     for w in step)
+    return step
 
 
 def describe(w):
@@ -507,7 +517,7 @@ def run_reference(args, dist):
     """The fp64 CPU oracle as the reference arm, on this workload."""
     if dist.rank != 0:
         return None
-    step = STEPS[args.workload]
+    step = select_step(args)
     host = [w.inputs() for w in step]
     threads = os.cpu_count() or 1
     one, pool = oracle_step_runner(step, host, threads)
