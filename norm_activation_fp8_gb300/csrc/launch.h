@@ -18,8 +18,9 @@ struct RowPlan {
   int block() const { return ntr * rpc; }
 };
 
-// Picks the plan for nch chunks per row (nch <= 4096).
-RowPlan plan_rows(int64_t T, int nch);
+// Picks the plan for nch chunks per row (nch <= 4096): at least `min_vpt`
+// chunks per thread, more if a row would need more than 512 threads.
+RowPlan plan_rows(int64_t T, int nch, int min_vpt);
 
 struct NormArgs {
   uint8_t *q;
@@ -53,6 +54,22 @@ struct SiluArgs {
 };
 
 cudaError_t launch_norm_fp8(NormArgs a, int mode, const RowPlan &plan, cudaStream_t stream);
+
+// Persistent TMA-pipelined norm kernel: `grid` CTAs of `block` threads (one
+// row at a time, vpt chunks per thread), `stages` rows staged ahead.
+struct TmaPlan {
+  int vpt;
+  int block;
+  int stages;
+  int64_t grid;
+};
+constexpr size_t kTmaMaxSmem = 227 * 1024;  // opt-in limit per CTA
+size_t norm_tma_smem_bytes(int H, bool res, int stages, int block, int vpt, int slots);
+cudaError_t launch_norm_fp8_tma(NormArgs a, int mode, const TmaPlan &plan, cudaStream_t stream);
+
+// Reads (and optionally clears) the norm kernels' device status word;
+// synchronous.  0xFFFFFFFF if it could not be read.
+uint32_t read_norm_status(bool reset);
 cudaError_t launch_silu_fp8(SiluArgs a, int mode, const RowPlan &plan, cudaStream_t stream);
 
 }  // namespace vg

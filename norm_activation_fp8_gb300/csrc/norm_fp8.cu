@@ -4,112 +4,216 @@
 // torch.compile passes" page: fused_add_rms_norm(x, residual) (residual
 // updated in place) or rms_norm(x), followed by quant_fp8 with a static,
 // per-token or per-token-group scale, in one kernel.  The normalised row is
-// never written: it lives in registers between the two halves of the kernel.
+// never written: t = r*w stays in registers between the two halves.
 //
-// Per row (n = H, chunks of 8 bf16):
-//   1. 16-byte loads of x, residual and weight for every chunk the thread
-//      owns, all issued before any is used;
-//   2. r = bf16(x + residual) (fp32 add, RNE) -> residual_out; t = r*w
-//      (exact in fp32: 8-bit x 8-bit significands) kept in registers;
-//      sum(r^2); amax of |t| per chunk;
-//   3. one reduction over the row's threads: warp butterflies, then shared
+// Per row (n = H, chunks of 8 bf16; a row's ntr threads own chunks
+// c = lr + k*ntr, k < VPT):
+//   1. r = bf16(x + residual) (fp32 add, RNE) -> residual_out; t = r*w
+//      (exact in fp32: 8-bit x 8-bit significands); sum(r^2); amax |t| per
+//      chunk;
+//   2. one reduction over the row's threads: warp butterflies, then shared
 //      memory across the row's warps;
-//   4. y = t * inv with inv = 1/sqrt(sum/H + eps); scale; q = e4m3(y / s)
+//   3. y = t * inv with inv = 1/sqrt(sum/H + eps); scale; q = e4m3(y / s)
 //      packed with cvt.rn.satfinite.e4m3x2 into 8-byte stores.
 //
 // Static scale: inv in fp32 (rsqrt), v = t * (inv / s).
+// Dynamic scales: see dyn_scale.cuh.  Each scale slot (group, or row) is
+// computed once, by the slot's own thread, through shared memory; r^2 is
+// summed in double-float (TwoSum; r^2 is exact in fp32).
 //
-// Dynamic scales (per token, per group): y/s = 448 t/amax up to the fp32
-// rounding of the stored scale s = fp32(amax inv / 448), and t and amax are
-// both products of two bf16 numbers, so a small fraction of elements fall
-// exactly on an e4m3 rounding midpoint.  Their correct code is decided by
-// the direction in which the stored scale was rounded, so the dynamic path
-//   - sums r^2 in double-float (TwoSum; r^2 is exact in fp32) and gets
-//     inv as a double-float (rsqrt_df), all in fp32 arithmetic;
-//   - forms X = amax * inv exactly enough to round s = fp32(X / 448)
-//     correctly and to know the sign of X - 448 s (an FMA residual that
-//     is exact);
-//   - per element computes q1 = 448 t / amax correctly rounded (one FMA
-//     correction of the product with the correctly rounded reciprocal), and
-//     where an exact FMA remainder shows q1 is the exact quotient -- the
-//     only case in which it can sit on a midpoint -- moves it one or two
-//     ulps in the direction of that sign before the conversion.  Elements
-//     that are not exact ties lie at least 2^-22 (relative) from every
-//     midpoint, so the move never changes their code.
+// Two kernels share that row logic:
+//   norm_fp8_kernel      one CTA per row group, inputs loaded straight into
+//                        registers with 16-byte loads issued up front (small
+//                        T: lowest latency);
+//   norm_fp8_tma_kernel  persistent CTAs, one row at a time, the next rows'
+//                        x and residual staged into shared memory by bulk
+//                        TMA copies on a ring of mbarrier-tracked stages, the
+//                        weight staged once per CTA (large T: HBM stays busy
+//                        while a CTA reduces, scales and stores a row).
+#include <atomic>
+
 #include "common.cuh"
+#include "dyn_scale.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace vg {
+
+// Status word of this translation unit's kernels (kErrWaitTimeout).
+__device__ uint32_t g_norm_status;
+
 namespace {
 
-// fp32(A_MIN / 448), the scale of a row or group whose amax is floored.
-constexpr float kFloorScale = (float)((double)kAmaxFloor / 448.0);
-constexpr float kAwayOneUlp = 1.0f + 1.0f / 8388608.0f;    // 1 + 2^-23
-constexpr float kTowardOneUlp = 1.0f - 1.0f / 16777216.0f; // 1 - 2^-24
+// ---------------------------------------------------------------- row logic
 
-// Per row (or group) quantities of the dynamic path.
-struct DynScale {
-  float s;   // stored dequantisation scale
-  float a;   // divisor: v = 448 t / a (a = amax, or the floored equivalent)
-  float ra;  // correctly rounded 1/a
-  float f;   // multiplier applied to an exact quotient (tie direction)
+struct RowAcc {
+  float2 ss = make_float2(0.f, 0.f);  // sum r^2 (two lanes)
+  float2 lo = make_float2(0.f, 0.f);  // its TwoSum error terms (dynamic modes)
 };
 
-__device__ __forceinline__ float next_up(float x) { return __uint_as_float(__float_as_uint(x) + 1u); }
-__device__ __forceinline__ float next_down(float x) { return __uint_as_float(__float_as_uint(x) - 1u); }
-
-// amax: max |r*w| of the row or group; inv = y + dy, a normalised
-// double-float (|dy| <= half an ulp of y).
-__device__ __forceinline__ DynScale make_dyn_scale(float amax, float y, float dy) {
-  const float xh = amax * y;
-  const float xl = fmaf(amax, y, -xh) + amax * dy;  // X = xh + xl, |xl| <~ ulp(xh)/2
-  DynScale d;
-  if (xh >= kAmaxFloor) {
-    // s = fp32(X / 448): the correctly rounded xh/448 is within one ulp of
-    // it; D = X - 448 s (the FMA part is exact) decides the last step.
-    float s = __fdiv_rn(xh, 448.0f);
-    float D = fmaf(-448.0f, s, xh) + xl;
-    const float half = 224.0f * (next_up(s) - s);
-    if (D > half) {
-      s = next_up(s);
-      D = fmaf(-448.0f, s, xh) + xl;
-    } else if (D < -half) {
-      s = next_down(s);
-      D = fmaf(-448.0f, s, xh) + xl;
+// Pass 1 over one chunk: r = bf16(x + residual) (returned packed, for
+// residual_out), t = r * w, the chunk's amax |t|, and sum r^2.
+template <bool DYN, bool RES>
+__device__ __forceinline__ uint4 pass1_chunk(const uint4 &xv, const uint4 &rv, const uint4 &wv,
+                                             float2 (&t)[4], float &cmax, RowAcc &acc) {
+  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+  const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+  const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+  const float2 neg1 = make_float2(-1.f, -1.f);
+  uint32_t ow[4];
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (RES) {
+      const float2 s2 = f2_add(bf16x2_to_f2(xw[i]), bf16x2_to_f2(rw[i]));
+      ow[i] = pack_bf16x2_rn(s2.x, s2.y);
+    } else {
+      ow[i] = xw[i];
     }
-    d.s = s;
-    d.f = D > 0.f ? kAwayOneUlp : (D < 0.f ? kTowardOneUlp : 1.0f);
-    d.a = amax;
-  } else {  // amax floored: v = t * inv / s, no exact ties to resolve
-    d.s = kFloorScale;
-    d.f = 1.0f;
-    d.a = amax > 0.f ? 448.0f * kFloorScale / y : 1.0f;
+    const float2 r = bf16x2_to_f2(ow[i]);
+    if (DYN) {  // packed TwoSum of r^2 into (ss, lo)
+      const float2 x = f2_mul(r, r);
+      const float2 s = f2_add(acc.ss, x);
+      const float2 bp = f2_fma(acc.ss, neg1, s);
+      const float2 e = f2_add(f2_fma(f2_fma(bp, neg1, s), neg1, acc.ss), f2_fma(bp, neg1, x));
+      acc.ss = s;
+      acc.lo = f2_add(acc.lo, e);
+    } else {
+      acc.ss = f2_fma(r, r, acc.ss);
+    }
+    t[i] = f2_mul(r, bf16x2_to_f2(ww[i]));
+    m = fmaxf(m, fmaxf(fabsf(t[i].x), fabsf(t[i].y)));
   }
-  d.ra = __frcp_rn(d.a);
-  return d;
+  cmax = m;
+  return make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
-// Two elements: v = 448 t / a correctly rounded, exact quotients scaled by f.
-__device__ __forceinline__ float2 dyn_values(float2 t, const DynScale &d) {
-  const float2 T = f2_mul(t, make_float2(kE4M3Max, kE4M3Max));  // exact
-  const float2 ra = make_float2(d.ra, d.ra);
-  const float2 na = make_float2(-d.a, -d.a);
-  const float2 q0 = f2_mul(T, ra);
-  const float2 q1 = f2_fma(f2_fma(q0, na, T), ra, q0);
-  const float2 e1 = f2_fma(q1, na, T);
-  const float2 m = make_float2(e1.x == 0.f ? d.f : 1.0f, e1.y == 0.f ? d.f : 1.0f);
-  return f2_mul(q1, m);
+// Shared memory a row group needs for the reduction and the scales.
+struct RowSmem {
+  float4 *red;    // [2][16] per-warp partials, double-buffered by row parity
+  float *cmax;    // [rpc][ntr * VPT] chunk amax (per-group)
+  DynScale *dyn;  // [rpc][nslots]
+};
+
+// Row reduction, scales and pass 2 (quantise + store q).  Called by every
+// thread of the CTA.
+template <int VPT, int MODE, int GCH>
+__device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)[VPT][4],
+                                            const float (&cmax)[VPT], const RowAcc &acc,
+                                            const RowSmem &sm, int parity, int slot, int lr,
+                                            int64_t row, bool live, int64_t base) {
+  constexpr bool DYN = MODE != kStatic;
+  const int lane = threadIdx.x & 31;
+  const int nw = a.ntr >> 5;
+  float4 *red = sm.red + parity * 16;
+
+  if (!DYN) {
+    float sum = warp_sum(acc.ss.x + acc.ss.y);
+    if (lane == 0) red[slot * nw + (lr >> 5)] = make_float4(sum, 0.f, 0.f, 0.f);
+    __syncthreads();
+    sum = 0.f;
+    for (int i = 0; i < nw; ++i) sum += red[slot * nw + i].x;
+    const float inv = rsqrtf(fmaf(sum, a.inv_h, a.eps));
+    const float mult = inv * __frcp_rn(__ldg(a.scale));
+    const float2 m2 = make_float2(mult, mult);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int c = lr + k * a.ntr;
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 q = f2_mul(t[k][i], m2);
+        v[2 * i] = q.x;
+        v[2 * i + 1] = q.y;
+      }
+      if (live && c < a.nch) st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
+    }
+    return;
+  }
+
+  // Dynamic scales: each scale slot (group, or the row) is computed once,
+  // by the slot's thread, from the warp partials and chunk amaxes.
+  const int row_chunks = a.ntr * VPT;
+  const int nslots = MODE == kPerToken ? 1 : a.ngroups;
+  float hi = acc.ss.x, lo = acc.lo.x + acc.lo.y;
+  two_sum_acc(hi, lo, acc.ss.y);
+  lanes_sum2(hi, lo, 32);
+  float am = 0.f;
+  if (MODE == kPerToken) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) am = fmaxf(am, cmax[k]);
+    am = warp_max(am);
+  } else {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) sm.cmax[slot * row_chunks + lr + k * a.ntr] = cmax[k];
+  }
+  if (lane == 0) red[slot * nw + (lr >> 5)] = make_float4(hi, lo, am, 0.f);
+  __syncthreads();
+  if (lr < nslots) {
+    float h = 0.f, l = 0.f, amr = 0.f;
+    for (int i = 0; i < nw; ++i) {  // same order in every slot thread
+      const float4 p = red[slot * nw + i];
+      two_sum_acc(h, l, p.x);
+      l += p.y;
+      amr = fmaxf(amr, p.z);
+    }
+    float y, dy;
+    rsqrt_df(h, l, (float)a.H, a.inv_h, a.eps, y, dy);
+    if (MODE == kPerGroup) {
+      amr = 0.f;
+#pragma unroll
+      for (int i = 0; i < GCH; ++i) amr = fmaxf(amr, sm.cmax[slot * row_chunks + lr * GCH + i]);
+    }
+    const DynScale d = make_dyn_scale(amr, y, dy);
+    sm.dyn[slot * nslots + lr] = d;
+    if (live) a.scale[row * nslots + lr] = d.s;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int c = lr + k * a.ntr;
+    // padding chunks (c >= nch) read slot 0 and store nothing
+    const DynScale d = sm.dyn[slot * nslots + (MODE == kPerToken || c >= a.nch ? 0 : c / GCH)];
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 q = dyn_values(t[k][i], d);
+      v[2 * i] = q.x;
+      v[2 * i + 1] = q.y;
+    }
+    if (live && c < a.nch) st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
+  }
 }
+
+__host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
+
+// Dynamic shared memory of the row logic: red, cmax, dyn.
+__host__ __device__ inline size_t row_smem_bytes(int block, int vpt, int slots) {
+  return 2 * 16 * sizeof(float4) + align128((size_t)block * vpt * 4) +
+         align128((size_t)slots * sizeof(DynScale));
+}
+
+__device__ inline RowSmem carve_row_smem(unsigned char *p, int block, int vpt) {
+  RowSmem sm;
+  sm.red = reinterpret_cast<float4 *>(p);
+  p += 2 * 16 * sizeof(float4);
+  sm.cmax = reinterpret_cast<float *>(p);
+  p += align128((size_t)block * vpt * 4);
+  sm.dyn = reinterpret_cast<DynScale *>(p);
+  return sm;
+}
+
+// ------------------------------------------------------- register kernel
 
 template <int VPT, int MODE, int GCH, bool RES>
 __global__ void __launch_bounds__(512) norm_fp8_kernel(const NormArgs a) {
   constexpr bool DYN = MODE != kStatic;
-  __shared__ float4 red[16];  // per-warp partials; blockDim <= 512
+  extern __shared__ __align__(128) unsigned char dsm[];
+  const RowSmem sm = carve_row_smem(dsm, blockDim.x, VPT);
 
   const int tid = threadIdx.x;
   const int slot = tid / a.ntr;       // row slot inside the CTA
   const int lr = tid - slot * a.ntr;  // thread index inside the row
-  const int lane = tid & 31;
   const int64_t row = (int64_t)blockIdx.x * a.rpc + slot;
   const bool live = row < a.T;
   const int64_t base = live ? row * a.H : 0;
@@ -129,124 +233,152 @@ __global__ void __launch_bounds__(512) norm_fp8_kernel(const NormArgs a) {
     }
   }
 
-  // r = bf16(x + residual) -> residual_out; t = r*w; sum r^2; amax |t|.
   float2 t[VPT][4];
   float cmax[VPT];
-  float2 ss = make_float2(0.f, 0.f), ss_lo = make_float2(0.f, 0.f);
-  const float2 neg1 = make_float2(-1.f, -1.f);
+  RowAcc acc;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
-    const uint32_t xw[4] = {xv[k].x, xv[k].y, xv[k].z, xv[k].w};
-    const uint32_t rw[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
-    const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
-    uint32_t ow[4];
-    float m = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (RES) {
-        const float2 s2 = f2_add(bf16x2_to_f2(xw[i]), bf16x2_to_f2(rw[i]));
-        ow[i] = pack_bf16x2_rn(s2.x, s2.y);
-      } else {
-        ow[i] = xw[i];
-      }
-      const float2 r = bf16x2_to_f2(ow[i]);
-      if (DYN) {  // packed TwoSum of r^2 into (ss, ss_lo)
-        const float2 x = f2_mul(r, r);
-        const float2 s = f2_add(ss, x);
-        const float2 bp = f2_fma(ss, neg1, s);
-        const float2 e = f2_add(f2_fma(f2_fma(bp, neg1, s), neg1, ss), f2_fma(bp, neg1, x));
-        ss = s;
-        ss_lo = f2_add(ss_lo, e);
-      } else {
-        ss = f2_fma(r, r, ss);
-      }
-      t[k][i] = f2_mul(r, bf16x2_to_f2(ww[i]));
-      m = fmaxf(m, fmaxf(fabsf(t[k][i].x), fabsf(t[k][i].y)));
-    }
-    cmax[k] = m;
+    const uint4 ow = pass1_chunk<DYN, RES>(xv[k], rv[k], wv[k], t[k], cmax[k], acc);
     const int c = lr + k * a.ntr;
-    if (RES && live && c < a.nch)
-      st_stream(a.res_out + base + c * kElemsPerChunk, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+    if (RES && live && c < a.nch) st_stream(a.res_out + base + c * kElemsPerChunk, ow);
   }
+  finish_rows<VPT, MODE, GCH>(a, t, cmax, acc, sm, 0, slot, lr, row, live, base);
+}
 
-  float mult = 0.f;
-  DynScale dk[VPT];
-  if (!DYN) {
-    float sum = ss.x + ss.y;
-    sum = warp_sum(sum);
-    if (a.ntr > 32) {  // uniform over the CTA
-      const int nw = a.ntr >> 5;
-      if (lane == 0) red[slot * nw + (lr >> 5)] = make_float4(sum, 0.f, 0.f, 0.f);
-      __syncthreads();
-      sum = 0.f;
-      for (int i = 0; i < nw; ++i) sum += red[slot * nw + i].x;
-    }
-    const float inv = rsqrtf(fmaf(sum, a.inv_h, a.eps));
-    mult = inv * __frcp_rn(__ldg(a.scale));
-  } else {
-    float hi = ss.x, lo = ss_lo.x + ss_lo.y;
-    two_sum_acc(hi, lo, ss.y);
-    lanes_sum2(hi, lo, 32);
-    float am = 0.f;
-    if (MODE == kPerToken) {
+// ------------------------------------------------------------ TMA kernel
+//
+// Dynamic shared memory: stages[S] (x row, then residual row), the weight
+// row, the row logic's buffers, then S + 1 mbarriers (full[S], weight).
+
+struct TmaLayout {
+  size_t stage_bytes, w_off, row_off, bar_off, total;
+  __host__ __device__ TmaLayout(int H, bool res, int stages, int block, int vpt, int slots) {
+    stage_bytes = align128((size_t)(res ? 4 : 2) * H);
+    w_off = stage_bytes * stages;
+    row_off = w_off + align128((size_t)2 * H);
+    bar_off = row_off + align128(row_smem_bytes(block, vpt, slots));
+    total = bar_off + (size_t)(stages + 1) * 8;
+  }
+};
+
+template <int VPT, int MODE, int GCH, bool RES>
+__global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, const int stages) {
+  constexpr bool DYN = MODE != kStatic;
+  extern __shared__ __align__(128) unsigned char dsm[];
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerToken ? 1 : a.ngroups);
+  const TmaLayout L(a.H, RES, stages, blockDim.x, VPT, slots);
+  const RowSmem sm = carve_row_smem(dsm + L.row_off, blockDim.x, VPT);
+  unsigned char *wbuf = dsm + L.w_off;
+  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + L.bar_off);
+  uint64_t *wbar = full + stages;
+  const uint32_t row_bytes = 2u * (uint32_t)a.H;
+
+  const int lr = threadIdx.x;  // one row at a time: ntr == blockDim.x
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+
+  auto issue = [&](int s, int64_t row) {
+    unsigned char *st = dsm + (size_t)s * L.stage_bytes;
+    mbar_arrive_expect_tx(&full[s], RES ? 2 * row_bytes : row_bytes);
+    tma_load_bulk(st, a.x + row * a.H, row_bytes, &full[s]);
+    if (RES) tma_load_bulk(st + row_bytes, a.res + row * a.H, row_bytes, &full[s]);
+  };
+
+  if (lr == 0) {
+    for (int s = 0; s <= stages; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (lr == 0) {
+    mbar_arrive_expect_tx(wbar, row_bytes);
+    tma_load_bulk(wbuf, a.w, row_bytes, wbar);
+    for (int s = 0; s < stages; ++s)
+      if (first + s * stride < a.T) issue(s, first + s * stride);
+  }
+  bool failed = __syncthreads_or(!mbar_wait_bounded(wbar, 0));
+
+  int64_t i = 0;
+  for (int64_t row = first; row < a.T && !failed; row += stride, ++i) {
+    const int s = (int)(i % stages);
+    const unsigned char *st = dsm + (size_t)s * L.stage_bytes;
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / stages) & 1));
+    const int64_t base = row * a.H;
+
+    float2 t[VPT][4];
+    float cmax[VPT];
+    RowAcc acc;
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) am = fmaxf(am, cmax[k]);
-      am = warp_max(am);
+    for (int k = 0; k < VPT; ++k) {
+      const int c = lr + k * a.ntr;
+      uint4 xv = make_uint4(0, 0, 0, 0), rv = xv, wv = xv;
+      if (ok && c < a.nch) {
+        xv = lds128(st + c * 16);
+        if (RES) rv = lds128(st + row_bytes + c * 16);
+        wv = lds128(wbuf + c * 16);
+      }
+      const uint4 ow = pass1_chunk<DYN, RES>(xv, rv, wv, t[k], cmax[k], acc);
+      if (RES && ok && c < a.nch) st_stream(a.res_out + base + c * kElemsPerChunk, ow);
     }
-    if (a.ntr > 32) {  // uniform over the CTA
-      const int nw = a.ntr >> 5;
-      if (lane == 0) red[slot * nw + (lr >> 5)] = make_float4(hi, lo, am, 0.f);
-      __syncthreads();
-      // every warp folds the row's partials the same way: lane i takes
-      // partial i, then one butterfly (identical result in every lane)
-      const float4 p = lane < nw ? red[slot * nw + lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-      hi = p.x;
-      lo = p.y;
-      lanes_sum2(hi, lo, 32);
-      if (MODE == kPerToken) am = warp_max(p.z);
+    // Every thread has read stage s once this barrier is passed, so its
+    // refill goes out now; a timed-out wait anywhere in the CTA ends the
+    // loop for all threads.
+    if (__syncthreads_or(!ok)) {
+      failed = true;
+      break;
     }
-    float y, dy;
-    rsqrt_df(hi, lo, (float)a.H, a.inv_h, a.eps, y, dy);
-    if (MODE == kPerToken) {
-      const DynScale d = make_dyn_scale(am, y, dy);
-      if (live && lr == 0) a.scale[row] = d.s;
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) dk[k] = d;
-    } else {
-      // Per group: the group's GCH chunks sit on GCH consecutive lanes.
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        const float gmax = lanes_max(cmax[k], GCH);
-        dk[k] = make_dyn_scale(gmax, y, dy);
-        const int c = lr + k * a.ntr;
-        if (live && c < a.nch && (lane & (GCH - 1)) == 0)
-          a.scale[row * a.ngroups + c / GCH] = dk[k].s;
+    if (lr == 0) {
+      const int64_t next = row + (int64_t)stages * stride;
+      if (next < a.T) {
+        fence_proxy_async_smem();
+        issue(s, next);
       }
     }
+    finish_rows<VPT, MODE, GCH>(a, t, cmax, acc, sm, (int)(i & 1), 0, lr, row, true, base);
   }
-
-  // q = e4m3(y / s).
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int c = lr + k * a.ntr;
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 q = DYN ? dyn_values(t[k][i], dk[k]) : f2_mul(t[k][i], make_float2(mult, mult));
-      v[2 * i] = q.x;
-      v[2 * i + 1] = q.y;
-    }
-    if (live && c < a.nch) st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
+  if (failed && lr == 0) {
+    atomicOr(&g_norm_status, kErrWaitTimeout);
+    // wait (bounded) for the copies this CTA may still have in flight
+    for (int64_t k = i; k < i + stages; ++k)
+      if (first + k * stride < a.T) mbar_wait_bounded(&full[k % stages], (uint32_t)((k / stages) & 1));
   }
 }
 
+// ------------------------------------------------------------ launchers
+
 template <int VPT, int MODE, int GCH>
 cudaError_t launch_res(const NormArgs &a, const RowPlan &p, cudaStream_t s) {
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerToken ? 1 : a.ngroups) * p.rpc;
+  const size_t smem = row_smem_bytes(p.block(), VPT, slots);
   if (a.res != nullptr)
-    norm_fp8_kernel<VPT, MODE, GCH, true><<<(unsigned)p.grid, p.block(), 0, s>>>(a);
+    norm_fp8_kernel<VPT, MODE, GCH, true><<<(unsigned)p.grid, p.block(), smem, s>>>(a);
   else
-    norm_fp8_kernel<VPT, MODE, GCH, false><<<(unsigned)p.grid, p.block(), 0, s>>>(a);
+    norm_fp8_kernel<VPT, MODE, GCH, false><<<(unsigned)p.grid, p.block(), smem, s>>>(a);
   return cudaGetLastError();
+}
+
+template <int VPT, int MODE, int GCH, bool RES>
+cudaError_t launch_tma_res(const NormArgs &a, const TmaPlan &p, cudaStream_t s) {
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerToken ? 1 : a.ngroups);
+  const TmaLayout L(a.H, RES, p.stages, p.block, VPT, slots);
+  auto kern = norm_fp8_tma_kernel<VPT, MODE, GCH, RES>;
+  // opt in to large dynamic shared memory once per instantiation and device
+  static std::atomic<uint64_t> opted_in{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(opted_in.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaMaxSmem);
+    if (e != cudaSuccess) return e;
+    opted_in.fetch_or(bit, std::memory_order_release);
+  }
+  kern<<<(unsigned)p.grid, p.block, L.total, s>>>(a, p.stages);
+  return cudaGetLastError();
+}
+
+template <int VPT, int MODE, int GCH>
+cudaError_t launch_tma_mode(const NormArgs &a, const TmaPlan &p, cudaStream_t s) {
+  return a.res != nullptr ? launch_tma_res<VPT, MODE, GCH, true>(a, p, s)
+                          : launch_tma_res<VPT, MODE, GCH, false>(a, p, s);
 }
 
 template <int VPT>
@@ -257,6 +389,17 @@ cudaError_t launch_mode(const NormArgs &a, int mode, const RowPlan &p, cudaStrea
     default:
       return a.gch == 8 ? launch_res<VPT, kPerGroup, 8>(a, p, s)
                         : launch_res<VPT, kPerGroup, 16>(a, p, s);
+  }
+}
+
+template <int VPT>
+cudaError_t launch_tma_vpt(const NormArgs &a, int mode, const TmaPlan &p, cudaStream_t s) {
+  switch (mode) {
+    case kStatic: return launch_tma_mode<VPT, kStatic, 1>(a, p, s);
+    case kPerToken: return launch_tma_mode<VPT, kPerToken, 1>(a, p, s);
+    default:
+      return a.gch == 8 ? launch_tma_mode<VPT, kPerGroup, 8>(a, p, s)
+                        : launch_tma_mode<VPT, kPerGroup, 16>(a, p, s);
   }
 }
 
@@ -271,6 +414,30 @@ cudaError_t launch_norm_fp8(NormArgs a, int mode, const RowPlan &p, cudaStream_t
     case 4: return launch_mode<4>(a, mode, p, s);
     default: return launch_mode<8>(a, mode, p, s);
   }
+}
+
+size_t norm_tma_smem_bytes(int H, bool res, int stages, int block, int vpt, int slots) {
+  return TmaLayout(H, res, stages, block, vpt, slots).total;
+}
+
+cudaError_t launch_norm_fp8_tma(NormArgs a, int mode, const TmaPlan &p, cudaStream_t s) {
+  a.ntr = p.block;
+  a.rpc = 1;
+  switch (p.vpt) {
+    case 2: return launch_tma_vpt<2>(a, mode, p, s);
+    case 4: return launch_tma_vpt<4>(a, mode, p, s);
+    default: return launch_tma_vpt<8>(a, mode, p, s);
+  }
+}
+
+uint32_t read_norm_status(bool reset) {
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_norm_status, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (reset) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_norm_status, &zero, sizeof(zero)) != cudaSuccess) return 0xFFFFFFFFu;
+  }
+  return v;
 }
 
 }  // namespace vg

@@ -18,20 +18,26 @@ namespace {
 constexpr int kMaxDevices = 64;
 // 0 = not checked yet, 1 = supported (cc 10.3), 2 = unsupported.
 std::atomic<int> g_device_state[kMaxDevices];
+std::atomic<int> g_device_sms[kMaxDevices];
 
-vg_status check_device() {
+// Checks (once per device) that the current device is a GB300 and returns
+// its SM count in *sms.
+vg_status check_device(int *sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return VG_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return VG_ERR_UNSUPPORTED_DEVICE;
-  int st = g_device_state[dev].load(std::memory_order_relaxed);
+  int st = g_device_state[dev].load(std::memory_order_acquire);
   if (st == 0) {
-    int major = 0, minor = 0;
+    int major = 0, minor = 0, n = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return VG_ERR_CUDA;
+    g_device_sms[dev].store(n, std::memory_order_relaxed);
     st = (major == 10 && minor == 3) ? 1 : 2;
-    g_device_state[dev].store(st, std::memory_order_relaxed);
+    g_device_state[dev].store(st, std::memory_order_release);
   }
+  *sms = g_device_sms[dev].load(std::memory_order_relaxed);
   return st == 1 ? VG_OK : VG_ERR_UNSUPPORTED_DEVICE;
 }
 
@@ -49,20 +55,51 @@ vg_status check_row(int64_t num_tokens, int64_t n, int32_t mode, int32_t group_s
 
 }  // namespace
 
-RowPlan plan_rows(int64_t T, int nch) {
+RowPlan plan_rows(int64_t T, int nch, int min_vpt) {
   RowPlan p;
   if (nch <= 128) {  // one warp per row, eight rows per CTA
     p.ntr = 32;
     p.vpt = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
     p.rpc = 8;
   } else {
-    p.vpt = nch <= 1024 ? 2 : (nch <= 2048 ? 4 : 8);
+    p.vpt = min_vpt;
+    while (p.vpt < 8 && (nch + p.vpt - 1) / p.vpt > 512) p.vpt *= 2;
     const int per = (nch + p.vpt - 1) / p.vpt;
     p.ntr = (per + 31) / 32 * 32;
     p.rpc = p.ntr <= 128 ? 2 : 1;
   }
   p.grid = (T + p.rpc - 1) / p.rpc;
   return p;
+}
+
+// The persistent TMA kernel pays off for dynamic scales once every SM has
+// several rows to stream: it needs T >= 4 rows per SM and a row whose stage
+// ring (at least two stages) fits in shared memory.  Among the fits it takes the most CTAs
+// per SM (up to 1024 threads), then the most stages.
+bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, TmaPlan *out) {
+  const int nch = H / 8;
+  // static scales gain nothing from staging: the register kernel already
+  // streams at the copy roofline there
+  if (mode == VG_SCALE_STATIC || T < 4LL * sms || nch < 256) return false;
+  TmaPlan p;
+  p.vpt = mode == VG_SCALE_STATIC ? 2 : 4;
+  while (p.vpt < 8 && (nch + p.vpt - 1) / p.vpt > 256) p.vpt *= 2;
+  p.block = ((nch + p.vpt - 1) / p.vpt + 31) / 32 * 32;
+  const int slots = mode == VG_SCALE_STATIC ? 0 : (mode == VG_SCALE_PER_TOKEN ? 1 : ngroups);
+  const size_t per_sm = 220 * 1024;
+  for (int ctas = 4; ctas >= 1; --ctas) {
+    if (ctas * p.block > 1024) continue;
+    for (int stages = 4; stages >= 2; --stages) {
+      const size_t bytes = norm_tma_smem_bytes(H, res, stages, p.block, p.vpt, slots);
+      if (bytes <= kTmaMaxSmem && bytes * ctas <= per_sm) {
+        p.stages = stages;
+        p.grid = T < (int64_t)sms * ctas ? T : (int64_t)sms * ctas;
+        *out = p;
+        return true;
+      }
+    }
+  }
+  return false;
 }
 
 }  // namespace vg
@@ -81,7 +118,8 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
   if (vg::misaligned(q, 16) || vg::misaligned(x, 16) || vg::misaligned(weight, 16) ||
       vg::misaligned(residual, 16) || vg::misaligned(residual_out, 16) || vg::misaligned(scale, 4))
     return VG_ERR_MISALIGNED;
-  if ((st = vg::check_device()) != VG_OK) return st;
+  int sms = 0;
+  if ((st = vg::check_device(&sms)) != VG_OK) return st;
 
   vg::NormArgs a{};
   a.q = q;
@@ -97,7 +135,12 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
   a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(hidden / group_size) : 1;
   a.eps = eps;
   a.inv_h = 1.0f / (float)hidden;
-  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch);
+  vg::TmaPlan tp;
+  if (vg::plan_norm_tma(num_tokens, (int)hidden, residual != nullptr, mode, a.ngroups, sms, &tp))
+    return vg::launch_norm_fp8_tma(a, mode, tp, (cudaStream_t)stream) == cudaSuccess ? VG_OK
+                                                                                     : VG_ERR_CUDA;
+  // Dynamic scales do more work per row: more chunks per thread amortise it.
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, mode == VG_SCALE_STATIC ? 2 : 4);
   return vg::launch_norm_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                    : VG_ERR_CUDA;
 }
@@ -109,7 +152,8 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
   if (!q || !scale || !gate_up) return VG_ERR_NULL_PTR;
   if (vg::misaligned(q, 16) || vg::misaligned(gate_up, 16) || vg::misaligned(scale, 4))
     return VG_ERR_MISALIGNED;
-  if ((st = vg::check_device()) != VG_OK) return st;
+  int sms = 0;
+  if ((st = vg::check_device(&sms)) != VG_OK) return st;
 
   vg::SiluArgs a{};
   a.q = q;
@@ -120,7 +164,7 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
   a.nch = (int32_t)(inter / 8);
   a.gch = mode == VG_SCALE_PER_GROUP ? group_size / 8 : 1;
   a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(inter / group_size) : 1;
-  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch);
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, 2);
   return vg::launch_silu_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                  : VG_ERR_CUDA;
 }

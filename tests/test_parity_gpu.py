@@ -247,3 +247,23 @@ def test_cuda_graph_capture_matches_eager():
         torch.cuda.synchronize()
         for a, b in zip(eager, graphed):
             assert torch.equal(a, b)
+
+
+# ------------------------------------------------- exact dynamic norm scales
+
+EXACT = [(T, H, mode, G) for (T, H) in ((4096, 4096), (2048, 8192), (257, 2880), (96, 1024))
+         for mode, G in ((PER_TOKEN, 128), (PER_GROUP, 128), (PER_GROUP, 64))
+         if not (mode == PER_GROUP and H % G)]
+
+
+@pytest.mark.parametrize("T,H,mode,G", EXACT, ids=[f"{t}x{h}-m{m}-g{g}" for t, h, m, g in EXACT])
+def test_dynamic_norm_matches_oracle_exactly(T, H, mode, G):
+    """Stronger than the tolerance: the dynamic norm rounds its stored scale
+    exactly as the oracle does and breaks exact e4m3 ties the same way, so
+    scales agree bit for bit and codes agree everywhere (a double rounding
+    or an fp64-level coincidence may differ once in a long while)."""
+    d = gen.norm_inputs(T, H, seed=T + H + mode)
+    g, o, st = run_norm(d["x"], d["residual"], d["weight"], 1e-5, mode, G)
+    s_bad = int(np.sum(g["scale"].view(np.uint32) != o["scale"].view(np.uint32)))
+    assert s_bad <= max(1, g["scale"].size // 10000), s_bad
+    assert st["mismatch"] <= max(1, T * H // 1000000), st
