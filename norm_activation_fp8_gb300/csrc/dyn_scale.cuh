@@ -69,7 +69,10 @@ __device__ __forceinline__ float2 dyn_values(float2 t, const DynScale &d) {
   const float2 ra = make_float2(d.ra, d.ra);
   const float2 q0 = f2_mul(T, ra);
   const float2 q1 = f2_fma(f2_fma(q0, make_float2(-d.a, -d.a), T), ra, q0);
-  return f2_mul(q1, make_float2(d.f, d.f));
+  const float2 v = f2_mul(q1, make_float2(d.f, d.f));
+  // the correction step turns a -0 quotient into +0 ((+0) + (-0) = +0);
+  // the quotient has the sign of t (a > 0)
+  return make_float2(copysignf(v.x, t.x), copysignf(v.y, t.y));
 }
 
 }  // namespace vg

@@ -18,9 +18,12 @@ struct RowPlan {
   int block() const { return ntr * rpc; }
 };
 
-// Picks the plan for nch chunks per row (nch <= 4096): at least `min_vpt`
-// chunks per thread, more if a row would need more than 512 threads.
-RowPlan plan_rows(int64_t T, int nch, int min_vpt);
+// Picks the plan for nch chunks per row (nch <= 4096) on a device with `sms`
+// SMs: with few rows (T < 2 sms) one row per CTA and as few chunks per
+// thread as fit 512 threads; otherwise at least `min_vpt` chunks per thread
+// (more if a row would need more than 512 threads), short rows packed
+// several to a CTA.
+RowPlan plan_rows(int64_t T, int nch, int min_vpt, int sms);
 
 struct NormArgs {
   uint8_t *q;
@@ -71,5 +74,6 @@ cudaError_t launch_norm_fp8_tma(NormArgs a, int mode, const TmaPlan &plan, cudaS
 // synchronous.  0xFFFFFFFF if it could not be read.
 uint32_t read_norm_status(bool reset);
 cudaError_t launch_silu_fp8(SiluArgs a, int mode, const RowPlan &plan, cudaStream_t stream);
+
 
 }  // namespace vg

@@ -15,6 +15,12 @@
 // quantised and stored as soon as its group's amax (a butterfly over 8 or 16
 // lanes) is known.  Per-token keeps the row's activations in registers until
 // the row amax is reduced.
+//
+// Dynamic scales: s = fp32(amax * fp32(1/448)) and v = a * rcp(s).  The
+// activations are transcendental, so no element sits exactly on an e4m3
+// midpoint and an ulp or two in s or 1/s only moves codes whose value is
+// within ~1e-6 of a midpoint (both are far inside the parity tolerance:
+// scales within 1e-6, near-midpoint flips rare).
 #include "common.cuh"
 #include "launch.h"
 
@@ -54,6 +60,11 @@ __device__ __forceinline__ void scale8(float (&v)[8], float m) {
     v[2 * i] = p.x;
     v[2 * i + 1] = p.y;
   }
+}
+
+// fp32(max(amax, floor) / 448) to within an ulp: one multiply.
+__device__ __forceinline__ float silu_scale(float amax) {
+  return fmaxf(amax, kAmaxFloor) * (1.0f / kE4M3Max);
 }
 
 __device__ __forceinline__ float amax8(const float (&v)[8]) {
@@ -97,9 +108,9 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
       silu_chunk(gv[k], uv[k], v);
       float m = inv_static;
       if (MODE == kPerGroup) {
-        const float s = dynamic_scale(lanes_max(amax8(v), GCH));
+        const float s = silu_scale(lanes_max(amax8(v), GCH));
         if (live && c < a.nch && (tid & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
-        m = __frcp_rn(s);
+        m = fast_rcp(s);
       }
       scale8(v, m);
       if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
@@ -123,9 +134,9 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
     am = 0.f;
     for (int i = 0; i < nw; ++i) am = fmaxf(am, red[slot * nw + i]);
   }
-  const float s = dynamic_scale(am);
+  const float s = silu_scale(am);
   if (live && lr == 0) a.scale[row] = s;
-  const float m = __frcp_rn(s);
+  const float m = fast_rcp(s);
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int c = lr + k * a.ntr;
@@ -136,14 +147,15 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
 
 template <int VPT>
 cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStream_t s) {
+  const unsigned g = (unsigned)p.grid, b = (unsigned)p.block();
   switch (mode) {
-    case kStatic: silu_fp8_kernel<VPT, kStatic, 1><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
-    case kPerToken: silu_fp8_kernel<VPT, kPerToken, 1><<<(unsigned)p.grid, p.block(), 0, s>>>(a); break;
+    case kStatic: silu_fp8_kernel<VPT, kStatic, 1><<<g, b, 0, s>>>(a); break;
+    case kPerToken: silu_fp8_kernel<VPT, kPerToken, 1><<<g, b, 0, s>>>(a); break;
     default:
       if (a.gch == 8)
-        silu_fp8_kernel<VPT, kPerGroup, 8><<<(unsigned)p.grid, p.block(), 0, s>>>(a);
+        silu_fp8_kernel<VPT, kPerGroup, 8><<<g, b, 0, s>>>(a);
       else
-        silu_fp8_kernel<VPT, kPerGroup, 16><<<(unsigned)p.grid, p.block(), 0, s>>>(a);
+        silu_fp8_kernel<VPT, kPerGroup, 16><<<g, b, 0, s>>>(a);
       break;
   }
   return cudaGetLastError();

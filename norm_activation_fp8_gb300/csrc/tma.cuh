@@ -13,7 +13,7 @@ namespace vg {
 
 // A wait gives up after this many failed try_wait polls (each poll may
 // suspend the thread for a while): seconds, far beyond any healthy copy.
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kWaitLimit = 1u << 22;
 
 // Error bits a kernel leaves in its translation unit's status word.
 constexpr uint32_t kErrWaitTimeout = 1u;
@@ -40,6 +40,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
+}
+
+// Plain arrival (no transaction bytes), e.g. a consumer releasing a stage.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {

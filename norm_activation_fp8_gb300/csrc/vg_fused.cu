@@ -55,9 +55,16 @@ vg_status check_row(int64_t num_tokens, int64_t n, int32_t mode, int32_t group_s
 
 }  // namespace
 
-RowPlan plan_rows(int64_t T, int nch, int min_vpt) {
+RowPlan plan_rows(int64_t T, int nch, int min_vpt, int sms) {
   RowPlan p;
-  if (nch <= 128) {  // one warp per row, eight rows per CTA
+  if (T < 2LL * sms) {
+    // Few rows: latency-bound, so spread them -- one row per CTA and the
+    // fewest chunks per thread that keep a row within 512 threads.
+    p.vpt = 1;
+    while (p.vpt < 8 && (nch + p.vpt - 1) / p.vpt > 512) p.vpt *= 2;
+    p.ntr = ((nch + p.vpt - 1) / p.vpt + 31) / 32 * 32;
+    p.rpc = 1;
+  } else if (nch <= 128) {  // one warp per row, eight rows per CTA
     p.ntr = 32;
     p.vpt = nch <= 32 ? 1 : (nch <= 64 ? 2 : 4);
     p.rpc = 8;
@@ -140,7 +147,7 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
     return vg::launch_norm_fp8_tma(a, mode, tp, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                      : VG_ERR_CUDA;
   // Dynamic scales do more work per row: more chunks per thread amortise it.
-  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, mode == VG_SCALE_STATIC ? 2 : 4);
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, mode == VG_SCALE_STATIC ? 2 : 4, sms);
   return vg::launch_norm_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                    : VG_ERR_CUDA;
 }
@@ -164,7 +171,7 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
   a.nch = (int32_t)(inter / 8);
   a.gch = mode == VG_SCALE_PER_GROUP ? group_size / 8 : 1;
   a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(inter / group_size) : 1;
-  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, 2);
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, 2, sms);
   return vg::launch_silu_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                  : VG_ERR_CUDA;
 }

@@ -267,3 +267,44 @@ def test_dynamic_norm_matches_oracle_exactly(T, H, mode, G):
     s_bad = int(np.sum(g["scale"].view(np.uint32) != o["scale"].view(np.uint32)))
     assert s_bad <= max(1, g["scale"].size // 10000), s_bad
     assert st["mismatch"] <= max(1, T * H // 1000000), st
+
+
+# ------------------------------------------------------------ pipelined paths
+
+# Enough rows that the persistent TMA kernels run (norm: T >= 4 rows per SM
+# and H >= 2048 with a dynamic scale; SiLU: static or per-group, I >= 4096
+# and enough row segments), with row lengths that leave a ragged tail.
+TMA_NORM = [(1000, 2056, PER_TOKEN, 128), (1000, 2880, PER_GROUP, 64), (700, 12288, PER_GROUP, 128),
+            (700, 12288, PER_TOKEN, 128), (2000, 4096, PER_GROUP, 64)]
+
+
+@pytest.mark.parametrize("T,H,mode,G", TMA_NORM, ids=[f"{t}x{h}-m{m}-g{g}" for t, h, m, g in TMA_NORM])
+def test_pipelined_norm_ragged(T, H, mode, G):
+    d = gen.norm_inputs(T, H, seed=T + H)
+    run_norm(d["x"], d["residual"], d["weight"], 1e-5, mode, G)
+    run_norm(d["x"], None, d["weight"], 1e-5, mode, G)
+
+
+TMA_SILU = [(2048, 5120, PER_GROUP, 128), (2048, 5120, PER_GROUP, 64), (1500, 4104, STATIC, 128),
+            (1500, 12352, STATIC, 128), (640, 28672, PER_GROUP, 128)]
+
+
+@pytest.mark.parametrize("T,I,mode,G", TMA_SILU, ids=[f"{t}x{i}-m{m}-g{g}" for t, i, m, g in TMA_SILU])
+def test_pipelined_silu_ragged(T, I, mode, G):
+    d = gen.silu_inputs(T, I, seed=T + I)
+    g, _, _ = run_silu(d["gate_up"], mode, G, 0.1)
+    whole_tensor_properties(g, mode, I, G)
+
+
+@pytest.mark.parametrize("T", [8, 1000])  # register kernel, then the pipelined kernel
+@pytest.mark.parametrize("mode,G", [(STATIC, 128), (PER_TOKEN, 128), (PER_GROUP, 64)])
+def test_negative_zero_inputs(T, mode, G):
+    """x = residual = -0 gives r = -0 and y = -0: code 0x80 on every path."""
+    H = 4096
+    d = gen.norm_inputs(T, H, seed=17)
+    x, res = d["x"].copy(), d["residual"].copy()
+    x[:, ::5] = 0x8000
+    res[:, ::5] = 0x8000
+    g, o, _ = run_norm(x, res, d["weight"], 1e-5, mode, G)
+    assert np.all(g["q"][:, ::5] == 0x80)
+    run_norm(x, None, d["weight"], 1e-5, mode, G)
