@@ -200,8 +200,11 @@ def measured_peak():
 
 
 KERNEL_SOURCES = {
-    "norm": ["norm_activation_fp8_gb300/csrc/norm_fp8.cu", "norm_activation_fp8_gb300/csrc/common.cuh"],
-    "silu": ["norm_activation_fp8_gb300/csrc/silu_fp8.cu", "norm_activation_fp8_gb300/csrc/common.cuh"],
+    "norm": ["norm_activation_fp8_gb300/csrc/norm_fp8.cu", "norm_activation_fp8_gb300/csrc/common.cuh",
+             "norm_activation_fp8_gb300/csrc/dyn_scale.cuh", "norm_activation_fp8_gb300/csrc/tma.cuh",
+             "norm_activation_fp8_gb300/csrc/vg_fused.cu"],
+    "silu": ["norm_activation_fp8_gb300/csrc/silu_fp8.cu", "norm_activation_fp8_gb300/csrc/common.cuh",
+             "norm_activation_fp8_gb300/csrc/vg_fused.cu"],
 }
 
 
@@ -213,10 +216,11 @@ def kernel_source_hash(op: str) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(op: str, workload: str, launch_bytes: int):
+def profiled_traffic(op: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel
-    and workload, or None if there is none or the kernel changed since."""
-    path = os.path.join(ROOT, "profiles", f"{op}_{workload}.md")
+    and workload (profiles/<workload>.md), or None if there is none or the
+    kernel's source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -362,7 +366,7 @@ def run_gpu(args, dist):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                 "kernel": dom.name, "kernel_ms": round(dom_ms, 6),
-                "traffic": profiled_traffic(dom.op, dom.name, dom.algorithmic_bytes())}
+                "traffic": profiled_traffic(dom.op, dom.name)}
 
     e2e = None if args.no_e2e else run_e2e(torch, vg, step, host, weights, dev, stream, args,
                                           dist)
