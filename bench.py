@@ -78,6 +78,9 @@ def parse_args(argv=None):
                    help="seconds of untimed replays under clock sampling before the timed one")
     p.add_argument("--tokens", type=int, default=None,
                    help="override num_tokens of every op of the step (smaller profiling captures)")
+    p.add_argument("--sweep", action="store_true",
+                   help="instead of the step: time every point of the bandwidth sweep and the named "
+                        "single-op configs, one JSON record per point")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -551,9 +554,64 @@ def run_reference(args, dist):
     }
 
 
+def run_sweep(args):
+    """Per-point kernel throughput: K launches of one op (rotating buffer sets
+    larger than 3x L2) in one CUDA graph, timed with CUDA events."""
+    import torch
+    import norm_activation_fp8_gb300 as vg
+    from norm_activation_fp8_gb300 import build as vg_build
+    if not os.path.exists(vg_build.LIB_PATH):
+        vg_build.build()
+    vg.load()
+    dev = torch.device("cuda", 0)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 132 * 2 ** 20)
+    peak, peak_kind = measured_peak()
+    stream = torch.cuda.Stream(device=dev)
+    points = list(gen.NAMED.values()) + gen.sweep()
+    cache = {}
+    for w in points:
+        key = (w.op, w.T, w.n, w.x_dist)
+        if key not in cache:
+            cache.clear()
+            cache[key] = w.inputs()
+        host = cache[key]
+        nbytes = w.algorithmic_bytes()
+        n_sets = max(2, min(64, math.ceil(3 * l2 / nbytes)))
+        weights = {w.name: torch.from_numpy(host["weight"].view(np.int16)).to(dev)} if w.op == "norm" else {}
+        sets = [DeviceSet(torch, (w,), [host], weights, dev) for _ in range(n_sets)]
+        k_launch = max(args.steps, n_sets)
+        with torch.cuda.stream(stream):
+            for k in range(args.warmup):
+                launch(vg, sets[k % n_sets].ops[0])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(k_launch):
+                launch(vg, sets[k % n_sets].ops[0])
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            s0.record()
+            g.replay()
+            s1.record()
+        torch.cuda.synchronize()
+        us = s0.elapsed_time(s1) * 1e3 / k_launch
+        gbs = nbytes / (us * 1e-6) / 1e9
+        print(json.dumps({"point": w.name, "op": w.op, "T": w.T, "n": w.n,
+                          "mode": gen.MODE_NAMES[w.mode], "bytes": nbytes, "us": round(us, 3),
+                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                          "peak": peak, "peak_source": peak_kind,
+                          "tokens_per_s": round(w.T / (us * 1e-6), 1)}), flush=True)
+        del sets, g
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     rank, world, local = dist_setup(args)
+    if args.sweep:
+        return run_sweep(args) if rank == 0 else 0
     if args.impl == "reference":
         if rank != 0:
             return 0

@@ -15,6 +15,7 @@ struct RowPlan {
   int ntr;
   int rpc;
   int64_t grid;
+  int segs = 1;  // column segments per row (row-state-free SiLU modes only)
   int block() const { return ntr * rpc; }
 };
 
@@ -24,6 +25,7 @@ struct RowPlan {
 // (more if a row would need more than 512 threads), short rows packed
 // several to a CTA.
 RowPlan plan_rows(int64_t T, int nch, int min_vpt, int sms);
+RowPlan plan_silu(int64_t T, int nch, int mode, int sms);
 
 struct NormArgs {
   uint8_t *q;

@@ -74,13 +74,24 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
   return m;
 }
 
-template <int VPT, int MODE, int GCH>
-__global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
-  __shared__ float red[16];
+// A row is covered by ntr * VPT chunks per CTA.  Static and per-group modes
+// keep no row state, so longer rows are split into column segments
+// (blockIdx.y), independent CTAs.  Per-token needs the amax of the whole row
+// in one CTA: up to 1024 threads (BIG) with four chunks each.
+//
+// Register budget: static and per-group chunks hold no row state between
+// loads and stores, so they fit three 512-thread CTAs per SM; per-token
+// keeps its row's activations and fits two 512-thread or one 1024-thread
+// CTA.
+template <int VPT, int MODE, int GCH, bool BIG>
+__global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken ? 2 : 3))
+    silu_fp8_kernel(const SiluArgs a) {
+  __shared__ float red[32];
 
   const int tid = threadIdx.x;
   const int slot = tid / a.ntr;
-  const int lr = tid - slot * a.ntr;
+  const int lr0 = tid - slot * a.ntr;
+  const int lr = lr0 + (int)blockIdx.y * a.ntr * VPT;  // chunk offset of the segment
   const int64_t row = (int64_t)blockIdx.x * a.rpc + slot;
   const bool live = row < a.T;
   const int64_t in_base = live ? row * 2 * a.I : 0;
@@ -109,7 +120,7 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
       float m = inv_static;
       if (MODE == kPerGroup) {
         const float s = silu_scale(lanes_max(amax8(v), GCH));
-        if (live && c < a.nch && (tid & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
+        if (live && c < a.nch && (c & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
         m = fast_rcp(s);
       }
       scale8(v, m);
@@ -129,7 +140,7 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
   am = warp_max(am);
   if (a.ntr > 32) {
     const int nw = a.ntr >> 5;
-    if ((lr & 31) == 0) red[slot * nw + (lr >> 5)] = am;
+    if ((lr0 & 31) == 0) red[slot * nw + (lr0 >> 5)] = am;
     __syncthreads();
     am = 0.f;
     for (int i = 0; i < nw; ++i) am = fmaxf(am, red[slot * nw + i]);
@@ -147,15 +158,20 @@ __global__ void __launch_bounds__(512) silu_fp8_kernel(const SiluArgs a) {
 
 template <int VPT>
 cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStream_t s) {
-  const unsigned g = (unsigned)p.grid, b = (unsigned)p.block();
+  const dim3 g((unsigned)p.grid, (unsigned)p.segs), b((unsigned)p.block());
   switch (mode) {
-    case kStatic: silu_fp8_kernel<VPT, kStatic, 1><<<g, b, 0, s>>>(a); break;
-    case kPerToken: silu_fp8_kernel<VPT, kPerToken, 1><<<g, b, 0, s>>>(a); break;
+    case kStatic: silu_fp8_kernel<VPT, kStatic, 1, false><<<g, b, 0, s>>>(a); break;
+    case kPerToken:
+      if (p.block() > 512)
+        silu_fp8_kernel<VPT, kPerToken, 1, true><<<g, b, 0, s>>>(a);
+      else
+        silu_fp8_kernel<VPT, kPerToken, 1, false><<<g, b, 0, s>>>(a);
+      break;
     default:
       if (a.gch == 8)
-        silu_fp8_kernel<VPT, kPerGroup, 8><<<g, b, 0, s>>>(a);
+        silu_fp8_kernel<VPT, kPerGroup, 8, false><<<g, b, 0, s>>>(a);
       else
-        silu_fp8_kernel<VPT, kPerGroup, 16><<<g, b, 0, s>>>(a);
+        silu_fp8_kernel<VPT, kPerGroup, 16, false><<<g, b, 0, s>>>(a);
       break;
   }
   return cudaGetLastError();
@@ -169,8 +185,7 @@ cudaError_t launch_silu_fp8(SiluArgs a, int mode, const RowPlan &p, cudaStream_t
   switch (p.vpt) {
     case 1: return launch_mode<1>(a, mode, p, s);
     case 2: return launch_mode<2>(a, mode, p, s);
-    case 4: return launch_mode<4>(a, mode, p, s);
-    default: return launch_mode<8>(a, mode, p, s);
+    default: return launch_mode<4>(a, mode, p, s);
   }
 }
 

@@ -79,6 +79,36 @@ RowPlan plan_rows(int64_t T, int nch, int min_vpt, int sms) {
   return p;
 }
 
+// SiLU.  Static / per-group keep no row state: a row is cut into column
+// segments of at most 448 threads x VPT chunks (static four chunks a
+// thread, per-group two), each an independent CTA; rows of <= 64 chunks go
+// one warp per row, eight rows per CTA.  Per-token needs the row in one CTA:
+// four chunks a thread, up to 1024 threads (fewer chunks when that still
+// fits 448 threads).
+RowPlan plan_silu(int64_t T, int nch, int mode, int sms) {
+  (void)sms;
+  RowPlan p;
+  p.rpc = 1;
+  p.segs = 1;
+  if (mode == VG_SCALE_PER_TOKEN) {
+    p.vpt = 4;
+    while (p.vpt > 1 && (nch + p.vpt / 2 - 1) / (p.vpt / 2) <= 448) p.vpt /= 2;
+  } else if (nch <= 64) {
+    p.ntr = 32;
+    p.vpt = nch <= 32 ? 1 : 2;
+    p.rpc = 8;
+    p.grid = (T + p.rpc - 1) / p.rpc;
+    return p;
+  } else {
+    p.vpt = mode == VG_SCALE_STATIC ? 4 : 2;
+    p.segs = (nch + 448 * p.vpt - 1) / (448 * p.vpt);
+  }
+  const int per = (nch + p.segs * p.vpt - 1) / (p.segs * p.vpt);
+  p.ntr = (per + 31) / 32 * 32;
+  p.grid = T;
+  return p;
+}
+
 // The persistent TMA kernel pays off for dynamic scales once every SM has
 // several rows to stream: it needs T >= 4 rows per SM and a row whose stage
 // ring (at least two stages) fits in shared memory.  Among the fits it takes the most CTAs
@@ -171,7 +201,7 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
   a.nch = (int32_t)(inter / 8);
   a.gch = mode == VG_SCALE_PER_GROUP ? group_size / 8 : 1;
   a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(inter / group_size) : 1;
-  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, 2, sms);
+  const vg::RowPlan plan = vg::plan_silu(num_tokens, a.nch, mode, sms);
   return vg::launch_silu_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                  : VG_ERR_CUDA;
 }
