@@ -117,6 +117,20 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up,
                           int64_t num_tokens, int64_t inter, int32_t mode,
                           int32_t group_size, vg_stream_t stream);
 
+/*
+ * Device-side status of the library's kernels on the current device (no
+ * counterpart on the pages; the pipelined kernels' own failure report).
+ * Every wait in the library's kernels is bounded; a wait that gives up sets
+ * VG_DEVICE_WAIT_TIMEOUT here, waits (bounded) for its own copies and
+ * returns, so the context stays usable and the outputs of that call are
+ * not valid.  Writes the flags seen since the last reset to *flags and,
+ * if reset != 0, clears them.  Synchronous (it reads device memory); not
+ * for use inside stream capture.  Returns VG_ERR_NULL_PTR, VG_ERR_CUDA or
+ * VG_OK.
+ */
+#define VG_DEVICE_WAIT_TIMEOUT 1u
+vg_status vg_device_status(uint32_t *flags, int32_t reset);
+
 /* Static English text for a status code (never NULL). */
 const char *vg_status_string(vg_status status);
 

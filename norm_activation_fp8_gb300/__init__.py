@@ -31,8 +31,9 @@ STATUS_NAMES = {
     4: "VG_ERR_BAD_MODE", 5: "VG_ERR_BAD_GROUP", 6: "VG_ERR_UNSUPPORTED_DEVICE", 7: "VG_ERR_CUDA",
 }
 
-EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_status_string",
-                    "vg_abi_version")
+EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_device_status",
+                    "vg_status_string", "vg_abi_version")
+DEVICE_WAIT_TIMEOUT = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +69,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.vg_status_string.restype = ctypes.c_char_p
         lib.vg_abi_version.argtypes = []
         lib.vg_abi_version.restype = i32
+        lib.vg_device_status.argtypes = [P, i32]
+        lib.vg_device_status.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -158,6 +161,15 @@ def vg_silu_mul_fp8(q, scale, gate_up, mode: int, group_size: int = 128, stream=
                                 _ptr(gate_up, bf16, "gate_up"), num_tokens, inter, mode,
                                 group_size, _stream(stream))
     _check(st)
+
+
+def vg_device_status(reset: bool = False) -> int:
+    """Flags the library's kernels left on the current device
+    (DEVICE_WAIT_TIMEOUT: a bounded wait gave up; that call's outputs are
+    not valid).  Synchronous."""
+    flags = ctypes.c_uint32(0)
+    _check(load().vg_device_status(ctypes.byref(flags), 1 if reset else 0))
+    return flags.value
 
 
 # ------------------------------------------------- allocating wrappers

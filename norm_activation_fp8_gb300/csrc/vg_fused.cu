@@ -206,6 +206,14 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
                                                                                  : VG_ERR_CUDA;
 }
 
+vg_status vg_device_status(uint32_t *flags, int32_t reset) {
+  if (!flags) return VG_ERR_NULL_PTR;
+  const uint32_t v = vg::read_norm_status(reset != 0);
+  if (v == 0xFFFFFFFFu) return VG_ERR_CUDA;
+  *flags = v;
+  return VG_OK;
+}
+
 const char *vg_status_string(vg_status s) {
   switch (s) {
     case VG_OK: return "ok";

@@ -126,3 +126,7 @@ def test_binding_rejects_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         vg.load(str(tmp_path / "absent.so"))
+
+
+def test_device_status_rejects_null(lib):
+    assert lib.vg_device_status(None, 0) == NULL

@@ -308,3 +308,12 @@ def test_negative_zero_inputs(T, mode, G):
     g, o, _ = run_norm(x, res, d["weight"], 1e-5, mode, G)
     assert np.all(g["q"][:, ::5] == 0x80)
     run_norm(x, None, d["weight"], 1e-5, mode, G)
+
+
+def test_device_status_clean_after_runs():
+    """No bounded wait gave up in any of the runs above (or in these)."""
+    import norm_activation_fp8_gb300 as vg
+    d = gen.norm_inputs(1000, 4096, seed=3)
+    run_norm(d["x"], d["residual"], d["weight"], 1e-5, PER_GROUP, 128)
+    assert vg.vg_device_status(reset=True) == 0
+    assert vg.vg_device_status() == 0
