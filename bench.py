@@ -22,7 +22,8 @@ Timing (device, CUDA events on the launching stream):
   * clocks are sampled by nvidia-smi over a window of untimed replays of the
     same graph just before the timed one, through the per-kernel replays.
 e2e repeats the step through the C ABI from pinned HOST buffers: every step
-copies its inputs host->device and reads every output back device->host.
+copies its inputs host->device and reads every output back device->host,
+pipelined over three streams as a serving loop would overlap them.
 --impl reference times the fp64 CPU oracle on the host cores instead.
 
 Prints ONE JSON line (rank 0).
@@ -71,6 +72,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("vg", "reference"), default="vg")
     p.add_argument("--workload", choices=sorted(STEPS), default=DEFAULT_STEP)
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-large-token", action="store_true",
+                   help="skip timing the large-token single-op configs after the step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="bound on the oracle's CPU-baseline sample")
@@ -376,6 +379,11 @@ def run_gpu(args, dist):
     cpu = None
     if not args.no_cpu_baseline and dist.rank == 0 and dist.world == 1:
         cpu = run_cpu_baseline(step, host, args.cpu_seconds)
+    large = None
+    if not args.no_large_token and dist.rank == 0 and args.tokens is None:
+        del sets
+        torch.cuda.empty_cache()
+        large = run_large_token(torch, vg, dev, stream, args, l2)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
@@ -402,6 +410,7 @@ def run_gpu(args, dist):
         "e2e": e2e,
         "gpu_launches": len(step) * args.steps,
         "clocks": clk,
+        "large_token": large,
     }
     return line
 
@@ -421,53 +430,139 @@ def describe(w):
             "bytes": w.algorithmic_bytes()}
 
 
-def run_e2e(torch, vg, step, host, weights, dev, stream, args, dist):
-    """The step through the C ABI from pinned host buffers: H2D of every
-    input, the two calls, D2H of every output, each step."""
-    dset = DeviceSet(torch, step, host, weights, dev)
-    pins_in, pins_out = [], []
-    h2d = d2h = 0
-    for op, h in zip(dset.ops, host):
-        if op["w"].op == "norm":
-            srcs = [(torch.from_numpy(h["x"].view(np.int16)).pin_memory(), op["x"]),
-                    (torch.from_numpy(h["residual"].view(np.int16)).pin_memory(), op["res"])]
-            dsts = [op["q"], op["res"]]
-        else:
-            srcs = [(torch.from_numpy(h["gate_up"].view(np.int16)).pin_memory(), op["gate_up"])]
-            dsts = [op["q"]]
-        if op["w"].mode != gen.STATIC:
-            dsts.append(op["scale"])
-        pins_in.append(srcs)
-        outs = [(d, torch.empty(d.shape, dtype=d.dtype, pin_memory=True)) for d in dsts]
-        pins_out.append(outs)
-        h2d += sum(s.numel() * s.element_size() for s, _ in srcs)
-        d2h += sum(d.numel() * d.element_size() for d, _ in outs)
+class PackedSet:
+    r"""One step's device tensors laid out in a single buffer so that the
+    step's inputs are one contiguous span and its outputs another:
 
-    def one_step():
-        for op, srcs, outs in zip(dset.ops, pins_in, pins_out):
-            for s, d in srcs:
-                d.copy_(s, non_blocking=True)
-            launch(vg, op)
-            for d, hbuf in outs:
-                hbuf.copy_(d, non_blocking=True)
+        [ x | gate_up | residual | q_norm | scale_norm | q_act | scale_act ]
+          \______ inputs (host->device) ____/
+                             \______________ outputs (device->host) ______/
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            one_step()
+    The residual, updated in place, ends the input span and starts the
+    output span.  Every tensor starts on a 256-byte boundary."""
+
+    def __init__(self, torch, step, host, weights, dev):
+        norm = next(w for w in step if w.op == "norm")
+        act = next(w for w in step if w.op == "silu")
+        self.norm_w, self.act_w = norm, act
+        parts = [("x", norm.T * norm.n * 2), ("gate_up", act.T * 2 * act.n * 2),
+                 ("res", norm.T * norm.n * 2), ("q_norm", norm.T * norm.n),
+                 ("s_norm", 4 * self._scales(norm)), ("q_act", act.T * act.n),
+                 ("s_act", 4 * self._scales(act))]
+        off, self.off = 0, {}
+        for name, nb in parts:
+            self.off[name] = (off, nb)
+            off += (nb + 255) // 256 * 256
+        self.total = off
+        self.dev_buf = torch.empty(off, dtype=torch.uint8, device=dev)
+        self.in_span = (self.off["x"][0], self.off["res"][0] + self.off["res"][1])
+        self.out_span = (self.off["res"][0], self.off["s_act"][0] + self.off["s_act"][1])
+        v = self.view
+        self.ops = [
+            dict(w=norm, x=v(torch, "x", torch.int16, (norm.T, norm.n)),
+                 res=v(torch, "res", torch.int16, (norm.T, norm.n)),
+                 q=v(torch, "q_norm", torch.uint8, (norm.T, norm.n)),
+                 scale=v(torch, "s_norm", torch.float32, (self._scales(norm),)),
+                 weight=weights[norm.name]),
+            dict(w=act, gate_up=v(torch, "gate_up", torch.int16, (act.T, 2 * act.n)),
+                 q=v(torch, "q_act", torch.uint8, (act.T, act.n)),
+                 scale=v(torch, "s_act", torch.float32, (self._scales(act),))),
+        ]
+        for op in self.ops:
+            if op["w"].mode == gen.STATIC:
+                op["scale"].fill_(op["w"].static_scale)
+
+    @staticmethod
+    def _scales(w):
+        return {gen.STATIC: 1, gen.PER_TOKEN: w.T}.get(w.mode, w.T * (w.n // w.group_size))
+
+    def view(self, torch, name, dtype, shape):
+        o, nb = self.off[name]
+        return self.dev_buf[o:o + nb].view(dtype).view(shape)
+
+    def host_inputs(self, torch, host):
+        """Pinned host image of the input span, filled with the step's inputs."""
+        lo, hi = self.in_span
+        img = torch.zeros(hi - lo, dtype=torch.uint8, pin_memory=True)
+        hn = next(h for w, h in zip((self.norm_w, self.act_w), host) if "x" in h)
+        ha = next(h for h in host if "gate_up" in h)
+        for name, arr in (("x", hn["x"]), ("gate_up", ha["gate_up"]), ("res", hn["residual"])):
+            o, nb = self.off[name]
+            img[o - lo:o - lo + nb].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
+        return img
+
+
+def run_e2e(torch, vg, step, host, weights, dev, stream, args, dist, ring=3):
+    """The step through the C ABI from pinned host buffers, pipelined the
+    way a serving loop would run it: every step uploads all its inputs
+    (one host->device copy of the input span, stream 1), runs the two calls
+    (stream 2) and reads every output back (one device->host copy of the
+    output span, stream 3).  A ring of `ring` device buffer sets lets step
+    k+1 upload and step k-1 download while step k computes; events order
+    each set's reuse."""
+    if sorted(w.op for w in step) != ["norm", "silu"]:
+        return None
+    sets = [PackedSet(torch, step, host, weights, dev) for _ in range(ring)]
+    h_in = sets[0].host_inputs(torch, host)
+    lo_o, hi_o = sets[0].out_span
+    h_out = [torch.empty(hi_o - lo_o, dtype=torch.uint8, pin_memory=True) for _ in range(ring)]
+    h2d, d2h = h_in.numel(), hi_o - lo_o
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def run(nsteps):
+        freed = [None] * ring
+        for k in range(nsteps):
+            b = k % ring
+            ps = sets[b]
+            up, done, fr = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                if freed[b] is not None:
+                    s_in.wait_event(freed[b])
+                lo, hi = ps.in_span
+                ps.dev_buf[lo:hi].copy_(h_in, non_blocking=True)
+                up.record(s_in)
+            with torch.cuda.stream(stream):
+                stream.wait_event(up)
+                for op in ps.ops:
+                    launch(vg, op)
+                done.record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                h_out[b].copy_(ps.dev_buf[lo_o:hi_o], non_blocking=True)
+                fr.record(s_out)
+            freed[b] = fr
+
+    run(args.warmup)
     torch.cuda.synchronize()
     dist.barrier()
     s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        s0.record()
-        for _ in range(args.steps):
-            one_step()
-        s1.record()
+    s0.record(s_in)
+    with torch.cuda.stream(s_out):
+        s_out.wait_event(s0)
+    run(args.steps)
+    s1.record(s_out)
     torch.cuda.synchronize()
     dist.barrier()
     ms = dist.max(s0.elapsed_time(s1))
+    # self-check of the packing: the last downloaded outputs equal a fresh,
+    # unpacked run of the same inputs
+    ref = DeviceSet(torch, step, host, weights, dev)
+    with torch.cuda.stream(stream):
+        for op in ref.ops:
+            launch(vg, op)
+    torch.cuda.synchronize()
+    last = h_out[(args.steps - 1) % ring]
+    for name, op in (("q_norm", ref.ops[0] if ref.ops[0]["w"].op == "norm" else ref.ops[1]),
+                     ("q_act", ref.ops[0] if ref.ops[0]["w"].op == "silu" else ref.ops[1])):
+        o, nb = sets[0].off[name]
+        got = last[o - lo_o:o - lo_o + nb]
+        if not torch.equal(got, op["q"].reshape(-1).cpu()):
+            raise RuntimeError(f"e2e output span check failed for {name}")
     value = step_bytes(step) * args.steps * dist.world / (ms * 1e-3) / 1e9
-    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms / args.steps, 6)}
+    return {"value": round(value, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(ms / args.steps, 6),
+            "pipeline": f"{ring}-deep ring; per step one host->device copy of the input span, "
+                        "the two calls, one device->host copy of the output span, on three streams"}
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -554,9 +649,46 @@ def run_reference(args, dist):
     }
 
 
+def time_op_point(torch, vg, w, host, dev, stream, steps, warmup, l2):
+    """Mean duration (us) of one op's launches: K launches over rotating
+    buffer sets (together > 3x L2) in one CUDA graph, CUDA events."""
+    nbytes = w.algorithmic_bytes()
+    n_sets = max(2, min(64, math.ceil(3 * l2 / nbytes)))
+    weights = {w.name: torch.from_numpy(host["weight"].view(np.int16)).to(dev)} if w.op == "norm" else {}
+    sets = [DeviceSet(torch, (w,), [host], weights, dev) for _ in range(n_sets)]
+    k_launch = max(steps, n_sets)
+    with torch.cuda.stream(stream):
+        for k in range(warmup):
+            launch(vg, sets[k % n_sets].ops[0])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for k in range(k_launch):
+            launch(vg, sets[k % n_sets].ops[0])
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+        s0.record()
+        g.replay()
+        s1.record()
+    torch.cuda.synchronize()
+    us = s0.elapsed_time(s1) * 1e3 / k_launch
+    del sets, g
+    torch.cuda.empty_cache()
+    return us
+
+
+def point_record(w, us, peak, peak_kind):
+    nbytes = w.algorithmic_bytes()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"point": w.name, "op": w.op, "T": w.T, "n": w.n, "mode": gen.MODE_NAMES[w.mode],
+            "bytes": nbytes, "us": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "peak": peak, "peak_source": peak_kind, "tokens_per_s": round(w.T / (us * 1e-6), 1)}
+
+
 def run_sweep(args):
-    """Per-point kernel throughput: K launches of one op (rotating buffer sets
-    larger than 3x L2) in one CUDA graph, timed with CUDA events."""
+    """Per-point kernel throughput of the bandwidth sweep and the named
+    single-op configs, one JSON record per point."""
     import torch
     import norm_activation_fp8_gb300 as vg
     from norm_activation_fp8_gb300 import build as vg_build
@@ -567,44 +699,28 @@ def run_sweep(args):
     l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 132 * 2 ** 20)
     peak, peak_kind = measured_peak()
     stream = torch.cuda.Stream(device=dev)
-    points = list(gen.NAMED.values()) + gen.sweep()
     cache = {}
-    for w in points:
+    for w in list(gen.NAMED.values()) + gen.sweep():
         key = (w.op, w.T, w.n, w.x_dist)
         if key not in cache:
             cache.clear()
             cache[key] = w.inputs()
-        host = cache[key]
-        nbytes = w.algorithmic_bytes()
-        n_sets = max(2, min(64, math.ceil(3 * l2 / nbytes)))
-        weights = {w.name: torch.from_numpy(host["weight"].view(np.int16)).to(dev)} if w.op == "norm" else {}
-        sets = [DeviceSet(torch, (w,), [host], weights, dev) for _ in range(n_sets)]
-        k_launch = max(args.steps, n_sets)
-        with torch.cuda.stream(stream):
-            for k in range(args.warmup):
-                launch(vg, sets[k % n_sets].ops[0])
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(k_launch):
-                launch(vg, sets[k % n_sets].ops[0])
-        torch.cuda.synchronize()
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            s0.record()
-            g.replay()
-            s1.record()
-        torch.cuda.synchronize()
-        us = s0.elapsed_time(s1) * 1e3 / k_launch
-        gbs = nbytes / (us * 1e-6) / 1e9
-        print(json.dumps({"point": w.name, "op": w.op, "T": w.T, "n": w.n,
-                          "mode": gen.MODE_NAMES[w.mode], "bytes": nbytes, "us": round(us, 3),
-                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                          "peak": peak, "peak_source": peak_kind,
-                          "tokens_per_s": round(w.T / (us * 1e-6), 1)}), flush=True)
-        del sets, g
-        torch.cuda.empty_cache()
+        us = time_op_point(torch, vg, w, cache[key], dev, stream, args.steps, args.warmup, l2)
+        print(json.dumps(point_record(w, us, peak, peak_kind)), flush=True)
     return 0
+
+
+def run_large_token(torch, vg, dev, stream, args, l2):
+    """The large-token single-op configs (the >= 80 % roofline gate), timed
+    after the step in the same run, for context next to the step line."""
+    peak, peak_kind = measured_peak()
+    out = []
+    for w in (gen.CFG2A, gen.CFG2B, gen.CFG3):
+        us = time_op_point(torch, vg, w, w.inputs(), dev, stream, max(8, args.steps // 10),
+                           args.warmup, l2)
+        r = point_record(w, us, peak, peak_kind)
+        out.append({k: r[k] for k in ("point", "us", "GB/s", "frac")})
+    return out
 
 
 def main(argv=None):
