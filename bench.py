@@ -59,8 +59,9 @@ STEPS = {
     "llama3_8b_decode": (gen.CFG1, gen.CFG1_ACT),
     "llama3_70b_prefill": (gen.CFG3, CFG3_ACT),
 }
-# every named single-op workload is also a (one-op) step
+# every named single-op workload and every sweep point is also a (one-op) step
 STEPS.update({name: (w,) for name, w in gen.NAMED.items()})
+STEPS.update({w.name: (w,) for w in gen.sweep()})
 DEFAULT_STEP = "llama3_8b_decode"
 
 
