@@ -68,7 +68,17 @@ struct TmaPlan {
   int stages;
   int64_t grid;
 };
-constexpr size_t kTmaMaxSmem = 227 * 1024;  // opt-in limit per CTA
+constexpr size_t kTmaMaxSmem = 227 * 1024;  // opt-in limit per CTA (static + dynamic)
+
+// Lets `kern` use dynamic shared memory up to the opt-in limit minus its own
+// static shared memory (asking for more fails the call).
+inline cudaError_t opt_in_dynamic_smem(const void *kern) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)(kTmaMaxSmem - fa.sharedSizeBytes));
+}
 size_t norm_tma_smem_bytes(int H, bool res, int stages, int block, int vpt, int slots);
 cudaError_t launch_norm_fp8_tma(NormArgs a, int mode, const TmaPlan &plan, cudaStream_t stream);
 
@@ -77,5 +87,17 @@ cudaError_t launch_norm_fp8_tma(NormArgs a, int mode, const TmaPlan &plan, cudaS
 uint32_t read_norm_status(bool reset);
 cudaError_t launch_silu_fp8(SiluArgs a, int mode, const RowPlan &plan, cudaStream_t stream);
 
+
+// Persistent TMA-staged per-token SiLU kernel: `grid` CTAs of `block`
+// threads (vpt chunks each), one row at a time in `nseg` staged segments.
+struct SiluTmaPlan {
+  int vpt;
+  int block;
+  int nseg;  // column segments of a row, one stage each (1 or 2)
+  int64_t grid;
+};
+size_t silu_tma_token_smem_bytes(int I, int nseg);
+cudaError_t launch_silu_fp8_tma_token(SiluArgs a, const SiluTmaPlan &plan, cudaStream_t stream);
+uint32_t read_silu_status(bool reset);
 
 }  // namespace vg

@@ -367,7 +367,7 @@ cudaError_t launch_tma_res(const NormArgs &a, const TmaPlan &p, cudaStream_t s) 
   if (e != cudaSuccess) return e;
   const uint64_t bit = 1ull << (dev & 63);
   if (!(opted_in.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTmaMaxSmem);
+    e = opt_in_dynamic_smem(reinterpret_cast<const void *>(kern));
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit, std::memory_order_release);
   }

@@ -21,10 +21,17 @@
 // midpoint and an ulp or two in s or 1/s only moves codes whose value is
 // within ~1e-6 of a midpoint (both are far inside the parity tolerance:
 // scales within 1e-6, near-midpoint flips rare).
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
+#include "tma.cuh"
 
 namespace vg {
+
+// Status word of this translation unit's kernels (kErrWaitTimeout).
+__device__ uint32_t g_silu_status;
+
 namespace {
 
 __device__ __forceinline__ float fast_rcp(float x) {
@@ -156,6 +163,124 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
   }
 }
 
+// ------------------------------------------------ TMA per-token kernel
+//
+// Persistent CTAs, one row at a time, for per-token rows at large T.  A row
+// is NSEG column segments; segment s of the current row sits in stage s of
+// shared memory (its gate part, then its up part), copied by two bulk TMA
+// copies.  As soon as every thread has pulled segment s's activations into
+// registers, the stage is refilled with segment s of the next row, so the
+// copies overlap the rest of pass 1, the amax reduction, the quantisation
+// and the stores.  NSEG = 2 keeps a 112 KB row (I = 28672) within one SM's
+// shared memory while still overlapping its copy with compute.  Dynamic
+// shared memory: NSEG stages, then NSEG full mbarriers.
+
+template <int VPT, bool BIG, int NSEG>
+__global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
+    silu_fp8_tma_token_kernel(const SiluArgs a) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ float red[2][32];
+  constexpr int KS = VPT / NSEG;                      // chunks per thread per segment
+  const int seg_ch = a.nch / NSEG;                     // chunks per segment
+  const uint32_t seg_bytes = 16u * (uint32_t)seg_ch;   // one half (gate or up) of a stage
+  uint64_t *full = reinterpret_cast<uint64_t *>(dsm + (size_t)NSEG * 2 * seg_bytes);
+  const int tid = threadIdx.x;
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+
+  auto issue = [&](int sg, int64_t row) {
+    unsigned char *st = dsm + (size_t)sg * 2 * seg_bytes;
+    const uint16_t *src = a.gate_up + row * 2 * a.I + (int64_t)sg * seg_ch * kElemsPerChunk;
+    mbar_arrive_expect_tx(&full[sg], 2 * seg_bytes);
+    tma_load_bulk(st, src, seg_bytes, &full[sg]);
+    tma_load_bulk(st + seg_bytes, src + a.I, seg_bytes, &full[sg]);
+  };
+  if (tid == 0) {
+    for (int sg = 0; sg < NSEG; ++sg) mbar_init(&full[sg], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0 && first < a.T)
+    for (int sg = 0; sg < NSEG; ++sg) issue(sg, first);
+
+  bool failed = false;
+  int fail_sg = 0;      // the segment whose wait gave up
+  bool ahead = false;   // stages before fail_sg already hold the next row's copies
+  int64_t i = 0;
+  for (int64_t row = first; row < a.T && !failed; row += stride, ++i) {
+    float act[VPT][8];
+    float am = 0.f;
+#pragma unroll
+    for (int sg = 0; sg < NSEG; ++sg) {
+      const unsigned char *st = dsm + (size_t)sg * 2 * seg_bytes;
+      const bool ok = mbar_wait_bounded(&full[sg], (uint32_t)(i & 1));
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        const int c = tid + k * a.ntr;  // chunk within the segment
+        const uint4 gv = (ok && c < seg_ch) ? lds128(st + c * 16) : make_uint4(0, 0, 0, 0);
+        const uint4 uv = (ok && c < seg_ch) ? lds128(st + seg_bytes + c * 16) : make_uint4(0, 0, 0, 0);
+        silu_chunk(gv, uv, act[sg * KS + k]);
+        am = fmaxf(am, amax8(act[sg * KS + k]));
+      }
+      // every thread has read segment sg: refill its stage with the next row
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        fail_sg = sg;
+        ahead = row + stride < a.T;
+        break;
+      }
+      if (tid == 0 && row + stride < a.T) {
+        fence_proxy_async_smem();
+        issue(sg, row + stride);
+      }
+    }
+    if (failed) break;
+    am = warp_max(am);
+    float *r = red[i & 1];
+    if ((tid & 31) == 0) r[tid >> 5] = am;
+    __syncthreads();
+    am = 0.f;
+    for (int w = 0; w < (a.ntr >> 5); ++w) am = fmaxf(am, r[w]);
+    const float s = silu_scale(am);
+    if (tid == 0) a.scale[row] = s;
+    const float m = fast_rcp(s);
+    const int64_t out_base = row * a.I;
+#pragma unroll
+    for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+      for (int k = 0; k < KS; ++k) {
+        const int c = tid + k * a.ntr;
+        scale8(act[sg * KS + k], m);
+        if (c < seg_ch)
+          st_stream(a.q + out_base + ((int64_t)sg * seg_ch + c) * kElemsPerChunk,
+                    quant8(act[sg * KS + k]));
+      }
+  }
+  if (failed && tid == 0) {
+    atomicOr(&g_silu_status, kErrWaitTimeout);
+    // the copies this CTA may still have in flight: one per stage, of the
+    // next row for stages already refilled, else of the current row
+    for (int sg = 0; sg < NSEG; ++sg)
+      mbar_wait_bounded(&full[sg], (uint32_t)((i + (sg < fail_sg && ahead ? 1 : 0)) & 1));
+  }
+}
+
+template <int VPT, bool BIG, int NSEG>
+cudaError_t launch_tma_token(const SiluArgs &a, const SiluTmaPlan &p, cudaStream_t s) {
+  auto kern = silu_fp8_tma_token_kernel<VPT, BIG, NSEG>;
+  static std::atomic<uint64_t> opted_in{0};  // once per instantiation and device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(opted_in.load(std::memory_order_acquire) & bit)) {
+    e = opt_in_dynamic_smem(reinterpret_cast<const void *>(kern));
+    if (e != cudaSuccess) return e;
+    opted_in.fetch_or(bit, std::memory_order_release);
+  }
+  kern<<<(unsigned)p.grid, p.block, silu_tma_token_smem_bytes(a.I, NSEG), s>>>(a);
+  return cudaGetLastError();
+}
+
 template <int VPT>
 cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStream_t s) {
   const dim3 g((unsigned)p.grid, (unsigned)p.segs), b((unsigned)p.block());
@@ -178,6 +303,30 @@ cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStrea
 }
 
 }  // namespace
+
+size_t silu_tma_token_smem_bytes(int I, int nseg) { return (size_t)4 * I + 8 * (size_t)nseg; }
+
+cudaError_t launch_silu_fp8_tma_token(SiluArgs a, const SiluTmaPlan &p, cudaStream_t s) {
+  a.ntr = p.block;
+  a.rpc = 1;
+  if (p.nseg == 2)  // four chunks a thread, two per segment
+    return p.block > 512 ? launch_tma_token<4, true, 2>(a, p, s) : launch_tma_token<4, false, 2>(a, p, s);
+  switch (p.vpt) {
+    case 1: return p.block > 512 ? launch_tma_token<1, true, 1>(a, p, s) : launch_tma_token<1, false, 1>(a, p, s);
+    case 2: return p.block > 512 ? launch_tma_token<2, true, 1>(a, p, s) : launch_tma_token<2, false, 1>(a, p, s);
+    default: return p.block > 512 ? launch_tma_token<4, true, 1>(a, p, s) : launch_tma_token<4, false, 1>(a, p, s);
+  }
+}
+
+uint32_t read_silu_status(bool reset) {
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_silu_status, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (reset) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_silu_status, &zero, sizeof(zero)) != cudaSuccess) return 0xFFFFFFFFu;
+  }
+  return v;
+}
 
 cudaError_t launch_silu_fp8(SiluArgs a, int mode, const RowPlan &p, cudaStream_t s) {
   a.ntr = p.ntr;

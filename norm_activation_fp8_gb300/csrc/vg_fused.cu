@@ -41,6 +41,11 @@ vg_status check_device(int *sms) {
   return st == 1 ? VG_OK : VG_ERR_UNSUPPORTED_DEVICE;
 }
 
+// Each launch reports its own error through cudaGetLastError(); clear any
+// earlier, non-sticky error of this library's runtime first so it is not
+// blamed on this call (a sticky, context-level error comes back anyway).
+inline void clear_stale_error() { (void)cudaGetLastError(); }
+
 inline bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
 
 vg_status check_row(int64_t num_tokens, int64_t n, int32_t mode, int32_t group_size) {
@@ -109,6 +114,24 @@ RowPlan plan_silu(int64_t T, int nch, int mode, int sms) {
   return p;
 }
 
+// Per-token SiLU at large T streams through the persistent TMA kernel.  A
+// row of up to 448 x 4 chunks is one stage, two CTAs per SM; a longer row
+// (a multiple of 16 columns) is two half-row stages in one CTA of up to 1024
+// threads, so each half's copy overlaps work on the other.
+bool plan_silu_tma_token(int64_t T, int nch, int mode, int sms, SiluTmaPlan *out) {
+  if (mode != VG_SCALE_PER_TOKEN || T < 4LL * sms || nch < 512) return false;
+  SiluTmaPlan p;
+  p.vpt = 4;
+  p.nseg = (nch > 448 * 4 && nch % 2 == 0) ? 2 : 1;
+  p.block = ((nch / p.nseg + p.vpt / p.nseg - 1) / (p.vpt / p.nseg) + 31) / 32 * 32;
+  const size_t smem = silu_tma_token_smem_bytes(nch * 8, p.nseg);
+  if (smem > kTmaMaxSmem - 1024 || p.block > 1024) return false;
+  const int ctas = (p.block <= 512 && 2 * smem <= 220 * 1024) ? 2 : 1;
+  p.grid = T < (int64_t)sms * ctas ? T : (int64_t)sms * ctas;
+  *out = p;
+  return true;
+}
+
 // The persistent TMA kernel pays off for dynamic scales once every SM has
 // several rows to stream: it needs T >= 4 rows per SM and a row whose stage
 // ring (at least two stages) fits in shared memory.  Among the fits it takes the most CTAs
@@ -157,6 +180,7 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
     return VG_ERR_MISALIGNED;
   int sms = 0;
   if ((st = vg::check_device(&sms)) != VG_OK) return st;
+  vg::clear_stale_error();
 
   vg::NormArgs a{};
   a.q = q;
@@ -191,6 +215,7 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
     return VG_ERR_MISALIGNED;
   int sms = 0;
   if ((st = vg::check_device(&sms)) != VG_OK) return st;
+  vg::clear_stale_error();
 
   vg::SiluArgs a{};
   a.q = q;
@@ -201,6 +226,10 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
   a.nch = (int32_t)(inter / 8);
   a.gch = mode == VG_SCALE_PER_GROUP ? group_size / 8 : 1;
   a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(inter / group_size) : 1;
+  vg::SiluTmaPlan tp;
+  if (vg::plan_silu_tma_token(num_tokens, a.nch, mode, sms, &tp))
+    return vg::launch_silu_fp8_tma_token(a, tp, (cudaStream_t)stream) == cudaSuccess ? VG_OK
+                                                                                    : VG_ERR_CUDA;
   const vg::RowPlan plan = vg::plan_silu(num_tokens, a.nch, mode, sms);
   return vg::launch_silu_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                  : VG_ERR_CUDA;
@@ -208,9 +237,9 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
 
 vg_status vg_device_status(uint32_t *flags, int32_t reset) {
   if (!flags) return VG_ERR_NULL_PTR;
-  const uint32_t v = vg::read_norm_status(reset != 0);
-  if (v == 0xFFFFFFFFu) return VG_ERR_CUDA;
-  *flags = v;
+  const uint32_t v = vg::read_norm_status(reset != 0), w = vg::read_silu_status(reset != 0);
+  if (v == 0xFFFFFFFFu || w == 0xFFFFFFFFu) return VG_ERR_CUDA;
+  *flags = v | w;
   return VG_OK;
 }
 

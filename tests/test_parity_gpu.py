@@ -271,9 +271,10 @@ def test_dynamic_norm_matches_oracle_exactly(T, H, mode, G):
 
 # ------------------------------------------------------------ pipelined paths
 
-# Enough rows that the persistent TMA kernels run (norm: T >= 4 rows per SM
-# and H >= 2048 with a dynamic scale; SiLU: static or per-group, I >= 4096
-# and enough row segments), with row lengths that leave a ragged tail.
+# Shapes with long rows and ragged tails: norm rows that take the persistent
+# TMA kernel (T >= 4 rows per SM, H >= 2048, dynamic scale), SiLU rows cut
+# into column segments (static, per-group) and per-token SiLU rows that take
+# the persistent TMA kernel (T >= 4 rows per SM, I >= 4096).
 TMA_NORM = [(1000, 2056, PER_TOKEN, 128), (1000, 2880, PER_GROUP, 64), (700, 12288, PER_GROUP, 128),
             (700, 12288, PER_TOKEN, 128), (2000, 4096, PER_GROUP, 64)]
 
@@ -286,7 +287,10 @@ def test_pipelined_norm_ragged(T, H, mode, G):
 
 
 TMA_SILU = [(2048, 5120, PER_GROUP, 128), (2048, 5120, PER_GROUP, 64), (1500, 4104, STATIC, 128),
-            (1500, 12352, STATIC, 128), (640, 28672, PER_GROUP, 128)]
+            (1500, 12352, STATIC, 128), (640, 28672, PER_GROUP, 128),
+            (1000, 4104, PER_TOKEN, 128), (700, 28672, PER_TOKEN, 128), (1200, 12352, PER_TOKEN, 128),
+            (650, 32768, PER_TOKEN, 128), (640, 14344, PER_TOKEN, 128), (620, 14352, PER_TOKEN, 128),
+            (700, 18440, PER_TOKEN, 128)]
 
 
 @pytest.mark.parametrize("T,I,mode,G", TMA_SILU, ids=[f"{t}x{i}-m{m}-g{g}" for t, i, m, g in TMA_SILU])
