@@ -115,14 +115,15 @@ RowPlan plan_silu(int64_t T, int nch, int mode, int sms) {
 }
 
 // Per-token SiLU at large T streams through the persistent TMA kernel.  A
-// row of up to 448 x 4 chunks is one stage, two CTAs per SM; a longer row
-// (a multiple of 16 columns) is two half-row stages in one CTA of up to 1024
-// threads, so each half's copy overlaps work on the other.
+// row of at least 1024 chunks, an even number of them, is two half-row
+// stages, so each half's copy overlaps work on the other; other rows are one
+// stage.  Rows of up to 448 x 4 chunks run two CTAs per SM, longer ones one
+// CTA of up to 1024 threads.
 bool plan_silu_tma_token(int64_t T, int nch, int mode, int sms, SiluTmaPlan *out) {
   if (mode != VG_SCALE_PER_TOKEN || T < 4LL * sms || nch < 512) return false;
   SiluTmaPlan p;
   p.vpt = 4;
-  p.nseg = (nch > 448 * 4 && nch % 2 == 0) ? 2 : 1;
+  p.nseg = (nch >= 1024 && nch % 2 == 0) ? 2 : 1;
   p.block = ((nch / p.nseg + p.vpt / p.nseg - 1) / (p.vpt / p.nseg) + 31) / 32 * 32;
   const size_t smem = silu_tma_token_smem_bytes(nch * 8, p.nseg);
   if (smem > kTmaMaxSmem - 1024 || p.block > 1024) return false;
@@ -133,33 +134,32 @@ bool plan_silu_tma_token(int64_t T, int nch, int mode, int sms, SiluTmaPlan *out
 }
 
 // The persistent TMA kernel pays off for dynamic scales once every SM has
-// several rows to stream: it needs T >= 4 rows per SM and a row whose stage
-// ring (at least two stages) fits in shared memory.  Among the fits it takes the most CTAs
-// per SM (up to 1024 threads), then the most stages.
+// several rows to stream: it needs T >= 4 rows per SM and a row whose
+// two-stage ring fits in shared memory.  Measured on GB300 over H = 2048..8192
+// and T = 2048..32768: about 384 resident threads per SM with two stages per
+// CTA stream best.  Fewer threads leave the SM short of warps; more CTAs or
+// deeper rings keep more row copies in flight across the GPU than the memory
+// system serves well, and run slower.  When a CTA would get fewer than ten
+// rows, one more CTA of 128 threads or more evens out the tail.
 bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, TmaPlan *out) {
   const int nch = H / 8;
   // static scales gain nothing from staging: the register kernel already
   // streams at the copy roofline there
   if (mode == VG_SCALE_STATIC || T < 4LL * sms || nch < 256) return false;
   TmaPlan p;
-  p.vpt = mode == VG_SCALE_STATIC ? 2 : 4;
+  p.vpt = 4;
   while (p.vpt < 8 && (nch + p.vpt - 1) / p.vpt > 256) p.vpt *= 2;
   p.block = ((nch + p.vpt - 1) / p.vpt + 31) / 32 * 32;
-  const int slots = mode == VG_SCALE_STATIC ? 0 : (mode == VG_SCALE_PER_TOKEN ? 1 : ngroups);
-  const size_t per_sm = 220 * 1024;
-  for (int ctas = 4; ctas >= 1; --ctas) {
-    if (ctas * p.block > 1024) continue;
-    for (int stages = 4; stages >= 2; --stages) {
-      const size_t bytes = norm_tma_smem_bytes(H, res, stages, p.block, p.vpt, slots);
-      if (bytes <= kTmaMaxSmem && bytes * ctas <= per_sm) {
-        p.stages = stages;
-        p.grid = T < (int64_t)sms * ctas ? T : (int64_t)sms * ctas;
-        *out = p;
-        return true;
-      }
-    }
-  }
-  return false;
+  p.stages = 2;
+  const int slots = mode == VG_SCALE_PER_TOKEN ? 1 : ngroups;
+  const size_t bytes = norm_tma_smem_bytes(H, res, p.stages, p.block, p.vpt, slots);
+  if (bytes > kTmaMaxSmem) return false;
+  int ctas = (384 + p.block - 1) / p.block;
+  if (p.block >= 128 && T < 10LL * sms * ctas) ++ctas;
+  while (ctas > 1 && (bytes * ctas > 220 * 1024 || ctas * p.block > 1024)) --ctas;
+  p.grid = T < (int64_t)sms * ctas ? T : (int64_t)sms * ctas;
+  *out = p;
+  return true;
 }
 
 }  // namespace vg
