@@ -7,8 +7,8 @@ package never imports it and shares no code with it.
 
 What each function computes is documented in ``oracle.c`` with the passages
 it follows ("Fusion torch.compile passes", sections "RMSNorm + Quantization
-(fuse_norm_quant)" and "SiLU+Mul + Quantization (fuse_act_quant)"; OCP OFP8
-for the E4M3 format).
+(fuse_norm_quant)", "SiLU+Mul + Quantization (fuse_act_quant)" and "MLA Dual
+RMSNorm (fuse_mla_dual_rms_norm)"; OCP OFP8 for the E4M3 format).
 
 Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
   bf16 / e4m3 codecs ........ pinned (spec points, exhaustive round trips,
@@ -17,6 +17,9 @@ Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
                               bf16 add, exact-arithmetic brute force)
   silu_mul_fp8 .............. pinned (closed forms, library sigmoid,
                               exact-arithmetic brute force)
+  rms_norm_bf16 ............. pinned (closed forms, invariants,
+                              exact-arithmetic brute force)
+  mla_dual_rms_norm ......... the two pinned norms above, side by side
   NaN / Inf inputs .......... parity unpinned (no workload contains them)
 """
 from __future__ import annotations
@@ -68,6 +71,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.orc_fused_add_rms_norm_fp8.restype = ctypes.c_int
     lib.orc_silu_mul_fp8.argtypes = [P, P, P, P, i64, i64, ctypes.c_int, i64]
     lib.orc_silu_mul_fp8.restype = ctypes.c_int
+    lib.orc_rms_norm_bf16.argtypes = [P, P, P, P, i64, i64, ctypes.c_float]
+    lib.orc_rms_norm_bf16.restype = ctypes.c_int
     for name in ("orc_bf16_decode_n", "orc_bf16_encode_n",
                  "orc_e4m3_decode_n", "orc_e4m3_encode_n"):
         getattr(lib, name).argtypes = [P, P, i64]
@@ -158,6 +163,43 @@ class Oracle:
         return {"q": q, "scale": s, "v": v}
 
 
+    def rms_norm_bf16(self, x, weight, eps: float, want_y: bool = True):
+        """rms_norm(x, weight, eps) with the output rounded once to bf16.
+
+        x: uint16 bf16 bits [T, H]; weight: uint16 [H].
+        Returns dict(out uint16 [T,H], y float64 [T,H] before rounding)."""
+        x = _u16(x)
+        T, H = x.shape
+        w = _u16(weight).reshape(H)
+        out = np.empty((T, H), np.uint16)
+        y = np.empty((T, H), np.float64) if want_y else None
+        rc = self.lib.orc_rms_norm_bf16(_ptr(out), _ptr(y), _ptr(x), _ptr(w), T, H,
+                                        ctypes.c_float(eps))
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (rc={rc})")
+        return {"out": out, "y": y}
+
+    def mla_dual_rms_norm(self, q_c, q_weight, kv_c, kv_weight, eps_q: float,
+                          eps_kv: float, q_fp8: bool = False, want_v: bool = True):
+        """fused_mla_dual_rms_norm: the two norms of the unfused MLA graph,
+        side by side.  q_normed = rms_norm(q_c, q_weight, eps_q) and
+        kv_normed = rms_norm(kv_c, kv_weight, eps_kv), both bf16.  With
+        ``q_fp8`` (fused_mla_dual_rms_norm_per_token_quant) the q side is the
+        plain rms_norm -> dynamic per-token FP8 of fuse_norm_quant instead.
+
+        Returns dict(kv uint16 [T,kv_dim], kv_y, and either q uint16 [T,q_dim]
+        with q_y, or q_fp8 uint8 [T,q_dim], q_scale float32 [T], q_v)."""
+        kv = self.rms_norm_bf16(kv_c, kv_weight, eps_kv, want_y=want_v)
+        out = {"kv": kv["out"], "kv_y": kv["y"]}
+        if q_fp8:
+            q = self.fused_add_rms_norm_fp8(q_c, None, q_weight, eps_q, PER_TOKEN, want_v=want_v)
+            out.update(q_fp8=q["q"], q_scale=q["scale"], q_v=q["v"])
+        else:
+            q = self.rms_norm_bf16(q_c, q_weight, eps_q, want_y=want_v)
+            out.update(q=q["out"], q_y=q["y"])
+        return out
+
+
 def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
@@ -223,3 +265,11 @@ def fused_add_rms_norm_fp8(*args, **kwargs):
 
 def silu_mul_fp8(*args, **kwargs):
     return default().silu_mul_fp8(*args, **kwargs)
+
+
+def rms_norm_bf16(*args, **kwargs):
+    return default().rms_norm_bf16(*args, **kwargs)
+
+
+def mla_dual_rms_norm(*args, **kwargs):
+    return default().mla_dual_rms_norm(*args, **kwargs)

@@ -18,6 +18,10 @@
  *         "SiLU+Mul + Quantization (fuse_act_quant)" -- SiLU(gate)*up then
  *         FP8 quant without materialising the activation; "Quick Reference"
  *         table rows fuse_norm_quant / fuse_act_quant.
+ *         Section "MLA Dual RMSNorm (fuse_mla_dual_rms_norm)" -- the
+ *         paired q_c / kv_c RMSNorms of MLA attention (each with its own
+ *         weight and eps) in one call, and its per-token-quant variant where
+ *         q goes to FP8 with a per-token scale and kv stays bf16.
  *  [OFP8] OCP 8-bit Floating Point Specification (OFP8), E4M3 encoding:
  *         bias 7, no infinities, S.1111.111 is NaN, max normal 448
  *         (S.1111.110), min normal 2^-6, min subnormal 2^-9.
@@ -38,6 +42,8 @@
  *    [T, n/G] fp32, row-major.
  *  - silu(g) = g / (1 + exp(-g)); the gate is columns [0, I) and the up
  *    projection columns [I, 2I) of one [T, 2I] row.
+ *  - A norm whose output stays in the activation dtype (the MLA dual
+ *    norm's bf16 rows) rounds y once, to nearest even bf16.
  *  - e4m3 conversion rounds to nearest, ties to even mantissa, saturates
  *    finite overflow (and infinity) to +-448, keeps the sign of zero, and
  *    maps NaN to 0x7F.
@@ -262,6 +268,39 @@ int orc_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *scale,
     }
     free(r);
     free(y);
+    return 0;
+}
+
+/* rms_norm(x, weight, eps) with a bf16 output, rows t = 0..T-1 ([FUS] "MLA
+ * Dual RMSNorm": q_c and kv_c each go through rms_norm with their own weight
+ * and eps, and the normalised rows stay bf16):
+ *   y_j   = x_j / sqrt(mean_j(x_j^2) + eps) * w_j     (fp64)
+ *   out_j = bf16(y_j)                                 (one rounding)
+ * Layouts: x and out [T, H] row-major, weight [H]; y (optional) [T, H]. */
+int orc_rms_norm_bf16(uint16_t *out, double *y, const uint16_t *x,
+                      const uint16_t *weight, int64_t T, int64_t H, float eps)
+{
+    if (T < 0 || H <= 0)
+        return -1;
+    double *r = (double *)malloc((size_t)H * sizeof(double));
+    if (!r)
+        return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t j = 0; j < H; ++j)
+            r[j] = orc_bf16_decode(x[t * H + j]);
+        double ss = 0.0;
+        for (int64_t j = 0; j < H; ++j)
+            ss += r[j] * r[j];
+        double mean = ss / (double)H;
+        double inv = 1.0 / sqrt(mean + (double)eps);
+        for (int64_t j = 0; j < H; ++j) {
+            double yj = r[j] * inv * orc_bf16_decode(weight[j]);
+            out[t * H + j] = orc_bf16_encode(yj);
+            if (y)
+                y[t * H + j] = yj;
+        }
+    }
+    free(r);
     return 0;
 }
 

@@ -9,6 +9,7 @@ planted mistake and requires that at least one check fails for each.
 from __future__ import annotations
 
 import os
+from fractions import Fraction as F
 
 import numpy as np
 import torch
@@ -362,11 +363,81 @@ def check_silu_modes(orc):
     np.testing.assert_allclose(grp["scale"], (amax / 448.0).astype(np.float32), rtol=1e-7)
 
 
+# ------------------------------------------------------- bf16 rms_norm
+
+
+def check_rms_norm_bf16_closed_forms(orc):
+    """With eps = 0 a constant row c gives y = sign(c) * w, so the bf16 output
+    is w with c's sign; a row holding one value a among H = 4 gives
+    y = sign(a) * 2 * w at that column and a signed zero elsewhere; with
+    eps > 0 a constant row gives c / sqrt(c^2 + eps) * w."""
+    rng = np.random.default_rng(21)
+    H = 64
+    w = _weight(rng, H)
+    wf = exact.bf16_bits_to_f64(w)
+    for c in (1.5, -0.375, 3.0e-3, -96.0):
+        x = _bits(np.full((1, H), c))
+        out = orc.rms_norm_bf16(x, w, 0.0)
+        want = w ^ np.uint16(0x8000) if c < 0 else w
+        assert np.array_equal(out["out"][0], want), c
+        cb = float(exact.bf16_bits_to_f64(x[0, 0]))
+        for eps in (1e-6, 0.5):
+            out = orc.rms_norm_bf16(x, w, eps)
+            eps32 = F(float(np.float32(eps)))
+            inv = 1 / exact._sqrt(F(cb) * F(cb) + eps32)
+            y = [F(cb) * inv * F(float(wj)) for wj in wf]
+            assert list(out["out"][0]) == [exact.bf16_nearest_code(v) for v in y], (c, eps)
+    w4 = _bits([0.75, -1.25, 3.0, -0.5])
+    for a, j in ((2.5, 0), (-0.125, 2), (7.0, 3)):
+        x = np.zeros((1, 4), np.uint16)
+        x[0, j] = _bits([a])[0]
+        out = orc.rms_norm_bf16(x, w4, 0.0)["out"][0]
+        w4f = exact.bf16_bits_to_f64(w4)
+        for k in range(4):
+            if k == j:
+                assert out[k] == _bits([np.sign(a) * 2.0 * w4f[k]])[0], (a, j)
+            else:
+                assert out[k] == (0x8000 if w4f[k] < 0 else 0x0000), (a, j, k)
+
+
+def check_rms_norm_bf16_invariants(orc):
+    """eps = 0: the RMS of y / w is 1, y / w is proportional to x within a row,
+    and doubling the input (exact in bf16) changes nothing."""
+    rng = np.random.default_rng(22)
+    T, H = 6, 192
+    x = _rand_bf16(rng, (T, H))
+    w = _weight(rng, H)
+    wf = exact.bf16_bits_to_f64(w)
+    out = orc.rms_norm_bf16(x, w, 0.0)
+    y_over_w = out["y"] / wf
+    np.testing.assert_allclose(np.sqrt(np.mean(y_over_w ** 2, axis=1)), 1.0, rtol=1e-13)
+    ratio = y_over_w / exact.bf16_bits_to_f64(x)
+    np.testing.assert_allclose(ratio, ratio[:, :1] * np.ones_like(ratio), rtol=1e-13)
+    out2 = orc.rms_norm_bf16(_bits(2.0 * exact.bf16_bits_to_f64(x)), w, 0.0)
+    assert np.array_equal(out2["out"], out["out"]) and np.array_equal(out2["y"], out["y"])
+
+
+def check_rms_norm_bf16_brute_force(orc):
+    """Tiny random rows against exact rational arithmetic: every output is
+    the nearest-even bf16 of the exact normalised value."""
+    rng = np.random.default_rng(23)
+    for H, eps in ((1, 1e-5), (8, 1e-5), (16, 0.25), (24, 1e-6)):
+        T = 3
+        x = _rand_bf16(rng, (T, H), scale=np.exp2(rng.integers(-6, 6, (T, H))))
+        w = _weight(rng, H)
+        out = orc.rms_norm_bf16(x, w, eps)
+        for t in range(T):
+            ex = exact.exact_norm_row(x[t], None, w, eps, STATIC, 0, 1.0, 1e-10)
+            assert list(out["out"][t]) == [exact.bf16_nearest_code(v) for v in ex["y"]], (H, t)
+            np.testing.assert_allclose(out["y"][t], [float(v) for v in ex["y"]], rtol=1e-13)
+
+
 ALL_CHECKS = [
     check_e4m3_spec_points, check_e4m3_all_codes, check_e4m3_encoder_brute_force,
     check_e4m3_special_values, check_bf16_all_patterns, check_bf16_encoder_brute_force,
     check_norm_constant_row, check_norm_h1_closed_form, check_norm_invariants,
     check_norm_residual_add_library, check_norm_brute_force, check_per_token_max_code,
     check_per_group_layout, check_zero_row_and_saturation, check_silu_closed_forms,
-    check_silu_brute_force, check_silu_modes,
+    check_silu_brute_force, check_silu_modes, check_rms_norm_bf16_closed_forms,
+    check_rms_norm_bf16_invariants, check_rms_norm_bf16_brute_force,
 ]

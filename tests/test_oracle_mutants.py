@@ -40,6 +40,15 @@ MUTANTS = {
     "amax_floor_dropped": ("double a = amax > orc_amax_floor() ? amax : orc_amax_floor();",
                            "double a = amax;"),
     "bf16_decode_shift": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    "bf16_norm_eps_dropped": ("sqrt(mean + (double)eps)", "sqrt(mean)"),
+    "bf16_norm_sum_not_mean": ("double mean = ss / (double)H;", "double mean = ss;"),
+    "bf16_norm_weight_dropped": ("double yj = r[j] * inv * orc_bf16_decode(weight[j]);",
+                                 "double yj = r[j] * inv;"),
+    "bf16_norm_rounded_twice": ("double yj = r[j] * inv * orc_bf16_decode(weight[j]);",
+                                "double yj = orc_bf16_decode(orc_bf16_encode(r[j] * inv))"
+                                " * orc_bf16_decode(weight[j]);"),
+    "bf16_norm_row_offset_dropped": ("r[j] = orc_bf16_decode(x[t * H + j]);",
+                                     "r[j] = orc_bf16_decode(x[j]);"),
 }
 
 
