@@ -7,7 +7,7 @@ keyed by ``(seed, tensor id, row block)``) and converts them to bf16 with
 PyTorch's CPU cast, which rounds to nearest even.
 
 Distributions follow the workloads in the design notes:
-  x, residual, gate_up ~ N(0, 1)
+  x, residual, gate_up, q_c, kv_c ~ N(0, 1)
   weight               ~ 1 + 0.1 * N(0, 1)
   prefill x            ~ Student-t(3) with 0.1 % of the elements scaled by 100
 Each tensor is split into blocks of rows generated independently, so a
@@ -23,6 +23,7 @@ import numpy as np
 import torch
 
 TENSOR_X, TENSOR_RESIDUAL, TENSOR_WEIGHT, TENSOR_GATE_UP = 1, 2, 3, 4
+TENSOR_Q_C, TENSOR_KV_C, TENSOR_Q_WEIGHT, TENSOR_KV_WEIGHT = 5, 6, 7, 8
 _ROW_BLOCK = 64
 
 STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
@@ -90,16 +91,27 @@ def silu_inputs(T: int, I: int, seed: int = 0):
     return {"gate_up": bf16_tensor("normal", seed, TENSOR_GATE_UP, T, 2 * I)}
 
 
+def mla_inputs(T: int, q_dim: int, kv_dim: int, seed: int = 0):
+    """q_c [T,q_dim], kv_c [T,kv_dim] and their weights as uint16 bf16 bits."""
+    return {
+        "q_c": bf16_tensor("normal", seed, TENSOR_Q_C, T, q_dim),
+        "kv_c": bf16_tensor("normal", seed, TENSOR_KV_C, T, kv_dim),
+        "q_weight": bf16_tensor("weight", seed, TENSOR_Q_WEIGHT, 1, q_dim).reshape(q_dim),
+        "kv_weight": bf16_tensor("weight", seed, TENSOR_KV_WEIGHT, 1, kv_dim).reshape(kv_dim),
+    }
+
+
 # ----------------------------------------------------------------- workloads
 
 @dataclass(frozen=True)
 class Workload:
     """One op invocation: which op, its shape, scale mode and inputs."""
     name: str
-    op: str                  # "norm" or "silu"
+    op: str                  # "norm", "silu" or "mla"
     T: int
-    n: int                   # hidden (norm) or intermediate (silu)
-    mode: int
+    n: int                   # hidden (norm), intermediate (silu) or q_dim (mla)
+    mode: int                # mla: PER_TOKEN = q to fp8, STATIC = bf16 q
+    n2: int = 0              # mla: kv_dim
     group_size: int = 128
     eps: float = 1e-5
     static_scale: float = 0.05
@@ -111,6 +123,8 @@ class Workload:
     def inputs(self):
         if self.op == "norm":
             return norm_inputs(self.T, self.n, self.seed, self.x_dist)
+        if self.op == "mla":
+            return mla_inputs(self.T, self.n, self.n2, self.seed)
         return silu_inputs(self.T, self.n, self.seed)
 
     def algorithmic_bytes(self) -> int:
@@ -121,6 +135,9 @@ class Workload:
         if self.op == "norm":
             per_row = (7 if self.residual else 3) * self.n + s_row
             return self.T * per_row + 2 * self.n + s0
+        if self.op == "mla":  # both rows read; q out as fp8 + scale or bf16; kv out bf16
+            q_out = self.n + 4 if self.mode == PER_TOKEN else 2 * self.n
+            return self.T * (2 * self.n + 4 * self.n2 + q_out) + 2 * (self.n + self.n2)
         return self.T * (5 * self.n + s_row) + s0
 
 
@@ -138,6 +155,18 @@ CFG3 = Workload("norm_per_group128_16384x8192_t3", "norm", 16384, 8192, PER_GROU
 CFG1_ACT = Workload("silu_per_token_256x14336", "silu", 256, 14336, PER_TOKEN)
 
 NAMED = {w.name: w for w in (CFG0, CFG1, CFG2A, CFG2B, CFG3, CFG1_ACT)}
+
+# The MLA dual norm at DeepSeek-V3's latent sizes (q_lora_rank 1536,
+# kv_lora_rank 512), bf16 and per-token-fp8 q, decode and prefill token counts.
+MLA_Q_DIM, MLA_KV_DIM, MLA_ROPE = 1536, 512, 64
+MLA_T = (1, 64, 512, 4096, 32768)
+
+
+def mla_workloads():
+    return [Workload(f"mla_dual_{'fp8' if m == PER_TOKEN else 'bf16'}_{T}x{MLA_Q_DIM}_{MLA_KV_DIM}",
+                     "mla", T, MLA_Q_DIM, m, n2=MLA_KV_DIM, eps=1e-6)
+            for m in (STATIC, PER_TOKEN) for T in MLA_T]
+
 
 SWEEP_T = (1, 8, 64, 512, 4096, 32768)
 SWEEP_SHAPES = ((4096, 14336), (8192, 28672))

@@ -11,7 +11,10 @@
  *   scales.  Section "SiLU+Mul + Quantization (fuse_act_quant)":
  *   silu_and_mul of the gate-up projection -> quant_fp8 in one kernel,
  *   without materialising the post-activation tensor.  "Quick Reference"
- *   table: both fusions apply for every num_tokens.
+ *   table: both fusions apply for every num_tokens.  Section "MLA Dual
+ *   RMSNorm (fuse_mla_dual_rms_norm)": the paired q_c / kv_c RMSNorms of MLA
+ *   attention in one kernel, and its per-token-quant variant (q to FP8 with
+ *   a per-token scale, kv in bf16).
  *
  * Numerics (the pages give no formulas; these are the readings the library
  * implements):
@@ -23,6 +26,8 @@
  *         per-token: fp32(max(amax over the row, 1e-10f) / 448)
  *         per-group: fp32(max(amax over G columns, 1e-10f) / 448)
  *   The kernels multiply by 1/s, computed once per row or group.
+ *   A norm with a bf16 output (the MLA dual norm) rounds y once, to nearest
+ *   even bf16, as the exact value would round.
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
@@ -30,7 +35,8 @@
  *     synchronises, and launches only on `stream` (NULL = legacy default
  *     stream).  Calls are asynchronous and may be captured in a CUDA graph.
  *   - bf16 tensors are passed as uint16_t bit patterns, fp8 outputs as
- *     uint8_t E4M3 codes.  All tensors are dense and row-major.
+ *     uint8_t E4M3 codes.  All tensors are dense and row-major, except the
+ *     MLA dual norm's two inputs, which are read through a row stride.
  *   - Every argument is validated on the host before any launch; a
  *     validation error returns its status and launches nothing.  A launch
  *     failure returns VG_ERR_CUDA.  num_tokens == 0 returns VG_OK without
@@ -56,7 +62,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *vg_stream_t;
 
-#define VG_ABI_VERSION 1
+#define VG_ABI_VERSION 2
 #define VG_MAX_ROW 32768 /* largest hidden / inter a row-resident kernel holds */
 
 typedef enum {
@@ -116,6 +122,49 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
 vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up,
                           int64_t num_tokens, int64_t inter, int32_t mode,
                           int32_t group_size, vg_stream_t stream);
+
+/*
+ * MLA dual RMSNorm ("MLA Dual RMSNorm (fuse_mla_dual_rms_norm)"): in one
+ * launch,
+ *   q_out  = bf16(rms_norm(q_c,  q_weight,  eps_q))
+ *   kv_out = bf16(rms_norm(kv_c, kv_weight, eps_kv))
+ * with rms_norm(x, w, eps)_j = x_j / sqrt(mean(x^2) + eps) * w_j.
+ *
+ *   q_out      out uint16 [T, q_dim]   bf16, dense
+ *   kv_out     out uint16 [T, kv_dim]  bf16, dense
+ *   q_c        in  uint16 bf16; row t is q_c[t * q_stride + j], j < q_dim
+ *   q_stride   elements between rows of q_c: >= q_dim, a multiple of 8
+ *              (q_c and kv_c are usually column slices of one projected
+ *              [T, q_dim + kv_dim + rope] tensor, both with its row length)
+ *   q_weight   in  uint16 [q_dim] bf16
+ *   kv_c, kv_stride, kv_weight   the same for the kv side
+ *   num_tokens T >= 0; q_dim, kv_dim: multiples of 8 in [8, VG_MAX_ROW]
+ *   eps_q, eps_kv  each side's epsilon
+ * Outputs must not overlap any input or each other.  A stride < dim or not
+ * a multiple of 8 is VG_ERR_BAD_SHAPE.
+ */
+vg_status vg_fused_mla_dual_rms_norm(uint16_t *q_out, uint16_t *kv_out, const uint16_t *q_c,
+                                     int64_t q_stride, const uint16_t *q_weight,
+                                     const uint16_t *kv_c, int64_t kv_stride,
+                                     const uint16_t *kv_weight, int64_t num_tokens,
+                                     int64_t q_dim, int64_t kv_dim, float eps_q,
+                                     float eps_kv, vg_stream_t stream);
+
+/*
+ * The per-token-quant variant ("MLA Dual RMSNorm", FP8 attention with a
+ * per-token q_b_proj): q goes through rms_norm -> dynamic per-token FP8 as
+ * in vg_fused_add_rms_norm_fp8 without a residual, kv stays bf16.
+ *
+ *   q_fp8    out uint8 [T, q_dim]  E4M3 codes of y / s
+ *   q_scale  out fp32  [T]         s = fp32(max(amax of the q row, 1e-10f) / 448)
+ *   kv_out   out uint16 [T, kv_dim] bf16
+ *   the inputs and sizes as for vg_fused_mla_dual_rms_norm.
+ */
+vg_status vg_fused_mla_dual_rms_norm_per_token_quant(
+    uint8_t *q_fp8, float *q_scale, uint16_t *kv_out, const uint16_t *q_c, int64_t q_stride,
+    const uint16_t *q_weight, const uint16_t *kv_c, int64_t kv_stride, const uint16_t *kv_weight,
+    int64_t num_tokens, int64_t q_dim, int64_t kv_dim, float eps_q, float eps_kv,
+    vg_stream_t stream);
 
 /*
  * Device-side status of the library's kernels on the current device (no

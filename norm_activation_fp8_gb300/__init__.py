@@ -11,9 +11,15 @@ Entry points (same names and argument order as the C ABI):
   vg_fused_add_rms_norm_fp8(q, residual_out, scale, x, residual, weight,
                             eps, mode, group_size=128, stream=None)
   vg_silu_mul_fp8(q, scale, gate_up, mode, group_size=128, stream=None)
+  vg_fused_mla_dual_rms_norm(q_out, kv_out, q_c, q_weight, kv_c, kv_weight,
+                             eps_q, eps_kv, stream=None)
+  vg_fused_mla_dual_rms_norm_per_token_quant(q_fp8, q_scale, kv_out, q_c,
+                             q_weight, kv_c, kv_weight, eps_q, eps_kv, stream=None)
+  (the MLA inputs may be column-slice views: their row stride is passed on)
 Convenience wrappers that allocate the outputs with torch:
   fused_add_rms_norm_fp8(x, residual, weight, eps, mode, ...)
   silu_mul_fp8(gate_up, mode, ...)
+  mla_dual_rms_norm(q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, q_fp8=False)
 """
 from __future__ import annotations
 
@@ -31,7 +37,8 @@ STATUS_NAMES = {
     4: "VG_ERR_BAD_MODE", 5: "VG_ERR_BAD_GROUP", 6: "VG_ERR_UNSUPPORTED_DEVICE", 7: "VG_ERR_CUDA",
 }
 
-EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_device_status",
+EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_fused_mla_dual_rms_norm",
+                    "vg_fused_mla_dual_rms_norm_per_token_quant", "vg_device_status",
                     "vg_status_string", "vg_abi_version")
 DEVICE_WAIT_TIMEOUT = 1
 
@@ -65,6 +72,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.vg_fused_add_rms_norm_fp8.restype = ctypes.c_int
         lib.vg_silu_mul_fp8.argtypes = [P, P, P, i64, i64, i32, i32, P]
         lib.vg_silu_mul_fp8.restype = ctypes.c_int
+        f32 = ctypes.c_float
+        lib.vg_fused_mla_dual_rms_norm.argtypes = [P, P, P, i64, P, P, i64, P, i64, i64, i64,
+                                                   f32, f32, P]
+        lib.vg_fused_mla_dual_rms_norm.restype = ctypes.c_int
+        lib.vg_fused_mla_dual_rms_norm_per_token_quant.argtypes = [P, P, P, P, i64, P, P, i64, P,
+                                                                   i64, i64, i64, f32, f32, P]
+        lib.vg_fused_mla_dual_rms_norm_per_token_quant.restype = ctypes.c_int
         lib.vg_status_string.argtypes = [ctypes.c_int]
         lib.vg_status_string.restype = ctypes.c_char_p
         lib.vg_abi_version.argtypes = []
@@ -163,6 +177,53 @@ def vg_silu_mul_fp8(q, scale, gate_up, mode: int, group_size: int = 128, stream=
     _check(st)
 
 
+def _rows_ptr(t, name):
+    """(device pointer, row stride in elements, rows, columns) of a 2-D bf16
+    CUDA tensor whose rows are contiguous (a column slice is fine)."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    bf16, _, _ = _dtypes()
+    if t.dtype not in bf16:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {bf16}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (there is no CPU path)")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name}: expected a 2-D [T, n] tensor with contiguous rows")
+    return t.data_ptr(), t.stride(0), t.shape[0], t.shape[1]
+
+
+def vg_fused_mla_dual_rms_norm(q_out, kv_out, q_c, q_weight, kv_c, kv_weight, eps_q: float,
+                               eps_kv: float, stream=None):
+    """MLA dual RMSNorm through the C ABI: q_out = bf16(rms_norm(q_c)),
+    kv_out = bf16(rms_norm(kv_c)) in one launch (outputs preallocated,
+    dense bf16; q_c / kv_c may be column slices of one projected tensor)."""
+    bf16, _, _ = _dtypes()
+    qp, qs, T, q_dim = _rows_ptr(q_c, "q_c")
+    kp, ks, T2, kv_dim = _rows_ptr(kv_c, "kv_c")
+    if T2 != T:
+        raise ValueError("q_c and kv_c must have the same number of rows")
+    _check(load().vg_fused_mla_dual_rms_norm(
+        _ptr(q_out, bf16, "q_out"), _ptr(kv_out, bf16, "kv_out"), qp, qs,
+        _ptr(q_weight, bf16, "q_weight"), kp, ks, _ptr(kv_weight, bf16, "kv_weight"),
+        T, q_dim, kv_dim, ctypes.c_float(eps_q), ctypes.c_float(eps_kv), _stream(stream)))
+
+
+def vg_fused_mla_dual_rms_norm_per_token_quant(q_fp8, q_scale, kv_out, q_c, q_weight, kv_c,
+                                               kv_weight, eps_q: float, eps_kv: float,
+                                               stream=None):
+    """The per-token-quant variant: q to FP8 with q_scale [T] fp32, kv bf16."""
+    bf16, fp8, f32 = _dtypes()
+    qp, qs, T, q_dim = _rows_ptr(q_c, "q_c")
+    kp, ks, T2, kv_dim = _rows_ptr(kv_c, "kv_c")
+    if T2 != T:
+        raise ValueError("q_c and kv_c must have the same number of rows")
+    _check(load().vg_fused_mla_dual_rms_norm_per_token_quant(
+        _ptr(q_fp8, fp8, "q_fp8"), _ptr(q_scale, f32, "q_scale"), _ptr(kv_out, bf16, "kv_out"),
+        qp, qs, _ptr(q_weight, bf16, "q_weight"), kp, ks, _ptr(kv_weight, bf16, "kv_weight"),
+        T, q_dim, kv_dim, ctypes.c_float(eps_q), ctypes.c_float(eps_kv), _stream(stream)))
+
+
 def vg_device_status(reset: bool = False) -> int:
     """Flags the library's kernels left on the current device
     (DEVICE_WAIT_TIMEOUT: a bounded wait gave up; that call's outputs are
@@ -208,3 +269,21 @@ def silu_mul_fp8(gate_up, mode: int, group_size: int = 128, scale=None, stream=N
     s = _scale_out(mode, T, two_i // 2, group_size, scale, gate_up.device)
     vg_silu_mul_fp8(q, s, gate_up, mode, group_size, stream)
     return q, s
+
+
+def mla_dual_rms_norm(q_c, q_weight, kv_c, kv_weight, eps_q: float, eps_kv: float,
+                      q_fp8: bool = False, stream=None):
+    """Returns (q_normed bf16 [T,q_dim], kv_normed bf16 [T,kv_dim]), or with
+    ``q_fp8`` (q float8_e4m3fn [T,q_dim], q_scale fp32 [T], kv_normed)."""
+    import torch
+    T, q_dim = q_c.shape
+    kv = torch.empty((T, kv_c.shape[1]), dtype=kv_c.dtype, device=kv_c.device)
+    if q_fp8:
+        q = torch.empty((T, q_dim), dtype=torch.float8_e4m3fn, device=q_c.device)
+        s = torch.empty((T,), dtype=torch.float32, device=q_c.device)
+        vg_fused_mla_dual_rms_norm_per_token_quant(q, s, kv, q_c, q_weight, kv_c, kv_weight,
+                                                   eps_q, eps_kv, stream)
+        return q, s, kv
+    q = torch.empty((T, q_dim), dtype=q_c.dtype, device=q_c.device)
+    vg_fused_mla_dual_rms_norm(q, kv, q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, stream)
+    return q, kv

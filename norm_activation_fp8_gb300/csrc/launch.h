@@ -100,4 +100,31 @@ size_t silu_tma_token_smem_bytes(int I, int nseg);
 cudaError_t launch_silu_fp8_tma_token(SiluArgs a, const SiluTmaPlan &plan, cudaStream_t stream);
 uint32_t read_silu_status(bool reset);
 
+// MLA dual RMSNorm: side 0 is the q row, side 1 the kv row of each token.
+struct MlaArgs {
+  const uint16_t *src[2];  // q_c, kv_c (strided rows)
+  const uint16_t *w[2];
+  int64_t stride[2];       // elements between rows of src
+  uint16_t *out[2];        // bf16 outputs (out[0] unused when q goes to fp8)
+  uint8_t *q8;             // fp8 q output (per-token-quant variant)
+  float *q_scale;          // [T]
+  int64_t T;
+  int32_t nch[2];          // chunks per row
+  int32_t thr[2];          // threads per row (multiples of 32)
+  int32_t rpc;             // tokens per CTA
+  float eps[2];
+  float n[2];              // row lengths
+  float inv_n[2];          // 1 / row length
+};
+
+struct MlaPlan {
+  int vpt;
+  int thr[2];
+  int rpc;
+  int block;
+  int64_t grid;
+};
+MlaPlan plan_mla(int64_t T, int nq, int nkv, int sms);
+cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaStream_t s);
+
 }  // namespace vg

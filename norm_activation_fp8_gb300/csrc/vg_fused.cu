@@ -162,9 +162,104 @@ bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, T
   return true;
 }
 
+// MLA dual norm: one token's q row and kv row in one thread group.  Few
+// tokens (decode) take one token per CTA and one chunk per thread for the
+// shortest chain; many tokens take two chunks per thread (more bytes in
+// flight) and pack tokens into CTAs of up to 512 threads.  A token's group
+// stays within 512 threads up to four chunks per thread (eight allow 1024).
+MlaPlan plan_mla(int64_t T, int nq, int nkv, int sms) {
+  MlaPlan p;
+  p.vpt = T >= 4LL * sms ? 2 : 1;
+  auto threads = [&](int nch) { return ((nch + p.vpt - 1) / p.vpt + 31) / 32 * 32; };
+  while (p.vpt < 8 && threads(nq) + threads(nkv) > 512) p.vpt *= 2;
+  p.thr[0] = threads(nq);
+  p.thr[1] = threads(nkv);
+  const int per_tok = p.thr[0] + p.thr[1];
+  p.rpc = T >= 2LL * sms ? (512 / per_tok > 1 ? 512 / per_tok : 1) : 1;
+  if (p.rpc > 16) p.rpc = 16;
+  p.block = p.rpc * per_tok;
+  p.grid = (T + p.rpc - 1) / p.rpc;
+  return p;
+}
+
+namespace {
+
+vg_status mla_dual_norm(uint16_t *q_out, uint8_t *q_fp8, float *q_scale, uint16_t *kv_out,
+                        const uint16_t *q_c, int64_t q_stride, const uint16_t *q_weight,
+                        const uint16_t *kv_c, int64_t kv_stride, const uint16_t *kv_weight,
+                        int64_t T, int64_t q_dim, int64_t kv_dim, float eps_q, float eps_kv,
+                        vg_stream_t stream) {
+  const bool fp8 = q_fp8 != nullptr || q_scale != nullptr;
+  auto bad_dim = [](int64_t n, int64_t stride) {
+    return n < 8 || n % 8 != 0 || n > VG_MAX_ROW || stride < n || stride % 8 != 0;
+  };
+  if (T < 0 || T > INT32_MAX || bad_dim(q_dim, q_stride) || bad_dim(kv_dim, kv_stride))
+    return VG_ERR_BAD_SHAPE;
+  if (T == 0) return VG_OK;
+  if (!kv_out || !q_c || !q_weight || !kv_c || !kv_weight || (fp8 ? !q_fp8 || !q_scale : !q_out))
+    return VG_ERR_NULL_PTR;
+  if (misaligned(q_out, 16) || misaligned(q_fp8, 16) || misaligned(kv_out, 16) ||
+      misaligned(q_c, 16) || misaligned(q_weight, 16) || misaligned(kv_c, 16) ||
+      misaligned(kv_weight, 16) || misaligned(q_scale, 4))
+    return VG_ERR_MISALIGNED;
+  int sms = 0;
+  vg_status st = check_device(&sms);
+  if (st != VG_OK) return st;
+  clear_stale_error();
+
+  MlaArgs a{};
+  a.src[0] = q_c;
+  a.src[1] = kv_c;
+  a.w[0] = q_weight;
+  a.w[1] = kv_weight;
+  a.stride[0] = q_stride;
+  a.stride[1] = kv_stride;
+  a.out[0] = q_out;
+  a.out[1] = kv_out;
+  a.q8 = q_fp8;
+  a.q_scale = q_scale;
+  a.T = T;
+  a.nch[0] = (int32_t)(q_dim / 8);
+  a.nch[1] = (int32_t)(kv_dim / 8);
+  a.eps[0] = eps_q;
+  a.eps[1] = eps_kv;
+  a.n[0] = (float)q_dim;
+  a.n[1] = (float)kv_dim;
+  a.inv_n[0] = 1.0f / (float)q_dim;
+  a.inv_n[1] = 1.0f / (float)kv_dim;
+  const MlaPlan p = plan_mla(T, a.nch[0], a.nch[1], sms);
+  return launch_mla_dual_norm(a, fp8, p, (cudaStream_t)stream) == cudaSuccess ? VG_OK
+                                                                               : VG_ERR_CUDA;
+}
+
+}  // namespace
+
 }  // namespace vg
 
 extern "C" {
+
+vg_status vg_fused_mla_dual_rms_norm(uint16_t *q_out, uint16_t *kv_out, const uint16_t *q_c,
+                                     int64_t q_stride, const uint16_t *q_weight,
+                                     const uint16_t *kv_c, int64_t kv_stride,
+                                     const uint16_t *kv_weight, int64_t num_tokens,
+                                     int64_t q_dim, int64_t kv_dim, float eps_q,
+                                     float eps_kv, vg_stream_t stream) {
+  if (num_tokens > 0 && !q_out) return VG_ERR_NULL_PTR;
+  return vg::mla_dual_norm(q_out, nullptr, nullptr, kv_out, q_c, q_stride, q_weight, kv_c,
+                           kv_stride, kv_weight, num_tokens, q_dim, kv_dim, eps_q, eps_kv,
+                           stream);
+}
+
+vg_status vg_fused_mla_dual_rms_norm_per_token_quant(
+    uint8_t *q_fp8, float *q_scale, uint16_t *kv_out, const uint16_t *q_c, int64_t q_stride,
+    const uint16_t *q_weight, const uint16_t *kv_c, int64_t kv_stride, const uint16_t *kv_weight,
+    int64_t num_tokens, int64_t q_dim, int64_t kv_dim, float eps_q, float eps_kv,
+    vg_stream_t stream) {
+  if (num_tokens > 0 && (!q_fp8 || !q_scale)) return VG_ERR_NULL_PTR;
+  return vg::mla_dual_norm(nullptr, q_fp8, q_scale, kv_out, q_c, q_stride, q_weight, kv_c,
+                           kv_stride, kv_weight, num_tokens, q_dim, kv_dim, eps_q, eps_kv,
+                           stream);
+}
 
 vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *scale,
                                     const uint16_t *x, const uint16_t *residual,

@@ -2,6 +2,8 @@
 seeded bytes, and compare them with the tolerance the benchmark spec fixes:
 
   residual_out  bf16, bit-exact
+  bf16 norm outputs (MLA dual norm): bit-exact (the kernel rounds the exact
+                product; see the MLA checks below)
   scale         |s_gpu - s_oracle| <= 1e-6 * |s_oracle|
   q             identical codes, except codes adjacent in value (1 ULP, same
                 sign) where the oracle's pre-rounding value v = y/s lies
@@ -178,6 +180,37 @@ def check_silu(gpu, orc, mode, rows=None):
     return stats
 
 
+def oracle_mla(q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, q_fp8):
+    """The oracle's MLA dual norm over row blocks run in threads."""
+    T = q_c.shape[0]
+    parts = [None] * T
+    blocks = _blocks(T, _threads())
+
+    def work(i):
+        r0, r1 = blocks[i]
+        parts[i] = oracle.mla_dual_rms_norm(q_c[r0:r1], q_weight, kv_c[r0:r1], kv_weight,
+                                            eps_q, eps_kv, q_fp8=q_fp8)
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(work, range(len(blocks))))
+    parts = [p for p in parts if p is not None]
+    if not parts:
+        return None
+    return {k: np.concatenate([p[k] for p in parts]) for k in parts[0]}
+
+
+def check_mla(gpu, orc, q_fp8):
+    """kv (and a bf16 q) bit-exact; an fp8 q under the code rule, its
+    per-token scales within 1e-6."""
+    compare_exact(gpu["kv"], orc["kv"], "kv_normed")
+    if not q_fp8:
+        compare_exact(gpu["q"], orc["q"], "q_normed")
+        return {}
+    stats = compare_codes(gpu["q_fp8"], orc["q_fp8"], orc["q_v"], "q_fp8")
+    stats.update(compare_scales(gpu["q_scale"], orc["q_scale"], "q_scale"))
+    return stats
+
+
 # --------------------------------------------------------------- GPU side
 
 GUARD = 256  # sentinel bytes before and after every GPU output
@@ -260,3 +293,53 @@ def gpu_silu(gate_up, mode, group_size=128, scale=None, device="cuda"):
     return {"q": q.view(T, I).cpu().numpy(),
             "scale": s.cpu().numpy() if mode == 0 else
             s.cpu().numpy().reshape((T,) if mode == 1 else (T, I // group_size))}
+
+
+def gpu_mla(q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, q_fp8, rope=64, q_pad=None,
+            kv_pad=None, device="cuda"):
+    """The CUDA MLA dual norm on numpy bf16-bit inputs.  By default q_c and
+    kv_c are column slices of one projected [T, q_dim + kv_dim + rope]
+    device tensor, as in the model; with q_pad / kv_pad each side is its own
+    tensor whose rows are padded by that many elements (another stride).
+    Outputs sit between 0xAA guard bands, checked afterwards."""
+    import torch
+    import norm_activation_fp8_gb300 as vg
+    T, q_dim = q_c.shape
+    kv_dim = kv_c.shape[1]
+    if q_pad is None and kv_pad is None:
+        proj = np.zeros((T, q_dim + kv_dim + rope), np.uint16)
+        proj[:, :q_dim] = q_c
+        proj[:, q_dim:q_dim + kv_dim] = kv_c
+        pt = torch.from_numpy(proj.view(np.int16)).to(device)
+        qt, kt = pt[:, :q_dim], pt[:, q_dim:q_dim + kv_dim]
+    else:
+        def padded(a, pad):
+            buf = np.full((T, a.shape[1] + (pad or 0)), 0x7FC0, np.uint16)  # NaN padding
+            buf[:, :a.shape[1]] = a
+            return torch.from_numpy(buf.view(np.int16)).to(device)[:, :a.shape[1]]
+        qt, kt = padded(q_c, q_pad), padded(kv_c, kv_pad)
+    qw = torch.from_numpy(np.ascontiguousarray(q_weight).view(np.int16)).to(device)
+    kw = torch.from_numpy(np.ascontiguousarray(kv_weight).view(np.int16)).to(device)
+    kbuf, kraw = _guarded(torch, T * kv_dim * 2, device)
+    kv_out = kraw.view(torch.int16).view(T, kv_dim)
+    out = {}
+    if q_fp8:
+        qbuf, qraw = _guarded(torch, T * q_dim, device)
+        sbuf, sraw = _guarded(torch, 4 * T, device)
+        vg.vg_fused_mla_dual_rms_norm_per_token_quant(qraw.view(T, q_dim), sraw.view(torch.float32),
+                                                      kv_out, qt, qw, kt, kw, eps_q, eps_kv)
+        torch.cuda.synchronize()
+        _check_guards(qbuf, T * q_dim, "q_fp8")
+        _check_guards(sbuf, 4 * T, "q_scale")
+        out["q_fp8"] = qraw.view(T, q_dim).cpu().numpy()
+        out["q_scale"] = sraw.view(torch.float32).cpu().numpy()
+    else:
+        qbuf, qraw = _guarded(torch, T * q_dim * 2, device)
+        q_out = qraw.view(torch.int16).view(T, q_dim)
+        vg.vg_fused_mla_dual_rms_norm(q_out, kv_out, qt, qw, kt, kw, eps_q, eps_kv)
+        torch.cuda.synchronize()
+        _check_guards(qbuf, T * q_dim * 2, "q_normed")
+        out["q"] = q_out.cpu().numpy().view(np.uint16)
+    _check_guards(kbuf, T * kv_dim * 2, "kv_normed")
+    out["kv"] = kv_out.cpu().numpy().view(np.uint16)
+    return out

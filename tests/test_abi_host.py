@@ -38,6 +38,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8"} <= names
+    assert {"vg_fused_mla_dual_rms_norm", "vg_fused_mla_dual_rms_norm_per_token_quant"} <= names
     assert names == set(vg.EXPORTED_SYMBOLS)
 
 
@@ -48,7 +49,7 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert name in exported, name
         assert getattr(lib, name) is not None
-    assert lib.vg_abi_version() == 1
+    assert lib.vg_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -130,3 +131,49 @@ def test_missing_library_fails_loudly(tmp_path):
 
 def test_device_status_rejects_null(lib):
     assert lib.vg_device_status(None, 0) == NULL
+
+
+def mla(lib, q=A, kv=A, qc=A, qs=2112, qw=A, kc=A, ks=2112, kw=A, T=4, qd=1536, kd=512):
+    return lib.vg_fused_mla_dual_rms_norm(q, kv, qc, qs, qw, kc, ks, kw, T, qd, kd,
+                                          ctypes.c_float(1e-6), ctypes.c_float(1e-6), None)
+
+
+def mla8(lib, q8=A, s=A, kv=A, qc=A, qs=2112, qw=A, kc=A, ks=2112, kw=A, T=4, qd=1536, kd=512):
+    return lib.vg_fused_mla_dual_rms_norm_per_token_quant(q8, s, kv, qc, qs, qw, kc, ks, kw, T, qd,
+                                                          kd, ctypes.c_float(1e-6),
+                                                          ctypes.c_float(1e-6), None)
+
+
+@pytest.mark.parametrize("fn", [mla, mla8])
+def test_mla_bad_shape(lib, fn):
+    for qd in (0, 4, 12, 32776):
+        assert fn(lib, qd=qd, qs=40000) == SHAPE, qd
+    for kd in (0, 1030, 65536):
+        assert fn(lib, kd=kd, ks=70000) == SHAPE, kd
+    assert fn(lib, qs=1528) == SHAPE          # stride below the row length
+    assert fn(lib, ks=2116) == SHAPE          # stride not a multiple of 8
+    assert fn(lib, T=-1) == SHAPE
+    assert fn(lib, T=2 ** 31) == SHAPE
+
+
+def test_mla_null_pointers(lib):
+    for k in ("q", "kv", "qc", "qw", "kc", "kw"):
+        assert mla(lib, **{k: None}) == NULL, k
+    for k in ("q8", "s", "kv", "qc", "qw", "kc", "kw"):
+        assert mla8(lib, **{k: None}) == NULL, k
+    assert mla(lib, q=None, kv=None, qc=None, qw=None, kc=None, kw=None, T=0) == OK
+    assert mla8(lib, q8=None, s=None, kv=None, qc=None, qw=None, kc=None, kw=None, T=0) == OK
+
+
+def test_mla_misaligned(lib):
+    for k in ("q", "kv", "qc", "qw", "kc", "kw"):
+        assert mla(lib, **{k: A + 8}) == ALIGN, k
+    assert mla8(lib, q8=A + 4) == ALIGN
+    assert mla8(lib, s=A + 2) == ALIGN
+
+
+def test_binding_mla_rejects_strided_columns(lib):
+    import torch
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        vg.vg_fused_mla_dual_rms_norm(None, None, x, None, x, None, 1e-6, 1e-6)
