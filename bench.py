@@ -62,6 +62,7 @@ STEPS = {
 # every named single-op workload and every sweep point is also a (one-op) step
 STEPS.update({name: (w,) for name, w in gen.NAMED.items()})
 STEPS.update({w.name: (w,) for w in gen.sweep()})
+STEPS.update({w.name: (w,) for w in gen.mla_workloads()})
 DEFAULT_STEP = "llama3_8b_decode"
 
 
@@ -206,12 +207,13 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+_CSRC = "norm_activation_fp8_gb300/csrc/"
 KERNEL_SOURCES = {
-    "norm": ["norm_activation_fp8_gb300/csrc/norm_fp8.cu", "norm_activation_fp8_gb300/csrc/common.cuh",
-             "norm_activation_fp8_gb300/csrc/dyn_scale.cuh", "norm_activation_fp8_gb300/csrc/tma.cuh",
-             "norm_activation_fp8_gb300/csrc/vg_fused.cu"],
-    "silu": ["norm_activation_fp8_gb300/csrc/silu_fp8.cu", "norm_activation_fp8_gb300/csrc/common.cuh",
-             "norm_activation_fp8_gb300/csrc/vg_fused.cu"],
+    "norm": [_CSRC + f for f in ("norm_fp8.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
+                                 "tma.cuh", "vg_fused.cu")],
+    "silu": [_CSRC + f for f in ("silu_fp8.cu", "common.cuh", "tma.cuh", "vg_fused.cu")],
+    "mla": [_CSRC + f for f in ("mla_norm.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
+                                "vg_fused.cu")],
 }
 
 
@@ -261,6 +263,19 @@ class DeviceSet:
                 q = torch.empty((w.T, w.n), dtype=torch.uint8, device=dev)
                 scale = self._scale(torch, w, dev)
                 self.ops.append(dict(w=w, q=q, res=res, scale=scale, x=x, weight=weights[w.name]))
+            elif w.op == "mla":
+                # q_c and kv_c as column slices of one projected tensor, as in the model
+                proj = np.zeros((w.T, w.n + w.n2 + gen.MLA_ROPE), np.uint16)
+                proj[:, :w.n] = h["q_c"]
+                proj[:, w.n:w.n + w.n2] = h["kv_c"]
+                pt = torch.from_numpy(proj.view(np.int16)).to(dev)
+                fp8 = w.mode == gen.PER_TOKEN
+                q = torch.empty((w.T, w.n), dtype=torch.uint8 if fp8 else torch.int16, device=dev)
+                scale = torch.empty((w.T,), dtype=torch.float32, device=dev) if fp8 else None
+                kv = torch.empty((w.T, w.n2), dtype=torch.int16, device=dev)
+                qw, kw = weights[w.name]
+                self.ops.append(dict(w=w, q=q, scale=scale, kv=kv, q_c=pt[:, :w.n],
+                                     kv_c=pt[:, w.n:w.n + w.n2], q_weight=qw, kv_weight=kw))
             else:
                 gu = torch.from_numpy(h["gate_up"].view(np.int16)).to(dev)
                 q = torch.empty((w.T, w.n), dtype=torch.uint8, device=dev)
@@ -276,11 +291,31 @@ class DeviceSet:
         return torch.empty((w.T, w.n // w.group_size), dtype=torch.float32, device=dev)
 
 
+def device_weights(torch, step, host, dev):
+    """Each op's weights on the device, shared by all buffer sets."""
+    out = {}
+    for w, h in zip(step, host):
+        if w.op == "norm":
+            out[w.name] = torch.from_numpy(h["weight"].view(np.int16)).to(dev)
+        elif w.op == "mla":
+            out[w.name] = tuple(torch.from_numpy(h[k].view(np.int16)).to(dev)
+                                for k in ("q_weight", "kv_weight"))
+    return out
+
+
 def launch(vg, op):
     w = op["w"]
     if w.op == "norm":
         vg.vg_fused_add_rms_norm_fp8(op["q"], op["res"], op["scale"], op["x"], op["res"],
                                      op["weight"], w.eps, w.mode, w.group_size)
+    elif w.op == "mla":
+        if w.mode == gen.PER_TOKEN:
+            vg.vg_fused_mla_dual_rms_norm_per_token_quant(op["q"], op["scale"], op["kv"], op["q_c"],
+                                                          op["q_weight"], op["kv_c"],
+                                                          op["kv_weight"], w.eps, w.eps)
+        else:
+            vg.vg_fused_mla_dual_rms_norm(op["q"], op["kv"], op["q_c"], op["q_weight"], op["kv_c"],
+                                          op["kv_weight"], w.eps, w.eps)
     else:
         vg.vg_silu_mul_fp8(op["q"], op["scale"], op["gate_up"], w.mode, w.group_size)
 
@@ -297,8 +332,7 @@ def run_gpu(args, dist):
     step = select_step(args)
     nbytes = step_bytes(step)
     host = [w.inputs() for w in step]
-    weights = {w.name: torch.from_numpy(h["weight"].view(np.int16)).to(dev)
-               for w, h in zip(step, host) if w.op == "norm"}
+    weights = device_weights(torch, step, host, dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
     resident = nbytes  # every set holds one copy of every input and output
@@ -425,10 +459,19 @@ def select_step(args):
     return step
 
 
+def mode_name(w):
+    if w.op == "mla":
+        return "q_fp8_per_token" if w.mode == gen.PER_TOKEN else "bf16"
+    return gen.MODE_NAMES[w.mode]
+
+
 def describe(w):
-    return {"name": w.name, "op": w.op, "T": w.T, "n": w.n,
-            "mode": gen.MODE_NAMES[w.mode], "group_size": w.group_size if w.mode == gen.PER_GROUP else None,
-            "bytes": w.algorithmic_bytes()}
+    d = {"name": w.name, "op": w.op, "T": w.T, "n": w.n, "mode": mode_name(w),
+         "group_size": w.group_size if w.mode == gen.PER_GROUP and w.op != "mla" else None,
+         "bytes": w.algorithmic_bytes()}
+    if w.op == "mla":
+        d["n2"] = w.n2
+    return d
 
 
 class PackedSet:
@@ -588,6 +631,10 @@ def oracle_step_runner(step, host, threads):
                     futs.append(pool.submit(orc.fused_add_rms_norm_fp8, h["x"][r0:r1],
                                             h["residual"][r0:r1], h["weight"], w.eps, w.mode,
                                             w.group_size, w.static_scale, False))
+                elif w.op == "mla":
+                    futs.append(pool.submit(orc.mla_dual_rms_norm, h["q_c"][r0:r1], h["q_weight"],
+                                            h["kv_c"][r0:r1], h["kv_weight"], w.eps, w.eps,
+                                            w.mode == gen.PER_TOKEN, False))
                 else:
                     futs.append(pool.submit(orc.silu_mul_fp8, h["gate_up"][r0:r1], w.mode,
                                             w.group_size, w.static_scale, False))
@@ -655,7 +702,7 @@ def time_op_point(torch, vg, w, host, dev, stream, steps, warmup, l2):
     buffer sets (together > 3x L2) in one CUDA graph, CUDA events."""
     nbytes = w.algorithmic_bytes()
     n_sets = max(2, min(64, math.ceil(3 * l2 / nbytes)))
-    weights = {w.name: torch.from_numpy(host["weight"].view(np.int16)).to(dev)} if w.op == "norm" else {}
+    weights = device_weights(torch, (w,), [host], dev)
     sets = [DeviceSet(torch, (w,), [host], weights, dev) for _ in range(n_sets)]
     k_launch = max(steps, n_sets)
     with torch.cuda.stream(stream):
@@ -682,7 +729,7 @@ def time_op_point(torch, vg, w, host, dev, stream, steps, warmup, l2):
 def point_record(w, us, peak, peak_kind):
     nbytes = w.algorithmic_bytes()
     gbs = nbytes / (us * 1e-6) / 1e9
-    return {"point": w.name, "op": w.op, "T": w.T, "n": w.n, "mode": gen.MODE_NAMES[w.mode],
+    return {"point": w.name, "op": w.op, "T": w.T, "n": w.n, "mode": mode_name(w),
             "bytes": nbytes, "us": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
             "peak": peak, "peak_source": peak_kind, "tokens_per_s": round(w.T / (us * 1e-6), 1)}
 
@@ -701,8 +748,8 @@ def run_sweep(args):
     peak, peak_kind = measured_peak()
     stream = torch.cuda.Stream(device=dev)
     cache = {}
-    for w in list(gen.NAMED.values()) + gen.sweep():
-        key = (w.op, w.T, w.n, w.x_dist)
+    for w in list(gen.NAMED.values()) + gen.sweep() + gen.mla_workloads():
+        key = (w.op, w.T, w.n, w.n2, w.x_dist)
         if key not in cache:
             cache.clear()
             cache[key] = w.inputs()

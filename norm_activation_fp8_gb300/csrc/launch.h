@@ -117,6 +117,8 @@ struct MlaArgs {
   float inv_n[2];          // 1 / row length
 };
 
+// vpt == 0: the warp-per-token kernel (block/32 tokens per CTA);
+// otherwise the warp-group kernel (rpc tokens per CTA).
 struct MlaPlan {
   int vpt;
   int thr[2];

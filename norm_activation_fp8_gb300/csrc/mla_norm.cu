@@ -9,7 +9,13 @@
 //   fp8  (fused_mla_dual_rms_norm_per_token_quant): q to FP8 e4m3 with a
 //        dynamic per-token scale, kv_normed in bf16.
 //
-// Layout of a CTA: `rpc` tokens, and per token thr[0] threads on the q row
+// Two kernels:
+//   mla_dual_norm_kernel       a token's rows spread over a group of warps
+//                              (the shortest chain per token: few tokens);
+//   mla_dual_norm_warp_kernel  one warp per token (the fewest instructions
+//                              and no barrier per token: many tokens).
+//
+// Layout of a CTA of the first: `rpc` tokens, and per token thr[0] threads on the q row
 // followed by thr[1] threads on the kv row (each a whole number of warps).
 // A thread owns chunks c = lr + k * thr[side], k < VPT, of its row, keeps
 // t = x * w in registers, and the row's sum of squares is reduced in
@@ -52,10 +58,36 @@ __device__ __forceinline__ uint32_t bf16x2_product_rn(float2 t, float y, float d
   return pack_bf16x2_rn(out[0], out[1]);
 }
 
-// Up to four chunks per thread a token takes at most 512 threads (register
-// room for the fp8 q row's state); eight per thread allow 1024.
-template <int VPT, bool QFP8>
-__global__ void __launch_bounds__(VPT < 8 ? 512 : 1024) mla_dual_norm_kernel(const MlaArgs a) {
+// CTAs of up to 512 threads leave room for the fp8 q row's state at up to
+// eight chunks per thread; a token wider than 512 threads (BIG) takes 1024.
+// bf16 of t * (y + dy) for a chunk of 8.  p = fp32(t * y) lies within
+// ~1.5 fp32 ulps of the exact product, so its bf16 rounding is the exact
+// product's unless p sits within a few fp32 ulps of a bf16 midpoint (low
+// half 0x8000); only such chunks (about 1 in 1000) take the double-float path.
+__device__ __noinline__ uint4 bf16x8_product_rn_slow(float2 t0, float2 t1, float2 t2, float2 t3,
+                                                     float y, float dy) {
+  return make_uint4(bf16x2_product_rn(t0, y, dy), bf16x2_product_rn(t1, y, dy),
+                    bf16x2_product_rn(t2, y, dy), bf16x2_product_rn(t3, y, dy));
+}
+
+__device__ __forceinline__ uint4 bf16x8_product_rn(const float2 (&t)[4], float y, float dy) {
+  const float2 yy = make_float2(y, y);
+  float2 p[4];
+  bool near = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    p[i] = f2_mul(t[i], yy);
+    near |= ((__float_as_uint(p[i].x) & 0xFFFFu) - 0x7FF8u) <= 0x10u;
+    near |= ((__float_as_uint(p[i].y) & 0xFFFFu) - 0x7FF8u) <= 0x10u;
+  }
+  if (near)  // rare: out of line, so it costs the common path no registers
+    return bf16x8_product_rn_slow(t[0], t[1], t[2], t[3], y, dy);
+  return make_uint4(pack_bf16x2_rn(p[0].x, p[0].y), pack_bf16x2_rn(p[1].x, p[1].y),
+                    pack_bf16x2_rn(p[2].x, p[2].y), pack_bf16x2_rn(p[3].x, p[3].y));
+}
+
+template <int VPT, bool QFP8, bool BIG>
+__global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const MlaArgs a) {
   __shared__ float4 red[32];      // per warp: sum hi, sum lo, amax
   __shared__ float2 inv[32][2];   // per token slot and side: y, dy
   __shared__ DynScale dq[32];     // per token slot: the q row's fp8 scale
@@ -145,22 +177,124 @@ __global__ void __launch_bounds__(VPT < 8 ? 512 : 1024) mla_dual_norm_kernel(con
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int c = lr + k * ntr;
-      uint4 o;
-      o.x = bf16x2_product_rn(t[k][0], yd.x, yd.y);
-      o.y = bf16x2_product_rn(t[k][1], yd.x, yd.y);
-      o.z = bf16x2_product_rn(t[k][2], yd.x, yd.y);
-      o.w = bf16x2_product_rn(t[k][3], yd.x, yd.y);
+      const uint4 o = bf16x8_product_rn(t[k], yd.x, yd.y);
       if (live && c < nch) st_stream(out + c * kElemsPerChunk, o);
     }
   }
 }
 
-template <int VPT>
+// ----------------------------------------------------------- warp kernel
+//
+// One warp per token when the token's two rows fit 8 chunks per lane
+// (q_dim + kv_dim <= 2048 after rounding each side to 32 chunks; DeepSeek's
+// 1536 + 512 is exactly 8): lane l holds chunks l, l+32, ... of the q row
+// (kq per lane) then of the kv row (kk per lane) as raw bf16.  Both sums of
+// squares reduce by shuffles, every lane computes the scales (the same
+// arithmetic in every lane, so no shared memory and no barrier), and pass 2
+// recomputes t = x * w from the registers.  Warps run independent tokens, so
+// one token's reduction latency hides behind the loads of others.
+
+__device__ __forceinline__ void chunk_t(const uint4 &xv, const uint4 &wv, float2 (&t)[4]) {
+  const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+  const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t[i] = f2_mul(bf16x2_to_f2(xw[i]), bf16x2_to_f2(ww[i]));
+}
+
+constexpr int kMlaWarpChunks = 8;  // chunks per lane over both rows of a token
+
+template <bool QFP8>
+__global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArgs a, const int kq) {
+  __shared__ uint4 ws[kMlaWarpChunks * 32];  // both weights: q chunks, then kv
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const bool live = row < a.T;  // warp-uniform
+  // (side is a run-time value of the unrolled index: selects, not indexing,
+  // keep everything in registers)
+  const uint16_t *src_q = a.src[0] + (live ? row * a.stride[0] : 0);
+  const uint16_t *src_kv = a.src[1] + (live ? row * a.stride[1] : 0);
+
+  // the token's loads go out first, then the CTA stages the weights, so the
+  // two round trips overlap
+  uint4 xv[kMlaWarpChunks];
+#pragma unroll
+  for (int j = 0; j < kMlaWarpChunks; ++j) {
+    const bool q = j < kq;
+    const int c = (q ? j : j - kq) * 32 + lane;
+    xv[j] = live && c < (q ? a.nch[0] : a.nch[1])
+                ? ld_stream_ro((q ? src_q : src_kv) + c * kElemsPerChunk)
+                : make_uint4(0, 0, 0, 0);
+  }
+  for (int i = threadIdx.x; i < a.nch[0] + a.nch[1]; i += blockDim.x)
+    ws[i] = i < a.nch[0] ? ld_keep(a.w[0] + i * kElemsPerChunk)
+                         : ld_keep(a.w[1] + (i - a.nch[0]) * kElemsPerChunk);
+  __syncthreads();
+  if (!live) return;  // whole warps leave together
+  RowAcc acc_q, acc_kv;
+  float am = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMlaWarpChunks; ++j) {
+    const bool q = j < kq;
+    const int c = (q ? j : j - kq) * 32 + lane;
+    const uint4 wv = c < (q ? a.nch[0] : a.nch[1]) ? ws[q ? c : a.nch[0] + c] : make_uint4(0, 0, 0, 0);
+    float2 t[4];
+    float cmax;
+    if (q) {
+      pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_q);
+      am = fmaxf(am, cmax);
+    } else {
+      pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_kv);
+    }
+  }
+  float yq, dyq, ykv, dykv;
+  {
+    float hi = acc_q.ss.x, lo = acc_q.lo.x + acc_q.lo.y;
+    two_sum_acc(hi, lo, acc_q.ss.y);
+    lanes_sum2(hi, lo, 32);
+    rsqrt_df(hi, lo, a.n[0], a.inv_n[0], a.eps[0], yq, dyq);
+  }
+  {
+    float hi = acc_kv.ss.x, lo = acc_kv.lo.x + acc_kv.lo.y;
+    two_sum_acc(hi, lo, acc_kv.ss.y);
+    lanes_sum2(hi, lo, 32);
+    rsqrt_df(hi, lo, a.n[1], a.inv_n[1], a.eps[1], ykv, dykv);
+  }
+  DynScale d;
+  if (QFP8) {
+    d = make_dyn_scale(warp_max(am), yq, dyq);
+    if (lane == 0) a.q_scale[row] = d.s;
+  }
+#pragma unroll
+  for (int j = 0; j < kMlaWarpChunks; ++j) {
+    const bool q = j < kq;
+    const int c = (q ? j : j - kq) * 32 + lane;
+    const int nch = q ? a.nch[0] : a.nch[1];
+    if (c >= nch) continue;
+    float2 t[4];
+    chunk_t(xv[j], ws[q ? c : a.nch[0] + c], t);
+    const int64_t off = (row * nch + c) * kElemsPerChunk;
+    if (QFP8 && q) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 qv = dyn_values(t[e], d);
+        v[2 * e] = qv.x;
+        v[2 * e + 1] = qv.y;
+      }
+      st_stream(a.q8 + off, quant8(v));
+    } else {
+      st_stream((q ? a.out[0] : a.out[1]) + off,
+                bf16x8_product_rn(t, q ? yq : ykv, q ? dyq : dykv));
+    }
+  }
+}
+
+template <int VPT, bool BIG>
 cudaError_t launch_vpt(const MlaArgs &a, bool q_fp8, const MlaPlan &p, cudaStream_t s) {
   if (q_fp8)
-    mla_dual_norm_kernel<VPT, true><<<(unsigned)p.grid, p.block, 0, s>>>(a);
+    mla_dual_norm_kernel<VPT, true, BIG><<<(unsigned)p.grid, p.block, 0, s>>>(a);
   else
-    mla_dual_norm_kernel<VPT, false><<<(unsigned)p.grid, p.block, 0, s>>>(a);
+    mla_dual_norm_kernel<VPT, false, BIG><<<(unsigned)p.grid, p.block, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -170,11 +304,20 @@ cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaSt
   a.thr[0] = p.thr[0];
   a.thr[1] = p.thr[1];
   a.rpc = p.rpc;
+  if (p.vpt == 0) {  // one warp per token
+    const int kq = (a.nch[0] + 31) / 32;
+    if (q_fp8)
+      mla_dual_norm_warp_kernel<true><<<(unsigned)p.grid, p.block, 0, s>>>(a, kq);
+    else
+      mla_dual_norm_warp_kernel<false><<<(unsigned)p.grid, p.block, 0, s>>>(a, kq);
+    return cudaGetLastError();
+  }
   switch (p.vpt) {
-    case 1: return launch_vpt<1>(a, q_fp8, p, s);
-    case 2: return launch_vpt<2>(a, q_fp8, p, s);
-    case 4: return launch_vpt<4>(a, q_fp8, p, s);
-    default: return launch_vpt<8>(a, q_fp8, p, s);
+    case 1: return launch_vpt<1, false>(a, q_fp8, p, s);
+    case 2: return launch_vpt<2, false>(a, q_fp8, p, s);
+    case 4: return launch_vpt<4, false>(a, q_fp8, p, s);
+    default: return p.block > 512 ? launch_vpt<8, true>(a, q_fp8, p, s)
+                                  : launch_vpt<8, false>(a, q_fp8, p, s);
   }
 }
 

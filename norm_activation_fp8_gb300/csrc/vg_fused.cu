@@ -162,13 +162,25 @@ bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, T
   return true;
 }
 
-// MLA dual norm: one token's q row and kv row in one thread group.  Few
-// tokens (decode) take one token per CTA and one chunk per thread for the
-// shortest chain; many tokens take two chunks per thread (more bytes in
-// flight) and pack tokens into CTAs of up to 512 threads.  A token's group
-// stays within 512 threads up to four chunks per thread (eight allow 1024).
+// MLA dual norm.  Many tokens whose two rows fit eight chunks per lane of a
+// warp (DeepSeek's 1536 + 512 exactly): one warp per token, eight tokens per
+// CTA -- the fewest instructions per element, but about 6 us of latency per
+// token, so it pays from about 13 tokens per SM (measured: from T ~ 2048 on
+// 152 SMs).  Otherwise a token's rows spread over a warp group: one token
+// per CTA and one chunk per thread for few tokens (the shortest chain); two
+// chunks per thread and tokens packed into CTAs of up to 512 threads for
+// more.  A token's group stays within 512 threads up to four chunks per
+// thread (eight allow 1024).
 MlaPlan plan_mla(int64_t T, int nq, int nkv, int sms) {
   MlaPlan p;
+  if ((nq + 31) / 32 + (nkv + 31) / 32 <= 8 && T >= 13LL * sms) {
+    p.vpt = 0;
+    p.thr[0] = p.thr[1] = 0;
+    p.rpc = 8;
+    p.block = 256;
+    p.grid = (T + 7) / 8;
+    return p;
+  }
   p.vpt = T >= 4LL * sms ? 2 : 1;
   auto threads = [&](int nch) { return ((nch + p.vpt - 1) / p.vpt + 31) / 32 * 32; };
   while (p.vpt < 8 && threads(nq) + threads(nkv) > 512) p.vpt *= 2;

@@ -40,6 +40,10 @@ def test_mla_deepseek_shapes(T, q_fp8):
     (4096, 2048, 16, 8, 611),     # two chunks per thread at large T
     (8192, 8192, 8, 8, 3),        # four chunks per thread
     (32768, 32768, 8, 8, 3),      # the largest rows: eight chunks per thread
+    (1544, 520, 8, 24, 2100),     # too wide for one warp at large T
+    (1024, 1016, 8, 8, 2100),     # the warp kernel: ragged 4 + 4 chunks per lane
+    (8, 8, 0, 8, 2100),           # the warp kernel: one chunk per side
+    (248, 1792, 0, 16, 3000),     # the warp kernel: 1 + 7 chunks per lane
 ])
 def test_mla_shapes_and_strides(q_dim, kv_dim, q_pad, kv_pad, T, q_fp8):
     run(T, q_dim, kv_dim, q_fp8, seed=q_dim + kv_dim + T, q_pad=q_pad, kv_pad=kv_pad)
