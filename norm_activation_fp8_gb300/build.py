@@ -41,23 +41,33 @@ def _inputs():
     return files
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(lib_path: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib_path):
         return True
-    built = os.path.getmtime(LIB_PATH)
+    built = os.path.getmtime(lib_path)
     return any(os.path.getmtime(f) > built for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link the CUDA library; returns its path."""
-    if not force and not is_stale():
-        return LIB_PATH
-    os.makedirs(BUILD, exist_ok=True)
+# A test-only copy of the library whose pipelined kernels give up their
+# first wait (it also waits on a barrier nothing arrives on) after a short
+# poll limit, so a GPU test can check the timeout report without a fault.
+WAIT_TEST_LIB = os.path.join(BUILD, "libvg_fused_wait_timeout_test.so")
+WAIT_TEST_FLAGS = ("-DVG_TEST_FORCE_WAIT_TIMEOUT", "-DVG_WAIT_LIMIT=4096u")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str | None = None) -> str:
+    """Compile and link the CUDA library (or, with ``out``, a copy built with
+    ``extra_flags`` under that name); returns its path."""
+    lib_path = out or LIB_PATH
+    if not force and not is_stale(lib_path):
+        return lib_path
+    obj_dir = BUILD if out is None else os.path.join(BUILD, "obj_" + os.path.basename(out))
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = nvcc_path()
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
@@ -72,10 +82,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed on {failed}")
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     subprocess.check_call([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs])
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build_wait_test(force: bool = False) -> str:
+    return build(force, extra_flags=WAIT_TEST_FLAGS, out=WAIT_TEST_LIB)
 
 
 if __name__ == "__main__":

@@ -242,8 +242,10 @@ __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, con
     if (RES) tma_load_bulk(st + row_bytes, a.res + row * a.H, row_bytes, &full[s]);
   };
 
+  VG_NEVER_BARRIER;
   if (lr == 0) {
     for (int s = 0; s <= stages; ++s) mbar_init(&full[s], 1);
+    VG_NEVER_BARRIER_INIT();
     fence_mbar_init();
   }
   __syncthreads();
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, con
   for (int64_t row = first; row < a.T && !failed; row += stride, ++i) {
     const int s = (int)(i % stages);
     const unsigned char *st = dsm + (size_t)s * L.stage_bytes;
-    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / stages) & 1));
+    const bool ok = mbar_wait_bounded(&full[s], (uint32_t)((i / stages) & 1)) && !VG_FORCED_TIMEOUT(i == 0);
     const int64_t base = row * a.H;
 
     float2 t[VPT][4];

@@ -194,8 +194,10 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
     tma_load_bulk(st, src, seg_bytes, &full[sg]);
     tma_load_bulk(st + seg_bytes, src + a.I, seg_bytes, &full[sg]);
   };
+  VG_NEVER_BARRIER;
   if (tid == 0) {
     for (int sg = 0; sg < NSEG; ++sg) mbar_init(&full[sg], 1);
+    VG_NEVER_BARRIER_INIT();
     fence_mbar_init();
   }
   __syncthreads();
@@ -212,7 +214,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
 #pragma unroll
     for (int sg = 0; sg < NSEG; ++sg) {
       const unsigned char *st = dsm + (size_t)sg * 2 * seg_bytes;
-      const bool ok = mbar_wait_bounded(&full[sg], (uint32_t)(i & 1));
+      const bool ok = mbar_wait_bounded(&full[sg], (uint32_t)(i & 1)) && !VG_FORCED_TIMEOUT(i == 0 && sg == 0);
 #pragma unroll
       for (int k = 0; k < KS; ++k) {
         const int c = tid + k * a.ntr;  // chunk within the segment

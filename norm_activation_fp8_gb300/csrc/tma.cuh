@@ -13,7 +13,11 @@ namespace vg {
 
 // A wait gives up after this many failed try_wait polls (each poll may
 // suspend the thread for a while): seconds, far beyond any healthy copy.
-constexpr uint32_t kWaitLimit = 1u << 22;
+// (A test build lowers it.)
+#ifndef VG_WAIT_LIMIT
+#define VG_WAIT_LIMIT (1u << 22)
+#endif
+constexpr uint32_t kWaitLimit = VG_WAIT_LIMIT;
 
 // Error bits a kernel leaves in its translation unit's status word.
 constexpr uint32_t kErrWaitTimeout = 1u;
@@ -76,6 +80,20 @@ __device__ __forceinline__ void tma_load_bulk(void *dst_smem, const void *src, u
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Test-only builds (VG_TEST_FORCE_WAIT_TIMEOUT): a barrier that nothing
+// arrives on.  A pipelined kernel waits on it after its first stage wait, so
+// that wait runs out and the CTA takes its failure path while its other
+// copies are in flight.  Product builds compile all of this away.
+#ifdef VG_TEST_FORCE_WAIT_TIMEOUT
+#define VG_NEVER_BARRIER __shared__ uint64_t vg_never_bar
+#define VG_NEVER_BARRIER_INIT() mbar_init(&vg_never_bar, 1)
+#define VG_FORCED_TIMEOUT(first) ((first) && !mbar_wait_bounded(&vg_never_bar, 0))
+#else
+#define VG_NEVER_BARRIER
+#define VG_NEVER_BARRIER_INIT()
+#define VG_FORCED_TIMEOUT(first) false
+#endif
 
 __device__ __forceinline__ uint4 lds128(const void *p) {
   uint4 v;
