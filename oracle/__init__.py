@@ -7,8 +7,9 @@ package never imports it and shares no code with it.
 
 What each function computes is documented in ``oracle.c`` with the passages
 it follows ("Fusion torch.compile passes", sections "RMSNorm + Quantization
-(fuse_norm_quant)", "SiLU+Mul + Quantization (fuse_act_quant)" and "MLA Dual
-RMSNorm (fuse_mla_dual_rms_norm)"; OCP OFP8 for the E4M3 format).
+(fuse_norm_quant)", "SiLU+Mul + Quantization (fuse_act_quant)", "MLA Dual
+RMSNorm (fuse_mla_dual_rms_norm)" and "RMSNorm + Padding (fuse_act_padding)";
+OCP OFP8 for the E4M3 format).
 
 Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
   bf16 / e4m3 codecs ........ pinned (spec points, exhaustive round trips,
@@ -20,6 +21,8 @@ Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
   rms_norm_bf16 ............. pinned (closed forms, invariants,
                               exact-arithmetic brute force)
   mla_dual_rms_norm ......... the two pinned norms above, side by side
+  fused_add_rms_norm_pad .... pinned (zero tail, bf16 rms_norm on the
+                              stored residual, library bf16 add)
   NaN / Inf inputs .......... parity unpinned (no workload contains them)
 """
 from __future__ import annotations
@@ -73,6 +76,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.orc_silu_mul_fp8.restype = ctypes.c_int
     lib.orc_rms_norm_bf16.argtypes = [P, P, P, P, i64, i64, ctypes.c_float]
     lib.orc_rms_norm_bf16.restype = ctypes.c_int
+    lib.orc_fused_add_rms_norm_pad.argtypes = [P, P, P, P, P, P, i64, i64, i64, ctypes.c_float]
+    lib.orc_fused_add_rms_norm_pad.restype = ctypes.c_int
     for name in ("orc_bf16_decode_n", "orc_bf16_encode_n",
                  "orc_e4m3_decode_n", "orc_e4m3_encode_n"):
         getattr(lib, name).argtypes = [P, P, i64]
@@ -179,6 +184,28 @@ class Oracle:
             raise ValueError(f"oracle rejected the arguments (rc={rc})")
         return {"out": out, "y": y}
 
+    def fused_add_rms_norm_pad(self, x, residual, weight, eps: float, padded: int,
+                               want_y: bool = True):
+        """fused_add_rms_norm(x, residual) with a bf16 output padded to
+        ``padded`` columns (zeros after the first H), or with ``residual``
+        None the plain rms_norm(x) variant.
+
+        Returns dict(out uint16 [T,padded], residual_out uint16 [T,H] or None,
+        y float64 [T,H] before rounding)."""
+        x = _u16(x)
+        T, H = x.shape
+        w = _u16(weight).reshape(H)
+        res = None if residual is None else _u16(residual).reshape(T, H)
+        out = np.empty((T, padded), np.uint16)
+        r_out = None if res is None else np.empty((T, H), np.uint16)
+        y = np.empty((T, H), np.float64) if want_y else None
+        rc = self.lib.orc_fused_add_rms_norm_pad(_ptr(out), _ptr(r_out), _ptr(y), _ptr(x),
+                                                 _ptr(res), _ptr(w), T, H, padded,
+                                                 ctypes.c_float(eps))
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (rc={rc})")
+        return {"out": out, "residual_out": r_out, "y": y}
+
     def mla_dual_rms_norm(self, q_c, q_weight, kv_c, kv_weight, eps_q: float,
                           eps_kv: float, q_fp8: bool = False, want_v: bool = True):
         """fused_mla_dual_rms_norm: the two norms of the unfused MLA graph,
@@ -273,3 +300,7 @@ def rms_norm_bf16(*args, **kwargs):
 
 def mla_dual_rms_norm(*args, **kwargs):
     return default().mla_dual_rms_norm(*args, **kwargs)
+
+
+def fused_add_rms_norm_pad(*args, **kwargs):
+    return default().fused_add_rms_norm_pad(*args, **kwargs)

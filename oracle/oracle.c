@@ -22,6 +22,9 @@
  *         paired q_c / kv_c RMSNorms of MLA attention (each with its own
  *         weight and eps) in one call, and its per-token-quant variant where
  *         q goes to FP8 with a per-token scale and kv stays bf16.
+ *         Section "RMSNorm + Padding (fuse_act_padding)" -- residual add +
+ *         RMSNorm fused with the padding of the hidden dimension to the
+ *         multiple the next GEMM needs (GPT-OSS, hidden 2880).
  *  [OFP8] OCP 8-bit Floating Point Specification (OFP8), E4M3 encoding:
  *         bias 7, no infinities, S.1111.111 is NaN, max normal 448
  *         (S.1111.110), min normal 2^-6, min subnormal 2^-9.
@@ -297,6 +300,50 @@ int orc_rms_norm_bf16(uint16_t *out, double *y, const uint16_t *x,
             double yj = r[j] * inv * orc_bf16_decode(weight[j]);
             out[t * H + j] = orc_bf16_encode(yj);
             if (y)
+                y[t * H + j] = yj;
+        }
+    }
+    free(r);
+    return 0;
+}
+
+/* fused_add_rms_norm(x, residual) -> pad, rows t = 0..T-1 ([FUS] "RMSNorm +
+ * Padding (fuse_act_padding)"): the normalised row stays bf16 and is written
+ * into a row of Hp >= H columns whose tail is zero:
+ *   r_j    = bf16(x_j + residual_j)   (-> residual_out; r = x without residual)
+ *   y_j    = r_j / sqrt(mean_j(r_j^2) + eps) * w_j          (fp64)
+ *   out_j  = bf16(y_j) for j < H, 0 for H <= j < Hp          (one rounding)
+ * Layouts: x, residual, residual_out [T, H]; out [T, Hp]; y (optional) [T, H]. */
+int orc_fused_add_rms_norm_pad(uint16_t *out, uint16_t *residual_out, double *y,
+                               const uint16_t *x, const uint16_t *residual,
+                               const uint16_t *weight, int64_t T, int64_t H,
+                               int64_t Hp, float eps)
+{
+    if (T < 0 || H <= 0 || Hp < H)
+        return -1;
+    double *r = (double *)malloc((size_t)H * sizeof(double));
+    if (!r)
+        return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t *xrow = x + t * H;
+        for (int64_t j = 0; j < H; ++j) {
+            if (residual) {
+                uint16_t rb = orc_bf16_encode(orc_bf16_decode(xrow[j]) +
+                                              orc_bf16_decode(residual[t * H + j]));
+                residual_out[t * H + j] = rb;
+                r[j] = orc_bf16_decode(residual_out[t * H + j]);
+            } else {
+                r[j] = orc_bf16_decode(xrow[j]);
+            }
+        }
+        double sq = 0.0;
+        for (int64_t j = 0; j < H; ++j)
+            sq += r[j] * r[j];
+        double scale = 1.0 / sqrt(sq / (double)H + (double)eps);
+        for (int64_t j = 0; j < Hp; ++j) {
+            double yj = j < H ? r[j] * scale * orc_bf16_decode(weight[j]) : 0.0;
+            out[t * Hp + j] = j < H ? orc_bf16_encode(yj) : 0;
+            if (y && j < H)
                 y[t * H + j] = yj;
         }
     }

@@ -432,6 +432,40 @@ def check_rms_norm_bf16_brute_force(orc):
             np.testing.assert_allclose(out["y"][t], [float(v) for v in ex["y"]], rtol=1e-13)
 
 
+# ----------------------------------------------------- act padding
+
+
+def check_norm_pad(orc):
+    """The padded tail is zero; the first H columns are the bf16 rms_norm of
+    the stored residual (pinned above); residual_out is torch's bf16 add; the
+    plain variant equals the bf16 rms_norm of x; padded = H adds nothing."""
+    rng = np.random.default_rng(24)
+    T, H, Hp = 5, 360, 384
+    x = _rand_bf16(rng, (T, H), scale=np.exp2(rng.integers(-4, 4, (T, H))))
+    res = _rand_bf16(rng, (T, H))
+    w = _weight(rng, H)
+    out = orc.fused_add_rms_norm_pad(x, res, w, 1e-6, Hp)
+    assert out["out"].shape == (T, Hp)
+    assert np.all(out["out"][:, H:] == 0)
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float()
+    rt = torch.from_numpy(res.view(np.int16)).view(torch.bfloat16).float()
+    lib = (xt + rt).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(out["residual_out"], lib)
+    ref = orc.rms_norm_bf16(out["residual_out"], w, 1e-6)
+    assert np.array_equal(out["out"][:, :H], ref["out"])
+    plain = orc.fused_add_rms_norm_pad(x, None, w, 1e-6, Hp)
+    assert plain["residual_out"] is None
+    assert np.array_equal(plain["out"][:, :H], orc.rms_norm_bf16(x, w, 1e-6)["out"])
+    big = orc.fused_add_rms_norm_pad(x, res, w, 0.5, Hp)  # an eps that matters
+    assert np.array_equal(big["out"][:, :H], orc.rms_norm_bf16(big["residual_out"], w, 0.5)["out"])
+    assert not np.array_equal(big["out"], out["out"])
+    same = orc.fused_add_rms_norm_pad(x, res, w, 1e-6, H)
+    assert np.array_equal(same["out"], out["out"][:, :H])
+    for t in range(2):
+        ex = exact.exact_norm_row(x[t], res[t], w, 1e-6, STATIC, 0, 1.0, 1e-10)
+        assert list(out["out"][t, :H]) == [exact.bf16_nearest_code(v) for v in ex["y"]]
+
+
 ALL_CHECKS = [
     check_e4m3_spec_points, check_e4m3_all_codes, check_e4m3_encoder_brute_force,
     check_e4m3_special_values, check_bf16_all_patterns, check_bf16_encoder_brute_force,
@@ -439,5 +473,5 @@ ALL_CHECKS = [
     check_norm_residual_add_library, check_norm_brute_force, check_per_token_max_code,
     check_per_group_layout, check_zero_row_and_saturation, check_silu_closed_forms,
     check_silu_brute_force, check_silu_modes, check_rms_norm_bf16_closed_forms,
-    check_rms_norm_bf16_invariants, check_rms_norm_bf16_brute_force,
+    check_rms_norm_bf16_invariants, check_rms_norm_bf16_brute_force, check_norm_pad,
 ]

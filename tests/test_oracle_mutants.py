@@ -49,6 +49,15 @@ MUTANTS = {
                                 " * orc_bf16_decode(weight[j]);"),
     "bf16_norm_row_offset_dropped": ("r[j] = orc_bf16_decode(x[t * H + j]);",
                                      "r[j] = orc_bf16_decode(x[j]);"),
+    "pad_tail_not_zero": ("out[t * Hp + j] = j < H ? orc_bf16_encode(yj) : 0;",
+                          "out[t * Hp + j] = j < H ? orc_bf16_encode(yj) : 0x3F80;"),
+    "pad_row_stride_unpadded": ("out[t * Hp + j] = j < H ? orc_bf16_encode(yj) : 0;",
+                                "if (j < H) out[t * H + j] = orc_bf16_encode(yj);"),
+    "pad_residual_not_added": ("uint16_t rb = orc_bf16_encode(orc_bf16_decode(xrow[j]) +\n"
+                               "                                              orc_bf16_decode(residual[t * H + j]));",
+                               "uint16_t rb = orc_bf16_encode(orc_bf16_decode(xrow[j]));"),
+    "pad_eps_dropped": ("double scale = 1.0 / sqrt(sq / (double)H + (double)eps);",
+                        "double scale = 1.0 / sqrt(sq / (double)H);"),
 }
 
 
