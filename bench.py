@@ -63,6 +63,7 @@ STEPS = {
 STEPS.update({name: (w,) for name, w in gen.NAMED.items()})
 STEPS.update({w.name: (w,) for w in gen.sweep()})
 STEPS.update({w.name: (w,) for w in gen.mla_workloads()})
+STEPS.update({w.name: (w,) for w in gen.pad_workloads()})
 DEFAULT_STEP = "llama3_8b_decode"
 
 
@@ -211,6 +212,8 @@ _CSRC = "norm_activation_fp8_gb300/csrc/"
 KERNEL_SOURCES = {
     "norm": [_CSRC + f for f in ("norm_fp8.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
                                  "tma.cuh", "vg_fused.cu")],
+    "pad": [_CSRC + f for f in ("norm_fp8.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
+                                "tma.cuh", "vg_fused.cu")],
     "silu": [_CSRC + f for f in ("silu_fp8.cu", "common.cuh", "tma.cuh", "vg_fused.cu")],
     "mla": [_CSRC + f for f in ("mla_norm.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
                                 "vg_fused.cu")],
@@ -263,6 +266,11 @@ class DeviceSet:
                 q = torch.empty((w.T, w.n), dtype=torch.uint8, device=dev)
                 scale = self._scale(torch, w, dev)
                 self.ops.append(dict(w=w, q=q, res=res, scale=scale, x=x, weight=weights[w.name]))
+            elif w.op == "pad":
+                x = torch.from_numpy(h["x"].view(np.int16)).to(dev)
+                res = torch.from_numpy(h["residual"].view(np.int16)).to(dev)
+                out = torch.empty((w.T, w.n2), dtype=torch.int16, device=dev)
+                self.ops.append(dict(w=w, out=out, res=res, x=x, weight=weights[w.name]))
             elif w.op == "mla":
                 # q_c and kv_c as column slices of one projected tensor, as in the model
                 proj = np.zeros((w.T, w.n + w.n2 + gen.MLA_ROPE), np.uint16)
@@ -295,7 +303,7 @@ def device_weights(torch, step, host, dev):
     """Each op's weights on the device, shared by all buffer sets."""
     out = {}
     for w, h in zip(step, host):
-        if w.op == "norm":
+        if w.op in ("norm", "pad"):
             out[w.name] = torch.from_numpy(h["weight"].view(np.int16)).to(dev)
         elif w.op == "mla":
             out[w.name] = tuple(torch.from_numpy(h[k].view(np.int16)).to(dev)
@@ -308,6 +316,8 @@ def launch(vg, op):
     if w.op == "norm":
         vg.vg_fused_add_rms_norm_fp8(op["q"], op["res"], op["scale"], op["x"], op["res"],
                                      op["weight"], w.eps, w.mode, w.group_size)
+    elif w.op == "pad":
+        vg.vg_fused_add_rms_norm_pad(op["out"], op["res"], op["x"], op["res"], op["weight"], w.eps)
     elif w.op == "mla":
         if w.mode == gen.PER_TOKEN:
             vg.vg_fused_mla_dual_rms_norm_per_token_quant(op["q"], op["scale"], op["kv"], op["q_c"],
@@ -460,6 +470,8 @@ def select_step(args):
 
 
 def mode_name(w):
+    if w.op == "pad":
+        return f"bf16_padded_to_{w.n2}"
     if w.op == "mla":
         return "q_fp8_per_token" if w.mode == gen.PER_TOKEN else "bf16"
     return gen.MODE_NAMES[w.mode]
@@ -469,7 +481,7 @@ def describe(w):
     d = {"name": w.name, "op": w.op, "T": w.T, "n": w.n, "mode": mode_name(w),
          "group_size": w.group_size if w.mode == gen.PER_GROUP and w.op != "mla" else None,
          "bytes": w.algorithmic_bytes()}
-    if w.op == "mla":
+    if w.op in ("mla", "pad"):
         d["n2"] = w.n2
     return d
 
@@ -631,6 +643,9 @@ def oracle_step_runner(step, host, threads):
                     futs.append(pool.submit(orc.fused_add_rms_norm_fp8, h["x"][r0:r1],
                                             h["residual"][r0:r1], h["weight"], w.eps, w.mode,
                                             w.group_size, w.static_scale, False))
+                elif w.op == "pad":
+                    futs.append(pool.submit(orc.fused_add_rms_norm_pad, h["x"][r0:r1],
+                                            h["residual"][r0:r1], h["weight"], w.eps, w.n2, False))
                 elif w.op == "mla":
                     futs.append(pool.submit(orc.mla_dual_rms_norm, h["q_c"][r0:r1], h["q_weight"],
                                             h["kv_c"][r0:r1], h["kv_weight"], w.eps, w.eps,
@@ -748,7 +763,7 @@ def run_sweep(args):
     peak, peak_kind = measured_peak()
     stream = torch.cuda.Stream(device=dev)
     cache = {}
-    for w in list(gen.NAMED.values()) + gen.sweep() + gen.mla_workloads():
+    for w in list(gen.NAMED.values()) + gen.sweep() + gen.mla_workloads() + gen.pad_workloads():
         key = (w.op, w.T, w.n, w.n2, w.x_dist)
         if key not in cache:
             cache.clear()

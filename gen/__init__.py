@@ -107,11 +107,11 @@ def mla_inputs(T: int, q_dim: int, kv_dim: int, seed: int = 0):
 class Workload:
     """One op invocation: which op, its shape, scale mode and inputs."""
     name: str
-    op: str                  # "norm", "silu" or "mla"
+    op: str                  # "norm", "silu", "mla" or "pad"
     T: int
     n: int                   # hidden (norm), intermediate (silu) or q_dim (mla)
     mode: int                # mla: PER_TOKEN = q to fp8, STATIC = bf16 q
-    n2: int = 0              # mla: kv_dim
+    n2: int = 0              # mla: kv_dim; pad: padded row length
     group_size: int = 128
     eps: float = 1e-5
     static_scale: float = 0.05
@@ -121,7 +121,7 @@ class Workload:
     note: str = field(default="", compare=False)
 
     def inputs(self):
-        if self.op == "norm":
+        if self.op in ("norm", "pad"):
             return norm_inputs(self.T, self.n, self.seed, self.x_dist)
         if self.op == "mla":
             return mla_inputs(self.T, self.n, self.n2, self.seed)
@@ -135,6 +135,8 @@ class Workload:
         if self.op == "norm":
             per_row = (7 if self.residual else 3) * self.n + s_row
             return self.T * per_row + 2 * self.n + s0
+        if self.op == "pad":  # x, residual read; residual_out and the padded row written
+            return self.T * (6 * self.n + 2 * self.n2) + 2 * self.n
         if self.op == "mla":  # both rows read; q out as fp8 + scale or bf16; kv out bf16
             q_out = self.n + 4 if self.mode == PER_TOKEN else 2 * self.n
             return self.T * (2 * self.n + 4 * self.n2 + q_out) + 2 * (self.n + self.n2)
@@ -155,6 +157,17 @@ CFG3 = Workload("norm_per_group128_16384x8192_t3", "norm", 16384, 8192, PER_GROU
 CFG1_ACT = Workload("silu_per_token_256x14336", "silu", 256, 14336, PER_TOKEN)
 
 NAMED = {w.name: w for w in (CFG0, CFG1, CFG2A, CFG2B, CFG3, CFG1_ACT)}
+
+# Residual add + RMSNorm into a padded bf16 row at GPT-OSS's hidden size,
+# padded to the next multiple of 256.
+PAD_HIDDEN, PAD_PADDED = 2880, 3072
+PAD_T = (1, 64, 512, 4096, 32768)
+
+
+def pad_workloads():
+    return [Workload(f"norm_pad_{T}x{PAD_HIDDEN}_{PAD_PADDED}", "pad", T, PAD_HIDDEN, PER_TOKEN,
+                     n2=PAD_PADDED, eps=1e-6) for T in PAD_T]
+
 
 # The MLA dual norm at DeepSeek-V3's latent sizes (q_lora_rank 1536,
 # kv_lora_rank 512), bf16 and per-token-fp8 q, decode and prefill token counts.

@@ -14,7 +14,9 @@
  *   table: both fusions apply for every num_tokens.  Section "MLA Dual
  *   RMSNorm (fuse_mla_dual_rms_norm)": the paired q_c / kv_c RMSNorms of MLA
  *   attention in one kernel, and its per-token-quant variant (q to FP8 with
- *   a per-token scale, kv in bf16).
+ *   a per-token scale, kv in bf16).  Section "RMSNorm + Padding
+ *   (fuse_act_padding)": residual add + RMSNorm written into a padded bf16
+ *   row.
  *
  * Numerics (the pages give no formulas; these are the readings the library
  * implements):
@@ -26,8 +28,8 @@
  *         per-token: fp32(max(amax over the row, 1e-10f) / 448)
  *         per-group: fp32(max(amax over G columns, 1e-10f) / 448)
  *   The kernels multiply by 1/s, computed once per row or group.
- *   A norm with a bf16 output (the MLA dual norm) rounds y once, to nearest
- *   even bf16, as the exact value would round.
+ *   A norm with a bf16 output (the MLA dual norm, the padded norm) rounds y
+ *   once, to nearest even bf16, as the exact value would round.
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
@@ -122,6 +124,27 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
 vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up,
                           int64_t num_tokens, int64_t inter, int32_t mode,
                           int32_t group_size, vg_stream_t stream);
+
+/*
+ * Residual add + RMSNorm into a padded bf16 row ("RMSNorm + Padding
+ * (fuse_act_padding)"): the normalised row stays bf16 and is written into a
+ * row of padded_hidden columns whose tail is zero, the width the next GEMM
+ * needs.
+ *
+ *   out          out  uint16 [T, padded_hidden]  bf16: columns [0, H) are
+ *                                    bf16(y) (one rounding), [H, padded) zero
+ *   residual_out out  uint16 [T, H]  as for vg_fused_add_rms_norm_fp8 (may
+ *                                    equal `residual`; NULL iff residual is)
+ *   x, residual, weight, num_tokens, hidden, eps  as for
+ *                                    vg_fused_add_rms_norm_fp8
+ *   padded_hidden  >= hidden, a multiple of 8, at most 2 * VG_MAX_ROW
+ *                  (else VG_ERR_BAD_SHAPE)
+ * `out` must not overlap any other tensor.
+ */
+vg_status vg_fused_add_rms_norm_pad(uint16_t *out, uint16_t *residual_out, const uint16_t *x,
+                                    const uint16_t *residual, const uint16_t *weight,
+                                    int64_t num_tokens, int64_t hidden, int64_t padded_hidden,
+                                    float eps, vg_stream_t stream);
 
 /*
  * MLA dual RMSNorm ("MLA Dual RMSNorm (fuse_mla_dual_rms_norm)"): in one

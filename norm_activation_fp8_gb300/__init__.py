@@ -11,6 +11,7 @@ Entry points (same names and argument order as the C ABI):
   vg_fused_add_rms_norm_fp8(q, residual_out, scale, x, residual, weight,
                             eps, mode, group_size=128, stream=None)
   vg_silu_mul_fp8(q, scale, gate_up, mode, group_size=128, stream=None)
+  vg_fused_add_rms_norm_pad(out, residual_out, x, residual, weight, eps, stream=None)
   vg_fused_mla_dual_rms_norm(q_out, kv_out, q_c, q_weight, kv_c, kv_weight,
                              eps_q, eps_kv, stream=None)
   vg_fused_mla_dual_rms_norm_per_token_quant(q_fp8, q_scale, kv_out, q_c,
@@ -19,6 +20,7 @@ Entry points (same names and argument order as the C ABI):
 Convenience wrappers that allocate the outputs with torch:
   fused_add_rms_norm_fp8(x, residual, weight, eps, mode, ...)
   silu_mul_fp8(gate_up, mode, ...)
+  fused_add_rms_norm_pad(x, residual, weight, eps, padded_hidden, ...)
   mla_dual_rms_norm(q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, q_fp8=False)
 """
 from __future__ import annotations
@@ -37,7 +39,8 @@ STATUS_NAMES = {
     4: "VG_ERR_BAD_MODE", 5: "VG_ERR_BAD_GROUP", 6: "VG_ERR_UNSUPPORTED_DEVICE", 7: "VG_ERR_CUDA",
 }
 
-EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_fused_mla_dual_rms_norm",
+EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_fused_add_rms_norm_pad",
+                    "vg_fused_mla_dual_rms_norm",
                     "vg_fused_mla_dual_rms_norm_per_token_quant", "vg_device_status",
                     "vg_status_string", "vg_abi_version")
 DEVICE_WAIT_TIMEOUT = 1
@@ -73,6 +76,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.vg_silu_mul_fp8.argtypes = [P, P, P, i64, i64, i32, i32, P]
         lib.vg_silu_mul_fp8.restype = ctypes.c_int
         f32 = ctypes.c_float
+        lib.vg_fused_add_rms_norm_pad.argtypes = [P, P, P, P, P, i64, i64, i64, f32, P]
+        lib.vg_fused_add_rms_norm_pad.restype = ctypes.c_int
         lib.vg_fused_mla_dual_rms_norm.argtypes = [P, P, P, i64, P, P, i64, P, i64, i64, i64,
                                                    f32, f32, P]
         lib.vg_fused_mla_dual_rms_norm.restype = ctypes.c_int
@@ -175,6 +180,24 @@ def vg_silu_mul_fp8(q, scale, gate_up, mode: int, group_size: int = 128, stream=
                                 _ptr(gate_up, bf16, "gate_up"), num_tokens, inter, mode,
                                 group_size, _stream(stream))
     _check(st)
+
+
+def vg_fused_add_rms_norm_pad(out, residual_out, x, residual, weight, eps: float, stream=None,
+                              num_tokens: int | None = None, hidden: int | None = None,
+                              padded_hidden: int | None = None):
+    """Residual add + RMSNorm into a padded bf16 row through the C ABI.
+
+    out [T, padded] bf16 (columns >= H come back zero); residual_out [T,H]
+    (may be ``residual`` itself) or None with residual None; x [T,H]; weight [H]."""
+    bf16, _, _ = _dtypes()
+    if num_tokens is None or hidden is None:
+        num_tokens, hidden = _rows(x, "x")
+    if padded_hidden is None:
+        padded_hidden = _rows(out, "out")[1]
+    _check(load().vg_fused_add_rms_norm_pad(
+        _ptr(out, bf16, "out"), _ptr(residual_out, bf16, "residual_out"), _ptr(x, bf16, "x"),
+        _ptr(residual, bf16, "residual"), _ptr(weight, bf16, "weight"), num_tokens, hidden,
+        padded_hidden, ctypes.c_float(eps), _stream(stream)))
 
 
 def _rows_ptr(t, name):
@@ -287,3 +310,16 @@ def mla_dual_rms_norm(q_c, q_weight, kv_c, kv_weight, eps_q: float, eps_kv: floa
     q = torch.empty((T, q_dim), dtype=q_c.dtype, device=q_c.device)
     vg_fused_mla_dual_rms_norm(q, kv, q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, stream)
     return q, kv
+
+
+def fused_add_rms_norm_pad(x, residual, weight, eps: float, padded_hidden: int,
+                           inplace: bool = True, stream=None):
+    """Returns (out bf16 [T, padded_hidden], residual_out)."""
+    import torch
+    T, H = x.shape
+    out = torch.empty((T, padded_hidden), dtype=x.dtype, device=x.device)
+    r_out = None
+    if residual is not None:
+        r_out = residual if inplace else torch.empty_like(residual)
+    vg_fused_add_rms_norm_pad(out, r_out, x, residual, weight, eps, stream)
+    return out, r_out

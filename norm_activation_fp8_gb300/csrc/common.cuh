@@ -8,13 +8,15 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "launch.h"
+
 namespace vg {
 
 constexpr float kE4M3Max = 448.0f;   // largest finite OCP E4M3FN value
 constexpr float kAmaxFloor = 1e-10f; // floor on a dynamic amax (no 0/0 on zero rows)
 constexpr int kElemsPerChunk = 8;    // bf16 elements per 16-byte vector
 
-enum ScaleMode : int { kStatic = 0, kPerToken = 1, kPerGroup = 2 };
+
 
 // ------------------------------------------------------------------ bf16
 

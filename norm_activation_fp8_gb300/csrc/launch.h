@@ -6,6 +6,10 @@
 
 namespace vg {
 
+// kStatic / kPerToken / kPerGroup are vg_scale_mode; kBf16Pad is the
+// norm's bf16 output into a padded row (no quantisation).
+enum ScaleMode : int { kStatic = 0, kPerToken = 1, kPerGroup = 2, kBf16Pad = 3 };
+
 // How a row-wise kernel covers a [T, n] tensor: each row is split into
 // nch = n/8 chunks of 16 bytes; `ntr` threads (a multiple of 32) own a row,
 // thread i holding chunks i, i + ntr, ..., i + (vpt-1)*ntr; a CTA carries
@@ -43,6 +47,8 @@ struct NormArgs {
   int32_t ngroups; // H / G, per-group mode only
   float eps;
   float inv_h;     // 1 / H
+  uint16_t *out16; // kBf16Pad: bf16 output rows of nch_pad chunks
+  int32_t nch_pad; // kBf16Pad: padded row length / 8
 };
 
 struct SiluArgs {

@@ -35,57 +35,8 @@ namespace vg {
 
 namespace {
 
-// bf16(t * (y + dy)) for two elements, rounded as the exact product would
-// be (y + dy normalised, |dy| <= half an ulp of y).
-__device__ __forceinline__ uint32_t bf16x2_product_rn(float2 t, float y, float dy) {
-  float out[2];
-  const float tv[2] = {t.x, t.y};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float p = tv[i] * y;
-    const float e = fmaf(tv[i], y, -p) + tv[i] * dy;  // t (y + dy) = p + e to ~2^-44
-    const float hi = p + e;                             // |e| < ulp(p): Fast2Sum
-    const float lo = e - (hi - p);
-    const uint32_t b = __float_as_uint(hi);
-    // a hi exactly on a bf16 midpoint is decided by the sign of lo
-    const float r = ((b & 0xFFFFu) == 0x8000u && lo != 0.f)
-                        ? __uint_as_float(((lo > 0.f) != (b >> 31 != 0u)) ? b + 1u : b - 1u)
-                        : hi;
-    // y > 0, so the product has the sign of t; this keeps a -0 that the
-    // additions above turn into +0
-    out[i] = copysignf(r, tv[i]);
-  }
-  return pack_bf16x2_rn(out[0], out[1]);
-}
-
 // CTAs of up to 512 threads leave room for the fp8 q row's state at up to
 // eight chunks per thread; a token wider than 512 threads (BIG) takes 1024.
-// bf16 of t * (y + dy) for a chunk of 8.  p = fp32(t * y) lies within
-// ~1.5 fp32 ulps of the exact product, so its bf16 rounding is the exact
-// product's unless p sits within a few fp32 ulps of a bf16 midpoint (low
-// half 0x8000); only such chunks (about 1 in 1000) take the double-float path.
-__device__ __noinline__ uint4 bf16x8_product_rn_slow(float2 t0, float2 t1, float2 t2, float2 t3,
-                                                     float y, float dy) {
-  return make_uint4(bf16x2_product_rn(t0, y, dy), bf16x2_product_rn(t1, y, dy),
-                    bf16x2_product_rn(t2, y, dy), bf16x2_product_rn(t3, y, dy));
-}
-
-__device__ __forceinline__ uint4 bf16x8_product_rn(const float2 (&t)[4], float y, float dy) {
-  const float2 yy = make_float2(y, y);
-  float2 p[4];
-  bool near = false;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    p[i] = f2_mul(t[i], yy);
-    near |= ((__float_as_uint(p[i].x) & 0xFFFFu) - 0x7FF8u) <= 0x10u;
-    near |= ((__float_as_uint(p[i].y) & 0xFFFFu) - 0x7FF8u) <= 0x10u;
-  }
-  if (near)  // rare: out of line, so it costs the common path no registers
-    return bf16x8_product_rn_slow(t[0], t[1], t[2], t[3], y, dy);
-  return make_uint4(pack_bf16x2_rn(p[0].x, p[0].y), pack_bf16x2_rn(p[1].x, p[1].y),
-                    pack_bf16x2_rn(p[2].x, p[2].y), pack_bf16x2_rn(p[3].x, p[3].y));
-}
-
 template <int VPT, bool QFP8, bool BIG>
 __global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const MlaArgs a) {
   __shared__ float4 red[32];      // per warp: sum hi, sum lo, amax

@@ -91,9 +91,10 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
   }
 
   // Dynamic scales: each scale slot (group, or the row) is computed once,
-  // by the slot's thread, from the warp partials and chunk amaxes.
+  // by the slot's thread, from the warp partials and chunk amaxes.  The bf16
+  // output has one slot per row holding inv = y + dy.
   const int row_chunks = a.ntr * VPT;
-  const int nslots = MODE == kPerToken ? 1 : a.ngroups;
+  const int nslots = MODE == kPerGroup ? a.ngroups : 1;
   float hi = acc.ss.x, lo = acc.lo.x + acc.lo.y;
   two_sum_acc(hi, lo, acc.ss.y);
   lanes_sum2(hi, lo, 32);
@@ -102,7 +103,7 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
 #pragma unroll
     for (int k = 0; k < VPT; ++k) am = fmaxf(am, cmax[k]);
     am = warp_max(am);
-  } else {
+  } else if (MODE == kPerGroup) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) sm.cmax[slot * row_chunks + lr + k * a.ntr] = cmax[k];
   }
@@ -118,16 +119,34 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
     }
     float y, dy;
     rsqrt_df(h, l, (float)a.H, a.inv_h, a.eps, y, dy);
-    if (MODE == kPerGroup) {
-      amr = 0.f;
+    if (MODE == kBf16Pad) {
+      sm.dyn[slot] = DynScale{y, dy, 0.f, 0.f};
+    } else {
+      if (MODE == kPerGroup) {
+        amr = 0.f;
 #pragma unroll
-      for (int i = 0; i < GCH; ++i) amr = fmaxf(amr, sm.cmax[slot * row_chunks + lr * GCH + i]);
+        for (int i = 0; i < GCH; ++i) amr = fmaxf(amr, sm.cmax[slot * row_chunks + lr * GCH + i]);
+      }
+      const DynScale d = make_dyn_scale(amr, y, dy);
+      sm.dyn[slot * nslots + lr] = d;
+      if (live) a.scale[row * nslots + lr] = d.s;
     }
-    const DynScale d = make_dyn_scale(amr, y, dy);
-    sm.dyn[slot * nslots + lr] = d;
-    if (live) a.scale[row * nslots + lr] = d.s;
   }
   __syncthreads();
+  if (MODE == kBf16Pad) {
+    const DynScale d = sm.dyn[slot];  // s = y, a = dy
+    uint16_t *out = a.out16 + (live ? row * (int64_t)a.nch_pad * kElemsPerChunk : 0);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int c = lr + k * a.ntr;
+      const uint4 o = bf16x8_product_rn(t[k], d.s, d.a);
+      if (live && c < a.nch) st_stream(out + c * kElemsPerChunk, o);
+    }
+    // the padded tail is zero
+    for (int c = a.nch + lr; live && c < a.nch_pad; c += a.ntr)
+      st_stream(out + c * kElemsPerChunk, make_uint4(0, 0, 0, 0));
+    return;
+  }
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int c = lr + k * a.ntr;
@@ -224,7 +243,7 @@ template <int VPT, int MODE, int GCH, bool RES>
 __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, const int stages) {
   constexpr bool DYN = MODE != kStatic;
   extern __shared__ __align__(128) unsigned char dsm[];
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerToken ? 1 : a.ngroups);
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup ? a.ngroups : 1);
   const TmaLayout L(a.H, RES, stages, blockDim.x, VPT, slots);
   const RowSmem sm = carve_row_smem(dsm + L.row_off, blockDim.x, VPT);
   unsigned char *wbuf = dsm + L.w_off;
@@ -307,7 +326,7 @@ __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, con
 
 template <int VPT, int MODE, int GCH>
 cudaError_t launch_res(const NormArgs &a, const RowPlan &p, cudaStream_t s) {
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerToken ? 1 : a.ngroups) * p.rpc;
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup ? a.ngroups : 1) * p.rpc;
   const size_t smem = row_smem_bytes(p.block(), VPT, slots);
   if (a.res != nullptr)
     norm_fp8_kernel<VPT, MODE, GCH, true><<<(unsigned)p.grid, p.block(), smem, s>>>(a);
@@ -318,7 +337,7 @@ cudaError_t launch_res(const NormArgs &a, const RowPlan &p, cudaStream_t s) {
 
 template <int VPT, int MODE, int GCH, bool RES>
 cudaError_t launch_tma_res(const NormArgs &a, const TmaPlan &p, cudaStream_t s) {
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerToken ? 1 : a.ngroups);
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup ? a.ngroups : 1);
   const TmaLayout L(a.H, RES, p.stages, p.block, VPT, slots);
   auto kern = norm_fp8_tma_kernel<VPT, MODE, GCH, RES>;
   // opt in to large dynamic shared memory once per instantiation and device
@@ -347,17 +366,20 @@ cudaError_t launch_mode(const NormArgs &a, int mode, const RowPlan &p, cudaStrea
   switch (mode) {
     case kStatic: return launch_res<VPT, kStatic, 1>(a, p, s);
     case kPerToken: return launch_res<VPT, kPerToken, 1>(a, p, s);
+    case kBf16Pad: return launch_res<VPT, kBf16Pad, 1>(a, p, s);
     default:
       return a.gch == 8 ? launch_res<VPT, kPerGroup, 8>(a, p, s)
                         : launch_res<VPT, kPerGroup, 16>(a, p, s);
   }
 }
 
+// (static scales never take the TMA kernel: the register kernel streams at
+// the copy roofline there)
 template <int VPT>
 cudaError_t launch_tma_vpt(const NormArgs &a, int mode, const TmaPlan &p, cudaStream_t s) {
   switch (mode) {
-    case kStatic: return launch_tma_mode<VPT, kStatic, 1>(a, p, s);
     case kPerToken: return launch_tma_mode<VPT, kPerToken, 1>(a, p, s);
+    case kBf16Pad: return launch_tma_mode<VPT, kBf16Pad, 1>(a, p, s);
     default:
       return a.gch == 8 ? launch_tma_mode<VPT, kPerGroup, 8>(a, p, s)
                         : launch_tma_mode<VPT, kPerGroup, 16>(a, p, s);

@@ -313,6 +313,51 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
                                                                                    : VG_ERR_CUDA;
 }
 
+vg_status vg_fused_add_rms_norm_pad(uint16_t *out, uint16_t *residual_out, const uint16_t *x,
+                                    const uint16_t *residual, const uint16_t *weight,
+                                    int64_t num_tokens, int64_t hidden, int64_t padded_hidden,
+                                    float eps, vg_stream_t stream) {
+  vg_status st = vg::check_row(num_tokens, hidden, VG_SCALE_PER_TOKEN, 0);
+  if (st != VG_OK) return st;
+  if (padded_hidden < hidden || padded_hidden % 8 != 0 || padded_hidden > 2LL * VG_MAX_ROW)
+    return VG_ERR_BAD_SHAPE;
+  if (num_tokens == 0) return VG_OK;
+  if (!out || !x || !weight || ((residual == nullptr) != (residual_out == nullptr)))
+    return VG_ERR_NULL_PTR;
+  if (vg::misaligned(out, 16) || vg::misaligned(x, 16) || vg::misaligned(weight, 16) ||
+      vg::misaligned(residual, 16) || vg::misaligned(residual_out, 16))
+    return VG_ERR_MISALIGNED;
+  int sms = 0;
+  if ((st = vg::check_device(&sms)) != VG_OK) return st;
+  vg::clear_stale_error();
+
+  vg::NormArgs a{};
+  a.res_out = residual_out;
+  a.x = x;
+  a.res = residual;
+  a.w = weight;
+  a.T = num_tokens;
+  a.H = (int32_t)hidden;
+  a.nch = (int32_t)(hidden / 8);
+  a.gch = 1;
+  a.ngroups = 1;
+  a.eps = eps;
+  a.inv_h = 1.0f / (float)hidden;
+  a.out16 = out;
+  a.nch_pad = (int32_t)(padded_hidden / 8);
+  // the same plans as the dynamic per-token norm: one double-float inv per row
+  vg::TmaPlan tp;
+  if (vg::plan_norm_tma(num_tokens, (int)hidden, residual != nullptr, VG_SCALE_PER_TOKEN, 1, sms,
+                        &tp))
+    return vg::launch_norm_fp8_tma(a, vg::kBf16Pad, tp, (cudaStream_t)stream) == cudaSuccess
+               ? VG_OK
+               : VG_ERR_CUDA;
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, 4, sms);
+  return vg::launch_norm_fp8(a, vg::kBf16Pad, plan, (cudaStream_t)stream) == cudaSuccess
+             ? VG_OK
+             : VG_ERR_CUDA;
+}
+
 vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int64_t num_tokens,
                           int64_t inter, int32_t mode, int32_t group_size, vg_stream_t stream) {
   vg_status st = vg::check_row(num_tokens, inter, mode, group_size);

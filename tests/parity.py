@@ -199,6 +199,33 @@ def oracle_mla(q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, q_fp8):
     return {k: np.concatenate([p[k] for p in parts]) for k in parts[0]}
 
 
+def oracle_pad(x, residual, weight, eps, padded):
+    """The oracle's padded norm over row blocks run in threads."""
+    T, H = x.shape
+    out = {"out": np.empty((T, padded), np.uint16),
+           "residual_out": None if residual is None else np.empty((T, H), np.uint16)}
+    blocks = _blocks(T, _threads())
+
+    def work(b):
+        r0, r1 = b
+        o = oracle.fused_add_rms_norm_pad(x[r0:r1], None if residual is None else residual[r0:r1],
+                                          weight, eps, padded, want_y=False)
+        out["out"][r0:r1] = o["out"]
+        if residual is not None:
+            out["residual_out"][r0:r1] = o["residual_out"]
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(work, blocks))
+    return out
+
+
+def check_pad(gpu, orc):
+    """The padded bf16 rows (tail included) and residual_out, bit-exact."""
+    compare_exact(gpu["out"], orc["out"], "out")
+    if orc["residual_out"] is not None:
+        compare_exact(gpu["residual_out"], orc["residual_out"], "residual_out")
+
+
 def check_mla(gpu, orc, q_fp8):
     """kv (and a bf16 q) bit-exact; an fp8 q under the code rule, its
     per-token scales within 1e-6."""
@@ -343,3 +370,33 @@ def gpu_mla(q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, q_fp8, rope=64, q_pad
     _check_guards(kbuf, T * kv_dim * 2, "kv_normed")
     out["kv"] = kv_out.cpu().numpy().view(np.uint16)
     return out
+
+
+def gpu_pad(x, residual, weight, eps, padded, inplace=True, device="cuda"):
+    """The CUDA padded norm on numpy bf16-bit inputs; outputs between 0xAA
+    guard bands (the padded tail starts as 0xAA too, so it must be written)."""
+    import torch
+    import norm_activation_fp8_gb300 as vg
+    T, H = x.shape
+    xt = torch.from_numpy(x.view(np.int16)).to(device)
+    wt = torch.from_numpy(np.ascontiguousarray(weight).view(np.int16)).to(device)
+    obuf, oraw = _guarded(torch, T * padded * 2, device)
+    out = oraw.view(torch.int16).view(T, padded)
+    rt = rbuf = r_out = None
+    if residual is not None:
+        rbuf, rraw = _guarded(torch, T * H * 2, device)
+        if inplace:
+            rt = rraw.view(torch.int16).view(T, H)
+            rt.copy_(torch.from_numpy(residual.view(np.int16)))
+            r_out = rt
+        else:
+            rt = torch.from_numpy(residual.view(np.int16)).to(device)
+            r_out = rraw.view(torch.int16).view(T, H)
+    vg.vg_fused_add_rms_norm_pad(out, r_out, xt, rt, wt, eps)
+    torch.cuda.synchronize()
+    _check_guards(obuf, T * padded * 2, "out")
+    res = {"out": out.cpu().numpy().view(np.uint16), "residual_out": None}
+    if residual is not None:
+        _check_guards(rbuf, T * H * 2, "residual_out")
+        res["residual_out"] = r_out.cpu().numpy().view(np.uint16)
+    return res

@@ -38,7 +38,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8"} <= names
-    assert {"vg_fused_mla_dual_rms_norm", "vg_fused_mla_dual_rms_norm_per_token_quant"} <= names
+    assert {"vg_fused_mla_dual_rms_norm", "vg_fused_mla_dual_rms_norm_per_token_quant",
+            "vg_fused_add_rms_norm_pad"} <= names
     assert names == set(vg.EXPORTED_SYMBOLS)
 
 
@@ -177,3 +178,23 @@ def test_binding_mla_rejects_strided_columns(lib):
     x = torch.zeros(4, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         vg.vg_fused_mla_dual_rms_norm(None, None, x, None, x, None, 1e-6, 1e-6)
+
+
+def pad(lib, out=A, r_out=A, x=A, res=A, w=A, T=4, H=2880, Hp=3072, eps=1e-6):
+    return lib.vg_fused_add_rms_norm_pad(out, r_out, x, res, w, T, H, Hp, ctypes.c_float(eps), None)
+
+
+def test_pad_validation(lib):
+    for H in (0, 4, 12, 32776):
+        assert pad(lib, H=H, Hp=70000) == SHAPE, H
+    assert pad(lib, Hp=2872) == SHAPE        # padded below hidden
+    assert pad(lib, Hp=3076) == SHAPE        # not a multiple of 8
+    assert pad(lib, Hp=65544) == SHAPE       # wider than 2 * VG_MAX_ROW
+    assert pad(lib, T=-1) == SHAPE
+    for k in ("out", "x", "w"):
+        assert pad(lib, **{k: None}) == NULL, k
+    assert pad(lib, res=None) == NULL
+    assert pad(lib, r_out=None) == NULL
+    assert pad(lib, out=None, r_out=None, x=None, res=None, w=None, T=0) == OK
+    for k in ("out", "r_out", "x", "res", "w"):
+        assert pad(lib, **{k: A + 8}) == ALIGN, k
