@@ -8,8 +8,8 @@ package never imports it and shares no code with it.
 What each function computes is documented in ``oracle.c`` with the passages
 it follows ("Fusion torch.compile passes", sections "RMSNorm + Quantization
 (fuse_norm_quant)", "SiLU+Mul + Quantization (fuse_act_quant)", "MLA Dual
-RMSNorm (fuse_mla_dual_rms_norm)" and "RMSNorm + Padding (fuse_act_padding)";
-OCP OFP8 for the E4M3 format).
+RMSNorm (fuse_mla_dual_rms_norm)", "RMSNorm + Padding (fuse_act_padding)" and
+"QK Norm + RoPE (enable_qk_norm_rope_fusion)"; OCP OFP8 for the E4M3 format).
 
 Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
   bf16 / e4m3 codecs ........ pinned (spec points, exhaustive round trips,
@@ -23,6 +23,9 @@ Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
   mla_dual_rms_norm ......... the two pinned norms above, side by side
   fused_add_rms_norm_pad .... pinned (zero tail, bf16 rms_norm on the
                               stored residual, library bf16 add)
+  qk_norm_rope .............. pinned (identity and quarter-turn rotations
+                              against the pinned bf16 rms_norm, V untouched,
+                              neox/gptj by permutation, exact rationals)
   NaN / Inf inputs .......... parity unpinned (no workload contains them)
 """
 from __future__ import annotations
@@ -78,6 +81,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.orc_rms_norm_bf16.restype = ctypes.c_int
     lib.orc_fused_add_rms_norm_pad.argtypes = [P, P, P, P, P, P, i64, i64, i64, ctypes.c_float]
     lib.orc_fused_add_rms_norm_pad.restype = ctypes.c_int
+    lib.orc_qk_norm_rope.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i64, ctypes.c_float,
+                                     ctypes.c_int]
+    lib.orc_qk_norm_rope.restype = ctypes.c_int
     for name in ("orc_bf16_decode_n", "orc_bf16_encode_n",
                  "orc_e4m3_decode_n", "orc_e4m3_encode_n"):
         getattr(lib, name).argtypes = [P, P, i64]
@@ -206,6 +212,26 @@ class Oracle:
             raise ValueError(f"oracle rejected the arguments (rc={rc})")
         return {"out": out, "residual_out": r_out, "y": y}
 
+    def qk_norm_rope(self, qkv, q_weight, k_weight, cos_sin_cache, positions, num_q_heads: int,
+                     num_kv_heads: int, head_dim: int, eps: float, is_neox: bool = True,
+                     want_o: bool = True):
+        """fused_qk_norm_rope on a copy of qkv (uint16 bf16 bits
+        [T, (Hq + 2 Hkv) * D]); cos_sin_cache float32 [max_pos, D];
+        positions int64 [T].  Returns dict(qkv uint16 (V columns unchanged),
+        o float64 [T, (Hq + Hkv) * D] before rounding)."""
+        out = _u16(qkv).copy()
+        T = out.shape[0]
+        cache = np.ascontiguousarray(cos_sin_cache, dtype=np.float32)
+        pos = np.ascontiguousarray(positions, dtype=np.int64).reshape(T)
+        o = np.empty((T, (num_q_heads + num_kv_heads) * head_dim), np.float64) if want_o else None
+        rc = self.lib.orc_qk_norm_rope(_ptr(out), _ptr(o), _ptr(_u16(q_weight)), _ptr(_u16(k_weight)),
+                                       _ptr(cache), _ptr(pos), T, num_q_heads, num_kv_heads,
+                                       head_dim, cache.shape[0], ctypes.c_float(eps),
+                                       1 if is_neox else 0)
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (rc={rc})")
+        return {"qkv": out, "o": o}
+
     def mla_dual_rms_norm(self, q_c, q_weight, kv_c, kv_weight, eps_q: float,
                           eps_kv: float, q_fp8: bool = False, want_v: bool = True):
         """fused_mla_dual_rms_norm: the two norms of the unfused MLA graph,
@@ -304,3 +330,7 @@ def mla_dual_rms_norm(*args, **kwargs):
 
 def fused_add_rms_norm_pad(*args, **kwargs):
     return default().fused_add_rms_norm_pad(*args, **kwargs)
+
+
+def qk_norm_rope(*args, **kwargs):
+    return default().qk_norm_rope(*args, **kwargs)

@@ -25,6 +25,9 @@
  *         Section "RMSNorm + Padding (fuse_act_padding)" -- residual add +
  *         RMSNorm fused with the padding of the hidden dimension to the
  *         multiple the next GEMM needs (GPT-OSS, hidden 2880).
+ *         Section "QK Norm + RoPE (enable_qk_norm_rope_fusion)" -- split
+ *         QKV, per-head RMSNorm of Q and K, then rotary embedding, in one
+ *         kernel (models that normalise Q and K per head before RoPE).
  *  [OFP8] OCP 8-bit Floating Point Specification (OFP8), E4M3 encoding:
  *         bias 7, no infinities, S.1111.111 is NaN, max normal 448
  *         (S.1111.110), min normal 2^-6, min subnormal 2^-9.
@@ -348,6 +351,68 @@ int orc_fused_add_rms_norm_pad(uint16_t *out, uint16_t *residual_out, double *y,
         }
     }
     free(r);
+    return 0;
+}
+
+/* fused_qk_norm_rope(qkv) ([FUS] "QK Norm + RoPE"): for every token t and
+ * every Q head (weight q_weight) and K head (weight k_weight) of qkv
+ * [T, (Hq + 2 Hkv) * D] (Q heads, then K heads, then V heads, each D
+ * contiguous columns):
+ *   y_j = x_j / sqrt(mean_j(x_j^2) + eps) * w_j                  (fp64)
+ * then the rotary embedding with c_i = cache[pos_t, i] and
+ * s_i = cache[pos_t, D/2 + i], i < D/2, on the pairs (a, b) = (i, i + D/2)
+ * (neox) or (2i, 2i + 1) (gptj):
+ *   o_a = y_a c_i - y_b s_i,   o_b = y_b c_i + y_a s_i           (fp64)
+ * written back in place as bf16 (one rounding); V heads are not touched.
+ * o (optional) receives the pre-rounding values [T, (Hq + Hkv) * D].
+ * Returns -1 on bad sizes or a position outside [0, max_pos). */
+int orc_qk_norm_rope(uint16_t *qkv, double *o, const uint16_t *q_weight,
+                     const uint16_t *k_weight, const float *cos_sin_cache,
+                     const int64_t *positions, int64_t T, int64_t Hq, int64_t Hkv,
+                     int64_t D, int64_t max_pos, float eps, int is_neox)
+{
+    if (T < 0 || Hq < 0 || Hkv < 0 || D <= 0 || D % 2 != 0 || max_pos <= 0)
+        return -1;
+    for (int64_t t = 0; t < T; ++t)
+        if (positions[t] < 0 || positions[t] >= max_pos)
+            return -1;
+    double *y = (double *)malloc((size_t)D * sizeof(double));
+    double *rot = (double *)malloc((size_t)D * sizeof(double));
+    if (!y || !rot) {
+        free(y);
+        free(rot);
+        return -2;
+    }
+    const int64_t row = (Hq + 2 * Hkv) * D;
+    for (int64_t t = 0; t < T; ++t) {
+        const float *cs = cos_sin_cache + positions[t] * D;
+        for (int64_t h = 0; h < Hq + Hkv; ++h) {
+            uint16_t *head = qkv + t * row + h * D;
+            const uint16_t *w = h < Hq ? q_weight : k_weight;
+            double sq = 0.0;
+            for (int64_t j = 0; j < D; ++j) {
+                double xj = orc_bf16_decode(head[j]);
+                sq += xj * xj;
+            }
+            double inv_rms = 1.0 / sqrt(sq / (double)D + (double)eps);
+            for (int64_t j = 0; j < D; ++j)
+                y[j] = orc_bf16_decode(head[j]) * inv_rms * orc_bf16_decode(w[j]);
+            for (int64_t i = 0; i < D / 2; ++i) {
+                int64_t a = is_neox ? i : 2 * i;
+                int64_t b = is_neox ? i + D / 2 : 2 * i + 1;
+                double c = (double)cs[i], sn = (double)cs[D / 2 + i];
+                rot[a] = y[a] * c - y[b] * sn;
+                rot[b] = y[b] * c + y[a] * sn;
+            }
+            for (int64_t j = 0; j < D; ++j) {
+                head[j] = orc_bf16_encode(rot[j]);
+                if (o)
+                    o[(t * (Hq + Hkv) + h) * D + j] = rot[j];
+            }
+        }
+    }
+    free(y);
+    free(rot);
     return 0;
 }
 

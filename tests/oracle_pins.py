@@ -466,6 +466,94 @@ def check_norm_pad(orc):
         assert list(out["out"][t, :H]) == [exact.bf16_nearest_code(v) for v in ex["y"]]
 
 
+# ------------------------------------------------------- QK norm + RoPE
+
+
+def _qk_case(rng, T, Hq, Hkv, D):
+    qkv = _rand_bf16(rng, (T, (Hq + 2 * Hkv) * D), scale=np.exp2(rng.integers(-3, 3, (T, (Hq + 2 * Hkv) * D))))
+    return qkv, _weight(rng, D), _bits(0.5 + rng.random(D))
+
+
+def check_qk_norm_rope_rotations(orc):
+    """Cache rows of exact rotations: the identity gives the pinned bf16
+    rms_norm of every head; a quarter turn swaps the pair members with one
+    sign flipped; a half turn negates; V columns are never touched."""
+    rng = np.random.default_rng(25)
+    T, Hq, Hkv, D = 3, 3, 2, 16
+    qkv, qw, kw = _qk_case(rng, T, Hq, Hkv, D)
+    cache = np.zeros((3, D), np.float32)
+    cache[0, :D // 2] = 1.0                     # cos 1, sin 0
+    cache[1, D // 2:] = 1.0                     # cos 0, sin 1
+    cache[2, :D // 2] = -1.0                    # cos -1, sin 0
+    nq = Hq * D
+    heads = qkv[:, :(Hq + Hkv) * D].reshape(T, Hq + Hkv, D)
+    ref = np.empty_like(heads)
+    for h in range(Hq + Hkv):
+        ref[:, h] = orc.rms_norm_bf16(heads[:, h], qw if h < Hq else kw, 1e-6)["out"]
+    sign = np.uint16(0x8000)
+    for neox in (True, False):
+        for row in range(3):
+            out = orc.qk_norm_rope(qkv, qw, kw, cache, np.full(T, row), Hq, Hkv, D, 1e-6, neox)
+            got = out["qkv"][:, :(Hq + Hkv) * D].reshape(T, Hq + Hkv, D)
+            if row == 0:
+                want = ref
+            elif row == 2:
+                want = ref ^ sign
+            else:
+                want = np.empty_like(ref)
+                a = np.arange(D // 2) if neox else 2 * np.arange(D // 2)
+                b = a + D // 2 if neox else a + 1
+                want[..., a] = ref[..., b] ^ sign
+                want[..., b] = ref[..., a]
+            assert np.array_equal(got, want), (neox, row)
+            assert np.array_equal(out["qkv"][:, (Hq + Hkv) * D:], qkv[:, (Hq + Hkv) * D:])
+            assert out["qkv"][:, nq:].shape[1] == 2 * Hkv * D
+
+
+def check_qk_norm_rope_pairings(orc):
+    """neox on a head equals gptj on the same head with its columns
+    interleaved (column i -> 2i, column i + D/2 -> 2i + 1), weights likewise."""
+    rng = np.random.default_rng(26)
+    T, Hq, Hkv, D = 4, 2, 1, 16
+    qkv, qw, kw = _qk_case(rng, T, Hq, Hkv, D)
+    cache = (rng.random((5, D)) * 2 - 1).astype(np.float32)
+    pos = np.array([4, 0, 2, 2])
+    perm = np.empty(D, np.int64)
+    perm[2 * np.arange(D // 2)] = np.arange(D // 2)
+    perm[2 * np.arange(D // 2) + 1] = np.arange(D // 2) + D // 2   # gptj column k holds neox column perm[k]
+    heads = qkv.reshape(T, Hq + 2 * Hkv, D)
+    qkv_g = heads[:, :, perm].reshape(T, -1)
+    a = orc.qk_norm_rope(qkv, qw, kw, cache, pos, Hq, Hkv, D, 1e-5, True)["qkv"]
+    b = orc.qk_norm_rope(qkv_g, qw[perm], kw[perm], cache, pos, Hq, Hkv, D, 1e-5, False)["qkv"]
+    assert np.array_equal(a.reshape(T, -1, D)[:, :, perm], b.reshape(T, -1, D))
+
+
+def check_qk_norm_rope_brute_force(orc):
+    """Tiny heads against exact rational arithmetic (fp32 cache values taken
+    exactly, 60-digit sqrt): every output is the nearest-even bf16."""
+    rng = np.random.default_rng(27)
+    T, Hq, Hkv, D = 2, 1, 1, 8
+    for neox in (True, False):
+        qkv, qw, kw = _qk_case(rng, T, Hq, Hkv, D)
+        cache = (rng.random((4, D)) * 2 - 1).astype(np.float32)
+        pos = np.array([3, 1])
+        out = orc.qk_norm_rope(qkv, qw, kw, cache, pos, Hq, Hkv, D, 1e-4, neox)["qkv"]
+        for t in range(T):
+            for h in range(Hq + Hkv):
+                x = [F(float(v)) for v in exact.bf16_bits_to_f64(qkv[t, h * D:(h + 1) * D])]
+                w = [F(float(v)) for v in exact.bf16_bits_to_f64(qw if h < Hq else kw)]
+                inv = 1 / exact._sqrt(sum(v * v for v in x) / D + F(float(np.float32(1e-4))))
+                y = [x[j] * inv * w[j] for j in range(D)]
+                o = [None] * D
+                for i in range(D // 2):
+                    a, b = (i, i + D // 2) if neox else (2 * i, 2 * i + 1)
+                    c, sn = F(float(cache[pos[t], i])), F(float(cache[pos[t], D // 2 + i]))
+                    o[a] = y[a] * c - y[b] * sn
+                    o[b] = y[b] * c + y[a] * sn
+                assert list(out[t, h * D:(h + 1) * D]) == [exact.bf16_nearest_code(v) for v in o], \
+                    (neox, t, h)
+
+
 ALL_CHECKS = [
     check_e4m3_spec_points, check_e4m3_all_codes, check_e4m3_encoder_brute_force,
     check_e4m3_special_values, check_bf16_all_patterns, check_bf16_encoder_brute_force,
@@ -474,4 +562,5 @@ ALL_CHECKS = [
     check_per_group_layout, check_zero_row_and_saturation, check_silu_closed_forms,
     check_silu_brute_force, check_silu_modes, check_rms_norm_bf16_closed_forms,
     check_rms_norm_bf16_invariants, check_rms_norm_bf16_brute_force, check_norm_pad,
+    check_qk_norm_rope_rotations, check_qk_norm_rope_pairings, check_qk_norm_rope_brute_force,
 ]

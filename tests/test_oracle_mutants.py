@@ -58,6 +58,18 @@ MUTANTS = {
                                "uint16_t rb = orc_bf16_encode(orc_bf16_decode(xrow[j]));"),
     "pad_eps_dropped": ("double scale = 1.0 / sqrt(sq / (double)H + (double)eps);",
                         "double scale = 1.0 / sqrt(sq / (double)H);"),
+    "rope_sign": ("rot[a] = y[a] * c - y[b] * sn;", "rot[a] = y[a] * c + y[b] * sn;"),
+    "rope_cos_sin_swapped": ("double c = (double)cs[i], sn = (double)cs[D / 2 + i];",
+                             "double sn = (double)cs[i], c = (double)cs[D / 2 + i];"),
+    "rope_neox_pairs_adjacent": ("int64_t b = is_neox ? i + D / 2 : 2 * i + 1;",
+                                 "int64_t b = is_neox ? 2 * i + 1 : 2 * i + 1;\n"
+                                 "                a = is_neox ? 2 * i : a;"),
+    "qk_k_heads_use_q_weight": ("const uint16_t *w = h < Hq ? q_weight : k_weight;",
+                                "const uint16_t *w = q_weight;"),
+    "qk_position_ignored": ("const float *cs = cos_sin_cache + positions[t] * D;",
+                            "const float *cs = cos_sin_cache;"),
+    "qk_eps_dropped": ("double inv_rms = 1.0 / sqrt(sq / (double)D + (double)eps);",
+                       "double inv_rms = 1.0 / sqrt(sq / (double)D);"),
 }
 
 
