@@ -64,6 +64,7 @@ STEPS.update({name: (w,) for name, w in gen.NAMED.items()})
 STEPS.update({w.name: (w,) for w in gen.sweep()})
 STEPS.update({w.name: (w,) for w in gen.mla_workloads()})
 STEPS.update({w.name: (w,) for w in gen.pad_workloads()})
+STEPS.update({w.name: (w,) for w in gen.qk_workloads()})
 DEFAULT_STEP = "llama3_8b_decode"
 
 
@@ -217,6 +218,7 @@ KERNEL_SOURCES = {
     "silu": [_CSRC + f for f in ("silu_fp8.cu", "common.cuh", "tma.cuh", "vg_fused.cu")],
     "mla": [_CSRC + f for f in ("mla_norm.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
                                 "vg_fused.cu")],
+    "qk": [_CSRC + f for f in ("qk_norm_rope.cu", "row_norm.cuh", "common.cuh", "vg_fused.cu")],
 }
 
 
@@ -266,6 +268,11 @@ class DeviceSet:
                 q = torch.empty((w.T, w.n), dtype=torch.uint8, device=dev)
                 scale = self._scale(torch, w, dev)
                 self.ops.append(dict(w=w, q=q, res=res, scale=scale, x=x, weight=weights[w.name]))
+            elif w.op == "qk":
+                qkv = torch.from_numpy(h["qkv"].view(np.int16)).to(dev)
+                pos = torch.from_numpy(h["positions"]).to(dev)
+                qw, kw, cache = weights[w.name]
+                self.ops.append(dict(w=w, qkv=qkv, pos=pos, q_weight=qw, k_weight=kw, cache=cache))
             elif w.op == "pad":
                 x = torch.from_numpy(h["x"].view(np.int16)).to(dev)
                 res = torch.from_numpy(h["residual"].view(np.int16)).to(dev)
@@ -308,6 +315,10 @@ def device_weights(torch, step, host, dev):
         elif w.op == "mla":
             out[w.name] = tuple(torch.from_numpy(h[k].view(np.int16)).to(dev)
                                 for k in ("q_weight", "kv_weight"))
+        elif w.op == "qk":  # the weights and the cos/sin cache, model constants
+            out[w.name] = (torch.from_numpy(h["q_weight"].view(np.int16)).to(dev),
+                           torch.from_numpy(h["k_weight"].view(np.int16)).to(dev),
+                           torch.from_numpy(h["cos_sin_cache"]).to(dev))
     return out
 
 
@@ -318,6 +329,9 @@ def launch(vg, op):
                                      op["weight"], w.eps, w.mode, w.group_size)
     elif w.op == "pad":
         vg.vg_fused_add_rms_norm_pad(op["out"], op["res"], op["x"], op["res"], op["weight"], w.eps)
+    elif w.op == "qk":
+        vg.vg_fused_qk_norm_rope(op["qkv"], op["q_weight"], op["k_weight"], op["cache"], op["pos"],
+                                 w.hq, w.hkv, w.n, w.eps, w.mode == 1)
     elif w.op == "mla":
         if w.mode == gen.PER_TOKEN:
             vg.vg_fused_mla_dual_rms_norm_per_token_quant(op["q"], op["scale"], op["kv"], op["q_c"],
@@ -470,6 +484,8 @@ def select_step(args):
 
 
 def mode_name(w):
+    if w.op == "qk":
+        return "neox" if w.mode == 1 else "gptj"
     if w.op == "pad":
         return f"bf16_padded_to_{w.n2}"
     if w.op == "mla":
@@ -483,6 +499,8 @@ def describe(w):
          "bytes": w.algorithmic_bytes()}
     if w.op in ("mla", "pad"):
         d["n2"] = w.n2
+    if w.op == "qk":
+        d.update(q_heads=w.hq, kv_heads=w.hkv, max_pos=w.max_pos)
     return d
 
 
@@ -643,6 +661,11 @@ def oracle_step_runner(step, host, threads):
                     futs.append(pool.submit(orc.fused_add_rms_norm_fp8, h["x"][r0:r1],
                                             h["residual"][r0:r1], h["weight"], w.eps, w.mode,
                                             w.group_size, w.static_scale, False))
+                elif w.op == "qk":
+                    futs.append(pool.submit(orc.qk_norm_rope, h["qkv"][r0:r1], h["q_weight"],
+                                            h["k_weight"], h["cos_sin_cache"],
+                                            h["positions"][r0:r1], w.hq, w.hkv, w.n, w.eps,
+                                            w.mode == 1, False))
                 elif w.op == "pad":
                     futs.append(pool.submit(orc.fused_add_rms_norm_pad, h["x"][r0:r1],
                                             h["residual"][r0:r1], h["weight"], w.eps, w.n2, False))
@@ -763,7 +786,8 @@ def run_sweep(args):
     peak, peak_kind = measured_peak()
     stream = torch.cuda.Stream(device=dev)
     cache = {}
-    for w in list(gen.NAMED.values()) + gen.sweep() + gen.mla_workloads() + gen.pad_workloads():
+    for w in (list(gen.NAMED.values()) + gen.sweep() + gen.mla_workloads() + gen.pad_workloads()
+              + gen.qk_workloads()):
         key = (w.op, w.T, w.n, w.n2, w.x_dist)
         if key not in cache:
             cache.clear()

@@ -24,6 +24,7 @@ import torch
 
 TENSOR_X, TENSOR_RESIDUAL, TENSOR_WEIGHT, TENSOR_GATE_UP = 1, 2, 3, 4
 TENSOR_Q_C, TENSOR_KV_C, TENSOR_Q_WEIGHT, TENSOR_KV_WEIGHT = 5, 6, 7, 8
+TENSOR_QKV, TENSOR_POSITIONS = 9, 10
 _ROW_BLOCK = 64
 
 STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
@@ -101,17 +102,42 @@ def mla_inputs(T: int, q_dim: int, kv_dim: int, seed: int = 0):
     }
 
 
+def rope_cache(max_pos: int, head_dim: int, theta: float = 1.0e6) -> np.ndarray:
+    """The rotary embedding's cos/sin table, a model constant the op reads:
+    row p = [cos(p f_0), ..., cos(p f_{D/2-1}), sin(p f_0), ...] with
+    f_i = theta^(-2i/D), computed in fp64 and stored as fp32."""
+    f = theta ** (-np.arange(0, head_dim, 2, dtype=np.float64) / head_dim)
+    ang = np.outer(np.arange(max_pos, dtype=np.float64), f)
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def qk_inputs(T: int, hq: int, hkv: int, head_dim: int, max_pos: int, seed: int = 0):
+    """qkv [T, (hq + 2 hkv) * D] bf16 bits, q/k weights [D], positions int64
+    [T] uniform in [0, max_pos), and the cos/sin cache [max_pos, D]."""
+    rng = _rng(seed, TENSOR_POSITIONS, 0)
+    return {
+        "qkv": bf16_tensor("normal", seed, TENSOR_QKV, T, (hq + 2 * hkv) * head_dim),
+        "q_weight": bf16_tensor("weight", seed, TENSOR_Q_WEIGHT, 1, head_dim).reshape(head_dim),
+        "k_weight": bf16_tensor("weight", seed, TENSOR_KV_WEIGHT, 1, head_dim).reshape(head_dim),
+        "positions": rng.integers(0, max_pos, T).astype(np.int64),
+        "cos_sin_cache": rope_cache(max_pos, head_dim),
+    }
+
+
 # ----------------------------------------------------------------- workloads
 
 @dataclass(frozen=True)
 class Workload:
     """One op invocation: which op, its shape, scale mode and inputs."""
     name: str
-    op: str                  # "norm", "silu", "mla" or "pad"
+    op: str                  # "norm", "silu", "mla", "pad" or "qk"
     T: int
     n: int                   # hidden (norm), intermediate (silu) or q_dim (mla)
     mode: int                # mla: PER_TOKEN = q to fp8, STATIC = bf16 q
     n2: int = 0              # mla: kv_dim; pad: padded row length
+    hq: int = 0              # qk: query heads (n = head_dim, mode 1 = neox, 0 = gptj)
+    hkv: int = 0             # qk: key/value heads
+    max_pos: int = 0         # qk: rows of the cos/sin cache
     group_size: int = 128
     eps: float = 1e-5
     static_scale: float = 0.05
@@ -125,6 +151,8 @@ class Workload:
             return norm_inputs(self.T, self.n, self.seed, self.x_dist)
         if self.op == "mla":
             return mla_inputs(self.T, self.n, self.n2, self.seed)
+        if self.op == "qk":
+            return qk_inputs(self.T, self.hq, self.hkv, self.n, self.max_pos, self.seed)
         return silu_inputs(self.T, self.n, self.seed)
 
     def algorithmic_bytes(self) -> int:
@@ -135,6 +163,8 @@ class Workload:
         if self.op == "norm":
             per_row = (7 if self.residual else 3) * self.n + s_row
             return self.T * per_row + 2 * self.n + s0
+        if self.op == "qk":  # Q and K heads read and written; each token's cos/sin row and position
+            return self.T * ((self.hq + self.hkv) * self.n * 4 + self.n * 4 + 8) + 2 * 2 * self.n
         if self.op == "pad":  # x, residual read; residual_out and the padded row written
             return self.T * (6 * self.n + 2 * self.n2) + 2 * self.n
         if self.op == "mla":  # both rows read; q out as fp8 + scale or bf16; kv out bf16
@@ -167,6 +197,18 @@ PAD_T = (1, 64, 512, 4096, 32768)
 def pad_workloads():
     return [Workload(f"norm_pad_{T}x{PAD_HIDDEN}_{PAD_PADDED}", "pad", T, PAD_HIDDEN, PER_TOKEN,
                      n2=PAD_PADDED, eps=1e-6) for T in PAD_T]
+
+
+# Per-head QK RMSNorm + RoPE at Qwen3-8B's attention shape: 32 query heads,
+# 8 key/value heads, head_dim 128, rope theta 1e6, positions in [0, 32768).
+QK_HQ, QK_HKV, QK_D, QK_MAX_POS = 32, 8, 128, 32768
+QK_T = (1, 64, 512, 4096, 32768)
+
+
+def qk_workloads():
+    return [Workload(f"qk_norm_rope_{'neox' if m else 'gptj'}_{T}x{QK_HQ}q{QK_HKV}kv{QK_D}", "qk", T,
+                     QK_D, m, hq=QK_HQ, hkv=QK_HKV, max_pos=QK_MAX_POS, eps=1e-6)
+            for m in (1, 0) for T in QK_T]
 
 
 # The MLA dual norm at DeepSeek-V3's latent sizes (q_lora_rank 1536,

@@ -16,7 +16,8 @@
  *   attention in one kernel, and its per-token-quant variant (q to FP8 with
  *   a per-token scale, kv in bf16).  Section "RMSNorm + Padding
  *   (fuse_act_padding)": residual add + RMSNorm written into a padded bf16
- *   row.
+ *   row.  Section "QK Norm + RoPE (enable_qk_norm_rope_fusion)": per-head
+ *   RMSNorm of Q and K, then the rotary embedding, in place on qkv.
  *
  * Numerics (the pages give no formulas; these are the readings the library
  * implements):
@@ -29,7 +30,8 @@
  *         per-group: fp32(max(amax over G columns, 1e-10f) / 448)
  *   The kernels multiply by 1/s, computed once per row or group.
  *   A norm with a bf16 output (the MLA dual norm, the padded norm) rounds y
- *   once, to nearest even bf16, as the exact value would round.
+ *   once, to nearest even bf16, as the exact value would round (the QK
+ *   norm + RoPE: see its entry point).
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers owned by the caller.  The
@@ -190,6 +192,36 @@ vg_status vg_fused_mla_dual_rms_norm_per_token_quant(
     vg_stream_t stream);
 
 /*
+ * Per-head QK RMSNorm + rotary embedding, in place ("QK Norm + RoPE
+ * (enable_qk_norm_rope_fusion)").  For every token t and every Q head
+ * (weight q_weight) and K head (weight k_weight):
+ *   y_j = x_j / sqrt(mean(x^2) + eps) * w_j                 over the head's D columns
+ *   o_a = y_a c_i - y_b s_i,  o_b = y_b c_i + y_a s_i       i < D/2
+ * with c_i = cos_sin_cache[pos_t, i], s_i = cos_sin_cache[pos_t, D/2 + i]
+ * and the pairs (a, b) = (i, i + D/2) when is_neox, else (2i, 2i + 1); the
+ * head is overwritten with bf16(o), rounded once from an fp32 value within
+ * ~2^-20 (relative) of the exact o: so each output is the correctly rounded
+ * bf16, or one ulp from it where the exact o lies within ~2^-20 of a bf16
+ * rounding midpoint.  V heads are not touched.
+ *
+ *   qkv            in/out uint16 [T, (Hq + 2 Hkv) * D] bf16: Q heads, then K
+ *                  heads, then V heads, D contiguous columns each
+ *   q_weight, k_weight  in uint16 [D] bf16 (NULL allowed for zero heads)
+ *   cos_sin_cache  in fp32 [max_position, D]: cos in columns [0, D/2), sin
+ *                  in [D/2, D)
+ *   positions      in int64 [T] (8-byte aligned).  A position outside
+ *                  [0, max_position) leaves that token's heads unchanged and
+ *                  sets VG_DEVICE_BAD_POSITION (vg_device_status).
+ *   num_q_heads Hq >= 0, num_kv_heads Hkv >= 0, Hq + Hkv >= 1,
+ *   Hq + 2 Hkv <= 4096; head_dim D in {64, 128, 256}; max_position >= 1
+ */
+vg_status vg_fused_qk_norm_rope(uint16_t *qkv, const uint16_t *q_weight, const uint16_t *k_weight,
+                                const float *cos_sin_cache, const int64_t *positions,
+                                int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int64_t max_position, float eps, int32_t is_neox,
+                                vg_stream_t stream);
+
+/*
  * Device-side status of the library's kernels on the current device (no
  * counterpart on the pages; the pipelined kernels' own failure report).
  * Every wait in the library's kernels is bounded; a wait that gives up sets
@@ -201,6 +233,7 @@ vg_status vg_fused_mla_dual_rms_norm_per_token_quant(
  * VG_OK.
  */
 #define VG_DEVICE_WAIT_TIMEOUT 1u
+#define VG_DEVICE_BAD_POSITION 2u /* vg_fused_qk_norm_rope: a position out of range */
 vg_status vg_device_status(uint32_t *flags, int32_t reset);
 
 /* Static English text for a status code (never NULL). */

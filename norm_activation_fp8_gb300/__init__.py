@@ -12,6 +12,8 @@ Entry points (same names and argument order as the C ABI):
                             eps, mode, group_size=128, stream=None)
   vg_silu_mul_fp8(q, scale, gate_up, mode, group_size=128, stream=None)
   vg_fused_add_rms_norm_pad(out, residual_out, x, residual, weight, eps, stream=None)
+  vg_fused_qk_norm_rope(qkv, q_weight, k_weight, cos_sin_cache, positions,
+                        num_q_heads, num_kv_heads, head_dim, eps, is_neox=True, stream=None)
   vg_fused_mla_dual_rms_norm(q_out, kv_out, q_c, q_weight, kv_c, kv_weight,
                              eps_q, eps_kv, stream=None)
   vg_fused_mla_dual_rms_norm_per_token_quant(q_fp8, q_scale, kv_out, q_c,
@@ -40,10 +42,11 @@ STATUS_NAMES = {
 }
 
 EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_fused_add_rms_norm_pad",
-                    "vg_fused_mla_dual_rms_norm",
+                    "vg_fused_mla_dual_rms_norm", "vg_fused_qk_norm_rope",
                     "vg_fused_mla_dual_rms_norm_per_token_quant", "vg_device_status",
                     "vg_status_string", "vg_abi_version")
 DEVICE_WAIT_TIMEOUT = 1
+DEVICE_BAD_POSITION = 2
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +80,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.vg_silu_mul_fp8.restype = ctypes.c_int
         f32 = ctypes.c_float
         lib.vg_fused_add_rms_norm_pad.argtypes = [P, P, P, P, P, i64, i64, i64, f32, P]
+        lib.vg_fused_qk_norm_rope.argtypes = [P, P, P, P, P, i64, i32, i32, i32, i64, f32, i32, P]
+        lib.vg_fused_qk_norm_rope.restype = ctypes.c_int
         lib.vg_fused_add_rms_norm_pad.restype = ctypes.c_int
         lib.vg_fused_mla_dual_rms_norm.argtypes = [P, P, P, i64, P, P, i64, P, i64, i64, i64,
                                                    f32, f32, P]
@@ -198,6 +203,23 @@ def vg_fused_add_rms_norm_pad(out, residual_out, x, residual, weight, eps: float
         _ptr(out, bf16, "out"), _ptr(residual_out, bf16, "residual_out"), _ptr(x, bf16, "x"),
         _ptr(residual, bf16, "residual"), _ptr(weight, bf16, "weight"), num_tokens, hidden,
         padded_hidden, ctypes.c_float(eps), _stream(stream)))
+
+
+def vg_fused_qk_norm_rope(qkv, q_weight, k_weight, cos_sin_cache, positions, num_q_heads: int,
+                          num_kv_heads: int, head_dim: int, eps: float, is_neox: bool = True,
+                          stream=None):
+    """Per-head QK RMSNorm + rotary embedding, in place on qkv
+    [T, (Hq + 2 Hkv) * D] bf16; cos_sin_cache fp32 [max_pos, D]; positions
+    int64 [T]."""
+    import torch
+    bf16, _, f32 = _dtypes()
+    T = _rows(qkv, "qkv")[0]
+    max_pos = _rows(cos_sin_cache, "cos_sin_cache")[0]
+    _check(load().vg_fused_qk_norm_rope(
+        _ptr(qkv, bf16, "qkv"), _ptr(q_weight, bf16, "q_weight"), _ptr(k_weight, bf16, "k_weight"),
+        _ptr(cos_sin_cache, f32, "cos_sin_cache"), _ptr(positions, (torch.int64,), "positions"),
+        T, num_q_heads, num_kv_heads, head_dim, max_pos, ctypes.c_float(eps),
+        1 if is_neox else 0, _stream(stream)))
 
 
 def _rows_ptr(t, name):

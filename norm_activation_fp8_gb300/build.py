@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB_NAME = "libvg_fused.so"
 LIB_PATH = os.path.join(BUILD, LIB_NAME)
 
-SOURCES = ["vg_fused.cu", "norm_fp8.cu", "silu_fp8.cu", "mla_norm.cu"]
+SOURCES = ["vg_fused.cu", "norm_fp8.cu", "silu_fp8.cu", "mla_norm.cu", "qk_norm_rope.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I", INCLUDE, "-I", CSRC]

@@ -135,4 +135,23 @@ struct MlaPlan {
 MlaPlan plan_mla(int64_t T, int nq, int nkv, int sms);
 cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaStream_t s);
 
+// QK norm + RoPE, in place on qkv [T, row] with row = (hq + 2 hkv) * D.
+struct QkArgs {
+  uint16_t *qkv;
+  const uint16_t *qw;
+  const uint16_t *kw;
+  const float *cache;    // [max_pos, D]: cos | sin
+  const int64_t *pos;    // [T]
+  int64_t T;
+  int64_t row;           // elements per token row
+  int64_t max_pos;
+  int32_t nh;            // heads normalised: hq + hkv
+  int32_t hq;
+  float eps;
+};
+// Device status bit of the rope kernel: a position outside [0, max_pos).
+constexpr uint32_t kErrBadPosition = 2u;
+cudaError_t launch_qk_norm_rope(const QkArgs &a, int head_dim, bool neox, cudaStream_t s);
+uint32_t read_rope_status(bool reset);
+
 }  // namespace vg

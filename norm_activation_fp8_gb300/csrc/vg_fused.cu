@@ -358,6 +358,44 @@ vg_status vg_fused_add_rms_norm_pad(uint16_t *out, uint16_t *residual_out, const
              : VG_ERR_CUDA;
 }
 
+vg_status vg_fused_qk_norm_rope(uint16_t *qkv, const uint16_t *q_weight, const uint16_t *k_weight,
+                                const float *cos_sin_cache, const int64_t *positions,
+                                int64_t num_tokens, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int64_t max_position, float eps, int32_t is_neox,
+                                vg_stream_t stream) {
+  if (num_tokens < 0 || num_tokens > INT32_MAX || num_q_heads < 0 || num_kv_heads < 0 ||
+      num_q_heads + num_kv_heads < 1 || num_q_heads + 2LL * num_kv_heads > 4096 ||
+      (head_dim != 64 && head_dim != 128 && head_dim != 256) || max_position < 1)
+    return VG_ERR_BAD_SHAPE;
+  if (num_tokens == 0) return VG_OK;
+  if (!qkv || !cos_sin_cache || !positions || (num_q_heads > 0 && !q_weight) ||
+      (num_kv_heads > 0 && !k_weight))
+    return VG_ERR_NULL_PTR;
+  if (vg::misaligned(qkv, 16) || vg::misaligned(q_weight, 16) || vg::misaligned(k_weight, 16) ||
+      vg::misaligned(cos_sin_cache, 16) || vg::misaligned(positions, 8))
+    return VG_ERR_MISALIGNED;
+  int sms = 0;
+  vg_status st = vg::check_device(&sms);
+  if (st != VG_OK) return st;
+  vg::clear_stale_error();
+
+  vg::QkArgs a{};
+  a.qkv = qkv;
+  a.qw = q_weight;
+  a.kw = k_weight;
+  a.cache = cos_sin_cache;
+  a.pos = positions;
+  a.T = num_tokens;
+  a.row = (int64_t)(num_q_heads + 2 * num_kv_heads) * head_dim;
+  a.max_pos = max_position;
+  a.nh = num_q_heads + num_kv_heads;
+  a.hq = num_q_heads;
+  a.eps = eps;
+  return vg::launch_qk_norm_rope(a, head_dim, is_neox != 0, (cudaStream_t)stream) == cudaSuccess
+             ? VG_OK
+             : VG_ERR_CUDA;
+}
+
 vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int64_t num_tokens,
                           int64_t inter, int32_t mode, int32_t group_size, vg_stream_t stream) {
   vg_status st = vg::check_row(num_tokens, inter, mode, group_size);
@@ -389,9 +427,10 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
 
 vg_status vg_device_status(uint32_t *flags, int32_t reset) {
   if (!flags) return VG_ERR_NULL_PTR;
-  const uint32_t v = vg::read_norm_status(reset != 0), w = vg::read_silu_status(reset != 0);
-  if (v == 0xFFFFFFFFu || w == 0xFFFFFFFFu) return VG_ERR_CUDA;
-  *flags = v | w;
+  const uint32_t v = vg::read_norm_status(reset != 0), w = vg::read_silu_status(reset != 0),
+                 r = vg::read_rope_status(reset != 0);
+  if (v == 0xFFFFFFFFu || w == 0xFFFFFFFFu || r == 0xFFFFFFFFu) return VG_ERR_CUDA;
+  *flags = v | w | r;
   return VG_OK;
 }
 

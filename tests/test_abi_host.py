@@ -39,7 +39,7 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     assert {"vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8"} <= names
     assert {"vg_fused_mla_dual_rms_norm", "vg_fused_mla_dual_rms_norm_per_token_quant",
-            "vg_fused_add_rms_norm_pad"} <= names
+            "vg_fused_add_rms_norm_pad", "vg_fused_qk_norm_rope"} <= names
     assert names == set(vg.EXPORTED_SYMBOLS)
 
 
@@ -198,3 +198,24 @@ def test_pad_validation(lib):
     assert pad(lib, out=None, r_out=None, x=None, res=None, w=None, T=0) == OK
     for k in ("out", "r_out", "x", "res", "w"):
         assert pad(lib, **{k: A + 8}) == ALIGN, k
+
+
+def qk(lib, qkv=A, qw=A, kw=A, cache=A, pos=A, T=4, hq=32, hkv=8, D=128, maxp=4096, neox=1):
+    return lib.vg_fused_qk_norm_rope(qkv, qw, kw, cache, pos, T, hq, hkv, D, maxp,
+                                     ctypes.c_float(1e-6), neox, None)
+
+
+def test_qk_validation(lib):
+    for D in (0, 32, 96, 512):
+        assert qk(lib, D=D) == SHAPE, D
+    assert qk(lib, hq=0, hkv=0) == SHAPE
+    assert qk(lib, hq=-1) == SHAPE
+    assert qk(lib, hq=4000, hkv=100) == SHAPE   # more than 4096 heads in a row
+    assert qk(lib, maxp=0) == SHAPE
+    assert qk(lib, T=-1) == SHAPE
+    for k in ("qkv", "qw", "kw", "cache", "pos"):
+        assert qk(lib, **{k: None}) == NULL, k
+    assert qk(lib, qkv=None, qw=None, kw=None, cache=None, pos=None, T=0) == OK
+    for k in ("qkv", "qw", "kw", "cache"):
+        assert qk(lib, **{k: A + 8}) == ALIGN, k
+    assert qk(lib, pos=A + 4) == ALIGN

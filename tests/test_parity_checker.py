@@ -86,3 +86,28 @@ def test_residual_bit_exact():
     b[3] ^= 1
     with pytest.raises(parity.ParityError):
         parity.compare_exact(b, a, "residual_out")
+
+
+def test_bf16_checker_accepts_near_midpoint_flips_only():
+    import exact as ex
+    o = np.full(3000, 0x3F80, np.uint16)                    # 1.0 ...
+    o[1], o[2] = 0x3F81, 0xBF80                             # 1.0078125, -1.0
+    mid = (1.0 + 1.0078125) / 2
+    v = np.ones(3000)
+    v[0], v[1], v[2] = mid * (1 - 2.0 ** -21), 1.0078125, -1.0
+    g = o.copy()
+    g[0] = 0x3F81                                           # one ulp, v near the midpoint: allowed
+    assert parity.compare_bf16(g, o, v)["flips"] == 1
+    v_far = v.copy()
+    v_far[0] = 1.001                                        # far from the midpoint: rejected
+    with pytest.raises(parity.ParityError):
+        parity.compare_bf16(g, o, v_far)
+    g2 = o.copy()
+    g2[0] = 0x3F82                                          # two ulps: rejected
+    with pytest.raises(parity.ParityError):
+        parity.compare_bf16(g2, o, v)
+    g3 = o.copy()
+    g3[2] = 0xBF81                                          # sign kept, v not near: rejected
+    with pytest.raises(parity.ParityError):
+        parity.compare_bf16(g3, o, v)
+    assert ex.bf16_bits_to_f64(np.array([0x3F81], np.uint16))[0] == 1.0078125
