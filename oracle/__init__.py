@@ -23,6 +23,9 @@ Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
   mla_dual_rms_norm ......... the two pinned norms above, side by side
   fused_add_rms_norm_pad .... pinned (zero tail, bf16 rms_norm on the
                               stored residual, library bf16 add)
+  per-group UE8M0 / column-major scales ... pinned (powers of two that
+                              bracket amax/448, exact rationals, the
+                              transposed layout of the row-major scales)
   qk_norm_rope .............. pinned (identity and quarter-turn rotations
                               against the pinned bf16 rms_norm, V untouched,
                               neox/gptj by permutation, exact rationals)
@@ -38,6 +41,7 @@ import threading
 import numpy as np
 
 STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
+UE8M0, COL_MAJOR = 0x100, 0x200  # per-group options, or-ed into the mode
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -267,6 +271,12 @@ def _u16(a) -> np.ndarray:
 
 
 def _scale_buffer(mode: int, rows: int, n: int, group_size: int, scale):
+    if mode & COL_MAJOR and mode & 0xFF == PER_GROUP:
+        if group_size <= 0 or n % group_size:
+            raise ValueError("per-group mode needs a group size dividing the row")
+        # [n/G, T4]; the padding columns keep this sentinel (never written)
+        return np.full((n // group_size, (rows + 3) // 4 * 4), -1.0, np.float32)
+    mode &= 0xFF
     if mode == STATIC:
         if scale is None:
             raise ValueError("static mode needs the fp32 scale")

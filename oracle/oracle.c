@@ -46,6 +46,13 @@
  *    (it only keeps an all-zero row or group away from 0/0).
  *  - Per-group scales cover G contiguous columns; the scale tensor is
  *    [T, n/G] fp32, row-major.
+ *  - The per-group options that the GEMM side on sm100 wants (the "Support
+ *    Matrix" ties per-group FP8 there to DeepGEMM; the formats come from
+ *    the OCP Microscaling spec, E8M0): UE8M0 scales are the smallest power
+ *    of two >= max(amax, A_MIN) / 448 (an exponent with no mantissa), and
+ *    the column-major layout stores scale (t, g) at [g, t] of a [n/G, T4]
+ *    tensor, T4 = T rounded up to a multiple of 4 (16-byte rows); the
+ *    padding columns are not written.
  *  - silu(g) = g / (1 + exp(-g)); the gate is columns [0, I) and the up
  *    projection columns [I, 2I) of one [T, 2I] row.
  *  - A norm whose output stays in the activation dtype (the MLA dual
@@ -63,6 +70,9 @@
 #include <string.h>
 
 enum { ORC_STATIC = 0, ORC_PER_TOKEN = 1, ORC_PER_GROUP = 2 };
+/* Per-group options, or-ed into the mode: power-of-two (UE8M0) scales and a
+ * column-major scale layout. */
+enum { ORC_UE8M0 = 0x100, ORC_COL_MAJOR = 0x200 };
 
 #define ORC_E4M3_MAX 448.0
 
@@ -173,16 +183,33 @@ static float dynamic_scale(double amax)
     return (float)(a / ORC_E4M3_MAX);
 }
 
+/* UE8M0 scale: the smallest power of two s with s >= max(amax, A_MIN)/448,
+ * decided by exact comparisons with 448 * 2^e. */
+static double ue8m0_scale(double amax)
+{
+    const double a = fmax(amax, orc_amax_floor());
+    int e;
+    frexp(a / ORC_E4M3_MAX, &e);
+    while (ldexp(ORC_E4M3_MAX, e) < a)
+        ++e;
+    while (ldexp(ORC_E4M3_MAX, e - 1) >= a)
+        --e;
+    return ldexp(1.0, e);
+}
+
 /* quant_fp8 of one row y[0..n) ([FUS] "RMSNorm + Quantization": static
  * per-tensor, dynamic per-token, dynamic per-token-group).
  *   STATIC    : s = scale[0] (input)
  *   PER_TOKEN : s = fp32(max(amax_j |y_j|, A_MIN) / 448), written to scale[t]
  *   PER_GROUP : same over columns [g*G, (g+1)*G), written to scale[t*n/G + g]
+ *               (UE8M0: the power-of-two scale; COL_MAJOR: scale[g*T4 + t])
  * then v_j = y_j / s (fp64, with the stored fp32 s) and q_j = e4m3(v_j).
- * v (optional) receives v_j for the tolerance checker. */
+ * v (optional) receives v_j for the tolerance checker.  T: rows in all. */
 static void quantize_row(uint8_t *q, double *v, float *scale, const double *y,
-                         int64_t t, int64_t n, int mode, int64_t G)
+                         int64_t t, int64_t T, int64_t n, int mode, int64_t G)
 {
+    const int flags = mode & ~0xFF;
+    mode &= 0xFF;
     if (mode == ORC_STATIC) {
         double s = (double)scale[0];
         for (int64_t j = 0; j < n; ++j) {
@@ -201,8 +228,11 @@ static void quantize_row(uint8_t *q, double *v, float *scale, const double *y,
         for (int64_t j = 0; j < width; ++j)
             if (fabs(yg[j]) > amax)
                 amax = fabs(yg[j]);
-        float s32 = dynamic_scale(amax);
-        scale[t * ngroups + g] = s32;
+        float s32 = (flags & ORC_UE8M0) ? (float)ue8m0_scale(amax) : dynamic_scale(amax);
+        if (flags & ORC_COL_MAJOR)
+            scale[g * ((T + 3) / 4 * 4) + t] = s32;
+        else
+            scale[t * ngroups + g] = s32;
         double s = (double)s32;
         for (int64_t j = 0; j < width; ++j) {
             double vj = yg[j] / s;
@@ -215,7 +245,11 @@ static void quantize_row(uint8_t *q, double *v, float *scale, const double *y,
 
 static int check_mode(int mode, int64_t n, int64_t G)
 {
-    if (mode == ORC_STATIC || mode == ORC_PER_TOKEN)
+    const int flags = mode & ~0xFF;
+    if (flags & ~(ORC_UE8M0 | ORC_COL_MAJOR))
+        return -1;
+    mode &= 0xFF;
+    if ((mode == ORC_STATIC || mode == ORC_PER_TOKEN) && flags == 0)
         return 0;
     if (mode == ORC_PER_GROUP && G > 0 && n % G == 0)
         return 0;
@@ -270,7 +304,7 @@ int orc_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *scale,
         double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
         for (int64_t j = 0; j < H; ++j)
             y[j] = r[j] * inv * orc_bf16_decode(weight[j]);
-        quantize_row(q + t * H, v ? v + t * H : NULL, scale, y, t, H, mode, G);
+        quantize_row(q + t * H, v ? v + t * H : NULL, scale, y, t, T, H, mode, G);
     }
     free(r);
     free(y);
@@ -438,7 +472,7 @@ int orc_silu_mul_fp8(uint8_t *q, float *scale, double *v,
             double u = orc_bf16_decode(row[I + j]);
             a[j] = g / (1.0 + exp(-g)) * u;
         }
-        quantize_row(q + t * I, v ? v + t * I : NULL, scale, a, t, I, mode, G);
+        quantize_row(q + t * I, v ? v + t * I : NULL, scale, a, t, T, I, mode, G);
     }
     free(a);
     return 0;

@@ -138,9 +138,21 @@ def _exp(x: F) -> F:
         return F(d.exp())
 
 
-def exact_quantize(y: list[F], mode: int, group: int, static_scale, amax_floor: float):
+def pow2_at_least(x: F) -> F:
+    """The smallest power of two >= x > 0, by exact comparison."""
+    k = int(np.floor(np.log2(float(x))))
+    while F(2) ** k < x:
+        k += 1
+    while F(2) ** (k - 1) >= x:
+        k -= 1
+    return F(2) ** k
+
+
+def exact_quantize(y: list[F], mode: int, group: int, static_scale, amax_floor: float,
+                   ue8m0: bool = False):
     """Scales and (v, code) pairs of one row, every step exact except the
-    fp32 rounding of a dynamic scale, which is exact RNE."""
+    fp32 rounding of a dynamic scale, which is exact RNE (with ``ue8m0`` the
+    scale is the smallest power of two >= amax/448 instead)."""
     n = len(y)
     if mode == 0:
         s_list = [np.float32(static_scale)]
@@ -151,7 +163,8 @@ def exact_quantize(y: list[F], mode: int, group: int, static_scale, amax_floor: 
         for g in range(n // width):
             amax = max(abs(t) for t in y[g * width:(g + 1) * width])
             amax = max(amax, F(amax_floor))
-            s_list.append(fp32_nearest(amax / 448))
+            s_list.append(np.float32(float(pow2_at_least(amax / 448))) if ue8m0
+                          else fp32_nearest(amax / 448))
     v, codes = [], []
     for j, yj in enumerate(y):
         s = F(float(s_list[0 if mode == 0 else j // width]))
@@ -162,7 +175,7 @@ def exact_quantize(y: list[F], mode: int, group: int, static_scale, amax_floor: 
 
 
 def exact_norm_row(x_bits, res_bits, w_bits, eps: float, mode: int, group: int,
-                   static_scale, amax_floor: float):
+                   static_scale, amax_floor: float, ue8m0: bool = False):
     xs = [F(float(t)) for t in bf16_bits_to_f64(x_bits)]
     ws = [F(float(t)) for t in bf16_bits_to_f64(w_bits)]
     if res_bits is None:
@@ -176,14 +189,15 @@ def exact_norm_row(x_bits, res_bits, w_bits, eps: float, mode: int, group: int,
     ms = sum(t * t for t in r) / H
     inv = 1 / _sqrt(ms + F(float(np.float32(eps))))
     y = [rj * inv * wj for rj, wj in zip(r, ws)]
-    s, v, codes = exact_quantize(y, mode, group, static_scale, amax_floor)
+    s, v, codes = exact_quantize(y, mode, group, static_scale, amax_floor, ue8m0)
     return {"residual_out": r_codes, "y": y, "scale": s, "v": v, "q": codes}
 
 
-def exact_silu_row(gu_bits, mode: int, group: int, static_scale, amax_floor: float):
+def exact_silu_row(gu_bits, mode: int, group: int, static_scale, amax_floor: float,
+                   ue8m0: bool = False):
     vals = [F(float(t)) for t in bf16_bits_to_f64(gu_bits)]
     n = len(vals) // 2
     y = [vals[j] / (1 + _exp(-vals[j])) * vals[n + j] for j in range(n)]
-    s, v, codes = exact_quantize(y, mode, group, static_scale, amax_floor)
+    s, v, codes = exact_quantize(y, mode, group, static_scale, amax_floor, ue8m0)
     return {"y": y, "scale": s, "v": v, "q": codes}
 

@@ -432,6 +432,58 @@ def check_rms_norm_bf16_brute_force(orc):
             np.testing.assert_allclose(out["y"][t], [float(v) for v in ex["y"]], rtol=1e-13)
 
 
+# ------------------------------------- UE8M0 / column-major group scales
+
+UE8M0, COL_MAJOR = 0x100, 0x200
+
+
+def check_group_scale_options(orc):
+    """UE8M0 scales are the powers of two that bracket each group's amax/448
+    (exact rationals on tiny rows, codes included, both ops); the
+    column-major layout holds the row-major scales transposed, T padded to a
+    multiple of 4 with the padding left alone; the options need per-group."""
+    rng = np.random.default_rng(28)
+    floor = orc.amax_floor()
+    T, H, G = 3, 16, 8
+    x = _rand_bf16(rng, (T, H), scale=np.exp2(rng.integers(-5, 5, (T, H))))
+    w = _weight(rng, H)
+    out = orc.fused_add_rms_norm_fp8(x, None, w, 1e-5, PER_GROUP | UE8M0, G)
+    for t in range(T):
+        ex = exact.exact_norm_row(x[t], None, w, 1e-5, PER_GROUP, G, None, floor, ue8m0=True)
+        assert np.array_equal(out["scale"][t], ex["scale"]), t
+        assert list(out["q"][t]) == ex["q"], t
+    s = out["scale"].astype(np.float64)
+    assert np.all(np.exp2(np.round(np.log2(s))) == s)          # powers of two
+    gu = _rand_bf16(rng, (T, 2 * H), scale=3.0)
+    sout = orc.silu_mul_fp8(gu, PER_GROUP | UE8M0, G)
+    for t in range(T):
+        ex = exact.exact_silu_row(gu[t], PER_GROUP, G, None, floor, ue8m0=True)
+        assert np.array_equal(sout["scale"][t], ex["scale"]) and list(sout["q"][t]) == ex["q"], t
+    # layout: a larger T so that the padding is visible (T4 = 8 for T = 5)
+    T = 5
+    d = _rand_bf16(rng, (T, 256))
+    w = _weight(rng, 256)
+    for extra in (0, UE8M0):
+        row = orc.fused_add_rms_norm_fp8(d, None, w, 1e-5, PER_GROUP | extra, 64)
+        col = orc.fused_add_rms_norm_fp8(d, None, w, 1e-5, PER_GROUP | extra | COL_MAJOR, 64)
+        assert col["scale"].shape == (4, 8)
+        assert np.array_equal(col["scale"][:, :T], row["scale"].T)
+        assert np.all(col["scale"][:, T:] == -1.0)              # padding not written
+        assert np.array_equal(col["q"], row["q"])
+    # an all-zero group: the floored amax, so the power of two at A_MIN/448
+    z = d.copy()
+    z[1, :64] = 0
+    zo = orc.fused_add_rms_norm_fp8(z, None, w, 1e-5, PER_GROUP | UE8M0, 64)
+    assert zo["scale"][1, 0] == np.float32(float(exact.pow2_at_least(F(floor) / 448)))
+    assert np.all(zo["q"][1, :64] == 0)
+    for bad in (STATIC | UE8M0, PER_TOKEN | COL_MAJOR, PER_GROUP | 0x400):
+        try:
+            orc.fused_add_rms_norm_fp8(d, None, w, 1e-5, bad, 64, scale=1.0)
+        except ValueError:
+            continue
+        raise AssertionError(f"mode {bad:#x} accepted")
+
+
 # ----------------------------------------------------- act padding
 
 
@@ -563,4 +615,5 @@ ALL_CHECKS = [
     check_silu_brute_force, check_silu_modes, check_rms_norm_bf16_closed_forms,
     check_rms_norm_bf16_invariants, check_rms_norm_bf16_brute_force, check_norm_pad,
     check_qk_norm_rope_rotations, check_qk_norm_rope_pairings, check_qk_norm_rope_brute_force,
+    check_group_scale_options,
 ]

@@ -58,6 +58,12 @@ MUTANTS = {
                                "uint16_t rb = orc_bf16_encode(orc_bf16_decode(xrow[j]));"),
     "pad_eps_dropped": ("double scale = 1.0 / sqrt(sq / (double)H + (double)eps);",
                         "double scale = 1.0 / sqrt(sq / (double)H);"),
+    "ue8m0_rounds_down": ("    while (ldexp(ORC_E4M3_MAX, e - 1) >= a)\n        --e;\n    return ldexp(1.0, e);",
+                          "    while (ldexp(ORC_E4M3_MAX, e - 1) >= a)\n        --e;\n    return ldexp(1.0, e - 1);"),
+    "ue8m0_ignored": ("float s32 = (flags & ORC_UE8M0) ? (float)ue8m0_scale(amax) : dynamic_scale(amax);",
+                      "float s32 = dynamic_scale(amax);"),
+    "ue8m0_wrong_floor": ("const double a = fmax(amax, orc_amax_floor());", "const double a = fmax(amax, 1e-8);"),
+    "col_major_unpadded_stride": ("scale[g * ((T + 3) / 4 * 4) + t] = s32;", "scale[g * T + t] = s32;"),
     "rope_sign": ("rot[a] = y[a] * c - y[b] * sn;", "rot[a] = y[a] * c + y[b] * sn;"),
     "rope_cos_sin_swapped": ("double c = (double)cs[i], sn = (double)cs[D / 2 + i];",
                              "double sn = (double)cs[i], c = (double)cs[D / 2 + i];"),
