@@ -75,6 +75,21 @@ typedef enum {
     VG_SCALE_PER_GROUP = 2  /* s per G columns: scale[T, n/G] written, row-major    */
 } vg_scale_mode;
 
+/*
+ * Per-group options, or-ed into `mode` with VG_SCALE_PER_GROUP only (any
+ * other use is VG_ERR_BAD_MODE): the scale formats a GEMM on sm100 consumes
+ * (the pages' "Support Matrix" pairs per-group FP8 there with DeepGEMM;
+ * E8M0 is from the OCP Microscaling spec).
+ *   VG_SCALE_UE8M0         each scale is the smallest power of two
+ *                          >= max(amax, 1e-10f) / 448 (stored as fp32);
+ *                          codes are e4m3(y / s)
+ *   VG_SCALE_COLUMN_MAJOR  scale (t, g) is stored at [g, t] of an fp32
+ *                          [n/G, T4] tensor, T4 = T rounded up to a multiple
+ *                          of 4 (16-byte rows); columns [T, T4) are not written
+ */
+#define VG_SCALE_UE8M0 0x100
+#define VG_SCALE_COLUMN_MAJOR 0x200
+
 typedef enum {
     VG_OK = 0,
     VG_ERR_NULL_PTR = 1,           /* a required pointer is NULL, or residual_out
@@ -82,7 +97,8 @@ typedef enum {
     VG_ERR_BAD_SHAPE = 2,          /* num_tokens < 0, row length not a multiple
                                       of 8, < 8, or > VG_MAX_ROW                  */
     VG_ERR_MISALIGNED = 3,         /* a tensor pointer breaks the alignment rule */
-    VG_ERR_BAD_MODE = 4,           /* mode is not a vg_scale_mode                 */
+    VG_ERR_BAD_MODE = 4,           /* mode is not a vg_scale_mode (with valid
+                                      per-group options)                          */
     VG_ERR_BAD_GROUP = 5,          /* per-group with group_size not 64 or 128, or
                                       not dividing the row length                 */
     VG_ERR_UNSUPPORTED_DEVICE = 6, /* current device is not compute capability 10.3 */
@@ -104,8 +120,9 @@ typedef enum {
  *   weight       in   uint16 [H]     bf16
  *   num_tokens T >= 0; hidden H: multiple of 8, 8 <= H <= VG_MAX_ROW
  *   eps          added to mean(r^2) inside the square root
- *   mode         vg_scale_mode; group_size 64 or 128 (PER_GROUP only,
- *                ignored otherwise)
+ *   mode         vg_scale_mode, with VG_SCALE_PER_GROUP optionally or-ed
+ *                with VG_SCALE_UE8M0 / VG_SCALE_COLUMN_MAJOR; group_size 64
+ *                or 128 (PER_GROUP only, ignored otherwise)
  */
 vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *scale,
                                     const uint16_t *x, const uint16_t *residual,

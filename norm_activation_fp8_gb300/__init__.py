@@ -34,6 +34,7 @@ import threading
 from .build import LIB_PATH
 
 STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
+UE8M0, COLUMN_MAJOR = 0x100, 0x200  # per-group options, or-ed into the mode
 MAX_ROW = 32768
 
 STATUS_NAMES = {
@@ -282,6 +283,9 @@ def vg_device_status(reset: bool = False) -> int:
 
 def _scale_out(mode, T, n, group_size, scale, device):
     import torch
+    if mode & COLUMN_MAJOR:
+        return torch.empty((n // group_size, (T + 3) // 4 * 4), dtype=torch.float32, device=device)
+    mode &= 0xFF
     if mode == STATIC:
         if scale is None:
             raise ValueError("static mode needs a scale tensor")

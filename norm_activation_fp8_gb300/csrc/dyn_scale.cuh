@@ -59,6 +59,37 @@ __device__ __forceinline__ DynScale make_dyn_scale(float amax, float y, float dy
   return d;
 }
 
+// UE8M0 (power-of-two) scale of a row or group: the smallest s = 2^k with
+// 448 s >= X = max(amax * inv, A_MIN), inv = y + dy.  The comparisons with
+// 448 * 2^k are exact (an FMA difference of nearby fp32 numbers, then the
+// sign of the double-float remainder).  Returns s in .s and the element
+// multiplier y / s in .ra (v = t * ra; .a = 0 marks the power-of-two form).
+__device__ __forceinline__ bool df_at_most(float xh, float xl, float p) {
+  const float d = xh - p;  // exact when xh and p are within a factor of two
+  return d < 0.f || (d == 0.f && xl <= 0.f);
+}
+
+__device__ __forceinline__ DynScale make_pow2_scale(float amax, float y, float dy) {
+  float xh = amax * y;
+  float xl = fmaf(amax, y, -xh) + amax * dy;
+  if (xh < kAmaxFloor) {  // floored (the equal case rounds to the floor too)
+    xh = kAmaxFloor;
+    xl = 0.f;
+  }
+  int k;
+  frexpf(xh * kInv448, &k);  // 2^(k-1) <= ~X/448 < 2^k, possibly off by one
+  for (int it = 0; it < 2; ++it) {
+    if (!df_at_most(xh, xl, ldexpf(kE4M3Max, k))) ++k;
+    else if (df_at_most(xh, xl, ldexpf(kE4M3Max, k - 1))) --k;
+  }
+  DynScale d;
+  d.s = ldexpf(1.0f, k);
+  d.a = 0.f;
+  d.ra = ldexpf(y, -k);
+  d.f = 1.0f;
+  return d;
+}
+
 // Two elements: v = (448 t / a correctly rounded) * f.  For an exact tie the
 // quotient is exactly a midpoint and f moves it off, in the direction the
 // stored scale was rounded; every other quotient lies at least 2^-22

@@ -7,8 +7,10 @@
 namespace vg {
 
 // kStatic / kPerToken / kPerGroup are vg_scale_mode; kBf16Pad is the
-// norm's bf16 output into a padded row (no quantisation).
-enum ScaleMode : int { kStatic = 0, kPerToken = 1, kPerGroup = 2, kBf16Pad = 3 };
+// norm's bf16 output into a padded row (no quantisation); kPerGroupX is
+// per-group with scale options (UE8M0 scales and/or the column-major
+// layout), kept apart so that plain per-group code stays as it is.
+enum ScaleMode : int { kStatic = 0, kPerToken = 1, kPerGroup = 2, kBf16Pad = 3, kPerGroupX = 4 };
 
 // How a row-wise kernel covers a [T, n] tensor: each row is split into
 // nch = n/8 chunks of 16 bytes; `ntr` threads (a multiple of 32) own a row,
@@ -49,6 +51,12 @@ struct NormArgs {
   float inv_h;     // 1 / H
   uint16_t *out16; // kBf16Pad: bf16 output rows of nch_pad chunks
   int32_t nch_pad; // kBf16Pad: padded row length / 8
+  // per-group scale (t, g) lives at scale[t * s_ts + g * s_gs] (row-major:
+  // s_ts = ngroups, s_gs = 1; column-major: s_ts = 1, s_gs = T rounded up
+  // to 4); ue8m0: power-of-two scales
+  int32_t s_ts;
+  int32_t s_gs;
+  int32_t ue8m0;
 };
 
 struct SiluArgs {
@@ -62,6 +70,9 @@ struct SiluArgs {
   int32_t rpc;
   int32_t gch;
   int32_t ngroups;
+  int32_t s_ts;    // per-group scale (t, g) at scale[t * s_ts + g * s_gs]
+  int32_t s_gs;
+  int32_t ue8m0;   // power-of-two per-group scales
 };
 
 cudaError_t launch_norm_fp8(NormArgs a, int mode, const RowPlan &plan, cudaStream_t stream);

@@ -94,7 +94,8 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
   // by the slot's thread, from the warp partials and chunk amaxes.  The bf16
   // output has one slot per row holding inv = y + dy.
   const int row_chunks = a.ntr * VPT;
-  const int nslots = MODE == kPerGroup ? a.ngroups : 1;
+  constexpr bool PG = MODE == kPerGroup || MODE == kPerGroupX;
+  const int nslots = PG ? a.ngroups : 1;
   float hi = acc.ss.x, lo = acc.lo.x + acc.lo.y;
   two_sum_acc(hi, lo, acc.ss.y);
   lanes_sum2(hi, lo, 32);
@@ -103,7 +104,7 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
 #pragma unroll
     for (int k = 0; k < VPT; ++k) am = fmaxf(am, cmax[k]);
     am = warp_max(am);
-  } else if (MODE == kPerGroup) {
+  } else if (PG) {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) sm.cmax[slot * row_chunks + lr + k * a.ntr] = cmax[k];
   }
@@ -122,14 +123,20 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
     if (MODE == kBf16Pad) {
       sm.dyn[slot] = DynScale{y, dy, 0.f, 0.f};
     } else {
-      if (MODE == kPerGroup) {
+      if (PG) {
         amr = 0.f;
 #pragma unroll
         for (int i = 0; i < GCH; ++i) amr = fmaxf(amr, sm.cmax[slot * row_chunks + lr * GCH + i]);
       }
-      const DynScale d = make_dyn_scale(amr, y, dy);
+      const DynScale d = MODE == kPerGroupX && a.ue8m0 ? make_pow2_scale(amr, y, dy)
+                                                       : make_dyn_scale(amr, y, dy);
       sm.dyn[slot * nslots + lr] = d;
-      if (live) a.scale[row * nslots + lr] = d.s;
+      if (live) {
+        if (MODE == kPerGroupX)
+          a.scale[row * a.s_ts + (int64_t)lr * a.s_gs] = d.s;
+        else
+          a.scale[row * nslots + lr] = d.s;
+      }
     }
   }
   __syncthreads();
@@ -153,11 +160,21 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
     // padding chunks (c >= nch) read slot 0 and store nothing
     const DynScale d = sm.dyn[slot * nslots + (MODE == kPerToken || c >= a.nch ? 0 : c / GCH)];
     float v[8];
+    if (MODE == kPerGroupX && a.ue8m0) {  // v = t * y / 2^k (ulp-level, no exact ties)
+      const float2 m2 = make_float2(d.ra, d.ra);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 q = dyn_values(t[k][i], d);
-      v[2 * i] = q.x;
-      v[2 * i + 1] = q.y;
+      for (int i = 0; i < 4; ++i) {
+        const float2 q = f2_mul(t[k][i], m2);
+        v[2 * i] = q.x;
+        v[2 * i + 1] = q.y;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 q = dyn_values(t[k][i], d);
+        v[2 * i] = q.x;
+        v[2 * i + 1] = q.y;
+      }
     }
     if (live && c < a.nch) st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
   }
@@ -243,7 +260,7 @@ template <int VPT, int MODE, int GCH, bool RES>
 __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, const int stages) {
   constexpr bool DYN = MODE != kStatic;
   extern __shared__ __align__(128) unsigned char dsm[];
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup ? a.ngroups : 1);
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup || MODE == kPerGroupX ? a.ngroups : 1);
   const TmaLayout L(a.H, RES, stages, blockDim.x, VPT, slots);
   const RowSmem sm = carve_row_smem(dsm + L.row_off, blockDim.x, VPT);
   unsigned char *wbuf = dsm + L.w_off;
@@ -326,7 +343,7 @@ __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, con
 
 template <int VPT, int MODE, int GCH>
 cudaError_t launch_res(const NormArgs &a, const RowPlan &p, cudaStream_t s) {
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup ? a.ngroups : 1) * p.rpc;
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup || MODE == kPerGroupX ? a.ngroups : 1) * p.rpc;
   const size_t smem = row_smem_bytes(p.block(), VPT, slots);
   if (a.res != nullptr)
     norm_fp8_kernel<VPT, MODE, GCH, true><<<(unsigned)p.grid, p.block(), smem, s>>>(a);
@@ -337,7 +354,7 @@ cudaError_t launch_res(const NormArgs &a, const RowPlan &p, cudaStream_t s) {
 
 template <int VPT, int MODE, int GCH, bool RES>
 cudaError_t launch_tma_res(const NormArgs &a, const TmaPlan &p, cudaStream_t s) {
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup ? a.ngroups : 1);
+  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup || MODE == kPerGroupX ? a.ngroups : 1);
   const TmaLayout L(a.H, RES, p.stages, p.block, VPT, slots);
   auto kern = norm_fp8_tma_kernel<VPT, MODE, GCH, RES>;
   // opt in to large dynamic shared memory once per instantiation and device
@@ -368,6 +385,9 @@ cudaError_t launch_mode(const NormArgs &a, int mode, const RowPlan &p, cudaStrea
     case kPerToken: return launch_res<VPT, kPerToken, 1>(a, p, s);
     case kBf16Pad: return launch_res<VPT, kBf16Pad, 1>(a, p, s);
     default:
+      if (a.ue8m0 || a.s_gs != 1)
+        return a.gch == 8 ? launch_res<VPT, kPerGroupX, 8>(a, p, s)
+                          : launch_res<VPT, kPerGroupX, 16>(a, p, s);
       return a.gch == 8 ? launch_res<VPT, kPerGroup, 8>(a, p, s)
                         : launch_res<VPT, kPerGroup, 16>(a, p, s);
   }
@@ -381,6 +401,9 @@ cudaError_t launch_tma_vpt(const NormArgs &a, int mode, const TmaPlan &p, cudaSt
     case kPerToken: return launch_tma_mode<VPT, kPerToken, 1>(a, p, s);
     case kBf16Pad: return launch_tma_mode<VPT, kBf16Pad, 1>(a, p, s);
     default:
+      if (a.ue8m0 || a.s_gs != 1)
+        return a.gch == 8 ? launch_tma_mode<VPT, kPerGroupX, 8>(a, p, s)
+                          : launch_tma_mode<VPT, kPerGroupX, 16>(a, p, s);
       return a.gch == 8 ? launch_tma_mode<VPT, kPerGroup, 8>(a, p, s)
                         : launch_tma_mode<VPT, kPerGroup, 16>(a, p, s);
   }

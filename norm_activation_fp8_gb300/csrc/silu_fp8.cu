@@ -74,6 +74,35 @@ __device__ __forceinline__ float silu_scale(float amax) {
   return fmaxf(amax, kAmaxFloor) * (1.0f / kE4M3Max);
 }
 
+// The SiLU values of a chunk in fp64 (the exponential by CUDA's double exp):
+// used only to settle a power-of-two scale whose fp32 amax lies within a few
+// ulps of a boundary.
+__device__ __noinline__ double silu_amax8_f64(uint4 gv, uint4 uv) {
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+  double m = 0.0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 g = bf16x2_to_f2(gw[i]), u = bf16x2_to_f2(uw[i]);
+    const double a0 = (double)g.x / (1.0 + exp(-(double)g.x)) * (double)u.x;
+    const double a1 = (double)g.y / (1.0 + exp(-(double)g.y)) * (double)u.y;
+    m = fmax(m, fmax(fabs(a0), fabs(a1)));
+  }
+  return m;
+}
+
+// The smallest k with 448 * 2^k >= max(amax, A_MIN) (exact comparisons).
+__device__ __forceinline__ int pow2_exponent(double amax) {
+  const double a = fmax(amax, (double)kAmaxFloor);
+  int k;
+  frexp(a * (1.0 / kE4M3Max), &k);
+  for (int it = 0; it < 2; ++it) {
+    if (ldexp((double)kE4M3Max, k) < a) ++k;
+    else if (ldexp((double)kE4M3Max, k - 1) >= a) --k;
+  }
+  return k;
+}
+
 __device__ __forceinline__ float amax8(const float (&v)[8]) {
   float m = 0.f;
 #pragma unroll
@@ -90,7 +119,9 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
 // loads and stores, so they fit three 512-thread CTAs per SM; per-token
 // keeps its row's activations and fits two 512-thread or one 1024-thread
 // CTA.
-template <int VPT, int MODE, int GCH, bool BIG>
+// OPT: per-group with scale options (UE8M0 and/or column-major), an
+// instance of its own so that plain per-group code stays as it is.
+template <int VPT, int MODE, int GCH, bool BIG, bool OPT = false>
 __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken ? 2 : 3))
     silu_fp8_kernel(const SiluArgs a) {
   __shared__ float red[32];
@@ -126,9 +157,35 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
       silu_chunk(gv[k], uv[k], v);
       float m = inv_static;
       if (MODE == kPerGroup) {
-        const float s = silu_scale(lanes_max(amax8(v), GCH));
-        if (live && c < a.nch && (c & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
-        m = fast_rcp(s);
+        if constexpr (OPT) {
+          const float am = lanes_max(amax8(v), GCH);
+          float s;
+          if (a.ue8m0) {
+            // power-of-two scale; the fp32 amax is within ~3 ulps of the
+            // exact one, so a boundary that close is settled in fp64
+            int e = pow2_exponent((double)am);
+            const float fa = fmaxf(am, kAmaxFloor);
+            const bool near = fa <= ldexpf(kE4M3Max, e - 1) * (1.0f + 1.0f / 262144.0f) ||
+                              fa >= ldexpf(kE4M3Max, e) * (1.0f - 1.0f / 262144.0f);
+            if (__any_sync(0xFFFFFFFFu, near)) {
+              double am64 = silu_amax8_f64(gv[k], uv[k]);
+              for (int o = GCH >> 1; o > 0; o >>= 1)
+                am64 = fmax(am64, __shfl_xor_sync(0xFFFFFFFFu, am64, o));
+              e = pow2_exponent(am64);
+            }
+            s = ldexpf(1.0f, e);
+            m = ldexpf(1.0f, -e);
+          } else {
+            s = silu_scale(am);
+            m = fast_rcp(s);
+          }
+          if (live && c < a.nch && (c & (GCH - 1)) == 0)
+            a.scale[row * a.s_ts + (int64_t)(c / GCH) * a.s_gs] = s;
+        } else {
+          const float s = silu_scale(lanes_max(amax8(v), GCH));
+          if (live && c < a.nch && (c & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
+          m = fast_rcp(s);
+        }
       }
       scale8(v, m);
       if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
@@ -295,10 +352,16 @@ cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStrea
         silu_fp8_kernel<VPT, kPerToken, 1, false><<<g, b, 0, s>>>(a);
       break;
     default:
-      if (a.gch == 8)
+      if (a.ue8m0 || a.s_gs != 1) {
+        if (a.gch == 8)
+          silu_fp8_kernel<VPT, kPerGroup, 8, false, true><<<g, b, 0, s>>>(a);
+        else
+          silu_fp8_kernel<VPT, kPerGroup, 16, false, true><<<g, b, 0, s>>>(a);
+      } else if (a.gch == 8) {
         silu_fp8_kernel<VPT, kPerGroup, 8, false><<<g, b, 0, s>>>(a);
-      else
+      } else {
         silu_fp8_kernel<VPT, kPerGroup, 16, false><<<g, b, 0, s>>>(a);
+      }
       break;
   }
   return cudaGetLastError();

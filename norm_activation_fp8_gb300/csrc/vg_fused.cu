@@ -48,14 +48,30 @@ inline void clear_stale_error() { (void)cudaGetLastError(); }
 
 inline bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
 
-vg_status check_row(int64_t num_tokens, int64_t n, int32_t mode, int32_t group_size) {
+vg_status check_row(int64_t num_tokens, int64_t n, int32_t mode_flags, int32_t group_size) {
+  const int32_t mode = mode_flags & 0xFF, flags = mode_flags & ~0xFF;
   if (mode != VG_SCALE_STATIC && mode != VG_SCALE_PER_TOKEN && mode != VG_SCALE_PER_GROUP)
     return VG_ERR_BAD_MODE;
+  if ((flags & ~(VG_SCALE_UE8M0 | VG_SCALE_COLUMN_MAJOR)) != 0 ||
+      (flags != 0 && mode != VG_SCALE_PER_GROUP))
+    return VG_ERR_BAD_MODE;
+  if ((flags & VG_SCALE_COLUMN_MAJOR) && num_tokens > INT32_MAX - 3)  // T4 must fit int32
+    return VG_ERR_BAD_SHAPE;
   if (num_tokens < 0 || num_tokens > INT32_MAX || n < 8 || n % 8 != 0 || n > VG_MAX_ROW)
     return VG_ERR_BAD_SHAPE;
   if (mode == VG_SCALE_PER_GROUP && ((group_size != 64 && group_size != 128) || n % group_size != 0))
     return VG_ERR_BAD_GROUP;
   return VG_OK;
+}
+
+// Where scale (t, g) goes and whether it is a power of two, from the mode's
+// per-group options.
+template <class Args>
+void set_scale_layout(Args &a, int32_t mode_flags, int64_t T) {
+  const bool col = (mode_flags & VG_SCALE_COLUMN_MAJOR) != 0;
+  a.s_ts = col ? 1 : a.ngroups;
+  a.s_gs = col ? (int32_t)((T + 3) / 4 * 4) : 1;
+  a.ue8m0 = (mode_flags & VG_SCALE_UE8M0) != 0;
 }
 
 }  // namespace
@@ -279,6 +295,8 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
                                     float eps, int32_t mode, int32_t group_size,
                                     vg_stream_t stream) {
   vg_status st = vg::check_row(num_tokens, hidden, mode, group_size);
+  const int32_t mode_flags = mode;
+  mode &= 0xFF;
   if (st != VG_OK || num_tokens == 0) return st;
   if (!q || !scale || !x || !weight || ((residual == nullptr) != (residual_out == nullptr)))
     return VG_ERR_NULL_PTR;
@@ -303,6 +321,7 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
   a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(hidden / group_size) : 1;
   a.eps = eps;
   a.inv_h = 1.0f / (float)hidden;
+  vg::set_scale_layout(a, mode_flags, num_tokens);
   vg::TmaPlan tp;
   if (vg::plan_norm_tma(num_tokens, (int)hidden, residual != nullptr, mode, a.ngroups, sms, &tp))
     return vg::launch_norm_fp8_tma(a, mode, tp, (cudaStream_t)stream) == cudaSuccess ? VG_OK
@@ -345,6 +364,7 @@ vg_status vg_fused_add_rms_norm_pad(uint16_t *out, uint16_t *residual_out, const
   a.inv_h = 1.0f / (float)hidden;
   a.out16 = out;
   a.nch_pad = (int32_t)(padded_hidden / 8);
+  vg::set_scale_layout(a, VG_SCALE_PER_TOKEN, num_tokens);
   // the same plans as the dynamic per-token norm: one double-float inv per row
   vg::TmaPlan tp;
   if (vg::plan_norm_tma(num_tokens, (int)hidden, residual != nullptr, VG_SCALE_PER_TOKEN, 1, sms,
@@ -399,6 +419,8 @@ vg_status vg_fused_qk_norm_rope(uint16_t *qkv, const uint16_t *q_weight, const u
 vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int64_t num_tokens,
                           int64_t inter, int32_t mode, int32_t group_size, vg_stream_t stream) {
   vg_status st = vg::check_row(num_tokens, inter, mode, group_size);
+  const int32_t mode_flags = mode;
+  mode &= 0xFF;
   if (st != VG_OK || num_tokens == 0) return st;
   if (!q || !scale || !gate_up) return VG_ERR_NULL_PTR;
   if (vg::misaligned(q, 16) || vg::misaligned(gate_up, 16) || vg::misaligned(scale, 4))
@@ -416,6 +438,7 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
   a.nch = (int32_t)(inter / 8);
   a.gch = mode == VG_SCALE_PER_GROUP ? group_size / 8 : 1;
   a.ngroups = mode == VG_SCALE_PER_GROUP ? (int32_t)(inter / group_size) : 1;
+  vg::set_scale_layout(a, mode_flags, num_tokens);
   vg::SiluTmaPlan tp;
   if (vg::plan_silu_tma_token(num_tokens, a.nch, mode, sms, &tp))
     return vg::launch_silu_fp8_tma_token(a, tp, (cudaStream_t)stream) == cudaSuccess ? VG_OK

@@ -41,6 +41,12 @@ def _blocks(rows, nblk):
 
 # ------------------------------------------------------------------ oracle
 
+def _oracle_mode(mode):
+    """The oracle runs a mode's arithmetic with row-major scales; the layout
+    itself is pinned in the oracle's own tests."""
+    return mode & ~COL_MAJOR
+
+
 def oracle_norm(x, residual, weight, eps, mode, group_size=128, scale=None, want_v=True):
     """The oracle over all rows of x, split into row blocks run in threads
     (rows are independent; the oracle releases the GIL in its C code)."""
@@ -48,9 +54,11 @@ def oracle_norm(x, residual, weight, eps, mode, group_size=128, scale=None, want
     out = {"q": np.empty((T, H), np.uint8),
            "residual_out": None if residual is None else np.empty((T, H), np.uint16),
            "v": np.empty((T, H), np.float64) if want_v else None}
-    if mode == 0:
+    base = mode & 0xFF
+    mode = _oracle_mode(mode)
+    if base == 0:
         out["scale"] = np.array([np.float32(scale)], np.float32)
-    elif mode == 1:
+    elif base == 1:
         out["scale"] = np.empty((T,), np.float32)
     else:
         out["scale"] = np.empty((T, H // group_size), np.float32)
@@ -77,9 +85,11 @@ def oracle_silu(gate_up, mode, group_size=128, scale=None, want_v=True):
     T, two_i = gate_up.shape
     I = two_i // 2
     out = {"q": np.empty((T, I), np.uint8), "v": np.empty((T, I), np.float64) if want_v else None}
-    if mode == 0:
+    base = mode & 0xFF
+    mode = _oracle_mode(mode)
+    if base == 0:
         out["scale"] = np.array([np.float32(scale)], np.float32)
-    elif mode == 1:
+    elif base == 1:
         out["scale"] = np.empty((T,), np.float32)
     else:
         out["scale"] = np.empty((T, I // group_size), np.float32)
@@ -319,6 +329,49 @@ def _check_guards(buf, nbytes, what):
         raise ParityError(f"{what}: write outside the output buffer")
 
 
+UE8M0, COL_MAJOR = 0x100, 0x200
+
+
+def _scale_buffer(torch, mode, T, n, group_size, scale, device):
+    """The guarded scale tensor for a mode (flags included): [1] static
+    (filled), [T] per-token, [T, n/G] per-group, or [n/G, T4] column-major,
+    whose padding columns keep the 0xAA guard pattern."""
+    base = mode & 0xFF
+    if base == 0:
+        sbuf, sraw = _guarded(torch, 4, device)
+        s = sraw.view(torch.float32)
+        s.fill_(float(np.float32(scale)))
+        return sbuf, s
+    if base == 1:
+        ns = T
+    elif mode & COL_MAJOR:
+        ns = (n // group_size) * ((T + 3) // 4 * 4)
+    else:
+        ns = T * (n // group_size)
+    sbuf, sraw = _guarded(torch, 4 * ns, device)
+    return sbuf, sraw.view(torch.float32)
+
+
+def _scales_row_major(s, mode, T, n, group_size):
+    """Scales as the oracle's row-major [T, n/G] (or [T] / [1]); a
+    column-major buffer must hold the guard pattern in its padding columns."""
+    base = mode & 0xFF
+    a = s.cpu().numpy()
+    if base == 0:
+        return a
+    if base == 1:
+        return a.reshape(T)
+    g = n // group_size
+    if mode & COL_MAJOR:
+        t4 = (T + 3) // 4 * 4
+        a = a.reshape(g, t4)
+        pad = a[:, T:].view(np.uint32)
+        if not np.all(pad == 0xAAAAAAAA):
+            raise ParityError("scale: column-major padding columns were written")
+        return np.ascontiguousarray(a[:, :T].T)
+    return a.reshape(T, g)
+
+
 def gpu_norm(x, residual, weight, eps, mode, group_size=128, scale=None, inplace=True,
              device="cuda"):
     """Runs the CUDA path through the C ABI on numpy bf16-bit inputs; outputs
@@ -340,21 +393,12 @@ def gpu_norm(x, residual, weight, eps, mode, group_size=128, scale=None, inplace
             rt = torch.from_numpy(residual.view(np.int16)).to(device)
             rbuf, rraw = _guarded(torch, T * H * 2, device)
             r_out = rraw.view(torch.int16).view(T, H)
-    if mode == 0:
-        sbuf, sraw = _guarded(torch, 4, device)
-        s = sraw.view(torch.float32)
-        s.fill_(float(np.float32(scale)))
-    else:
-        ns = T if mode == 1 else T * (H // group_size)
-        sbuf, sraw = _guarded(torch, 4 * ns, device)
-        s = sraw.view(torch.float32)
+    sbuf, s = _scale_buffer(torch, mode, T, H, group_size, scale, device)
     vg.vg_fused_add_rms_norm_fp8(q.view(T, H), r_out, s, xt, rt, wt, eps, mode, group_size)
     torch.cuda.synchronize()
     _check_guards(qbuf, T * H, "q")
     _check_guards(sbuf, s.numel() * 4, "scale")
-    out = {"q": q.view(T, H).cpu().numpy(),
-           "scale": s.cpu().numpy() if mode == 0 else
-           s.view(T, -1).cpu().numpy().reshape((T,) if mode == 1 else (T, H // group_size))}
+    out = {"q": q.view(T, H).cpu().numpy(), "scale": _scales_row_major(s, mode, T, H, group_size)}
     if residual is not None:
         _check_guards(rbuf, T * H * 2, "residual_out")
         out["residual_out"] = r_out.cpu().numpy().view(np.uint16)
@@ -370,21 +414,12 @@ def gpu_silu(gate_up, mode, group_size=128, scale=None, device="cuda"):
     I = two_i // 2
     gt = torch.from_numpy(gate_up.view(np.int16)).to(device)
     qbuf, q = _guarded(torch, T * I, device)
-    if mode == 0:
-        sbuf, sraw = _guarded(torch, 4, device)
-        s = sraw.view(torch.float32)
-        s.fill_(float(np.float32(scale)))
-    else:
-        ns = T if mode == 1 else T * (I // group_size)
-        sbuf, sraw = _guarded(torch, 4 * ns, device)
-        s = sraw.view(torch.float32)
+    sbuf, s = _scale_buffer(torch, mode, T, I, group_size, scale, device)
     vg.vg_silu_mul_fp8(q.view(T, I), s, gt, mode, group_size)
     torch.cuda.synchronize()
     _check_guards(qbuf, T * I, "q")
     _check_guards(sbuf, s.numel() * 4, "scale")
-    return {"q": q.view(T, I).cpu().numpy(),
-            "scale": s.cpu().numpy() if mode == 0 else
-            s.cpu().numpy().reshape((T,) if mode == 1 else (T, I // group_size))}
+    return {"q": q.view(T, I).cpu().numpy(), "scale": _scales_row_major(s, mode, T, I, group_size)}
 
 
 def gpu_mla(q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, q_fp8, rope=64, q_pad=None,
