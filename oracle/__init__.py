@@ -7,7 +7,8 @@ package never imports it and shares no code with it.
 
 What each function computes is documented in ``oracle.c`` with the passages
 it follows ("Fusion torch.compile passes", sections "RMSNorm + Quantization
-(fuse_norm_quant)", "SiLU+Mul + Quantization (fuse_act_quant)", "MLA Dual
+(fuse_norm_quant)", "SiLU+Mul + Quantization (fuse_act_quant)" (FP8, and FP4 as
+NVIDIA's NVFP4), "MLA Dual
 RMSNorm (fuse_mla_dual_rms_norm)", "RMSNorm + Padding (fuse_act_padding)" and
 "QK Norm + RoPE (enable_qk_norm_rope_fusion)"; OCP OFP8 for the E4M3 format).
 
@@ -26,6 +27,9 @@ Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
   per-group UE8M0 / column-major scales ... pinned (powers of two that
                               bracket amax/448, exact rationals, the
                               transposed layout of the row-major scales)
+  e2m1 codec, NVFP4 quant ... pinned (all 16 codes, exhaustive nearest
+                              value, block scales and codes against exact
+                              rationals, packing)
   qk_norm_rope .............. pinned (identity and quarter-turn rotations
                               against the pinned bf16 rms_norm, V untouched,
                               neox/gptj by permutation, exact rationals)
@@ -88,8 +92,14 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.orc_qk_norm_rope.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i64, ctypes.c_float,
                                      ctypes.c_int]
     lib.orc_qk_norm_rope.restype = ctypes.c_int
+    lib.orc_fused_add_rms_norm_nvfp4.argtypes = [P, P, P, P, P, P, P, ctypes.c_float, i64, i64,
+                                                 ctypes.c_float]
+    lib.orc_fused_add_rms_norm_nvfp4.restype = ctypes.c_int
+    lib.orc_silu_mul_nvfp4.argtypes = [P, P, P, P, ctypes.c_float, i64, i64]
+    lib.orc_silu_mul_nvfp4.restype = ctypes.c_int
     for name in ("orc_bf16_decode_n", "orc_bf16_encode_n",
-                 "orc_e4m3_decode_n", "orc_e4m3_encode_n"):
+                 "orc_e4m3_decode_n", "orc_e4m3_encode_n",
+                 "orc_e2m1_decode_n", "orc_e2m1_encode_n"):
         getattr(lib, name).argtypes = [P, P, i64]
         getattr(lib, name).restype = None
     lib.orc_amax_floor.argtypes = []
@@ -127,6 +137,18 @@ class Oracle:
         v = np.ascontiguousarray(values, dtype=np.float64)
         out = np.empty(v.shape, np.uint8)
         self.lib.orc_e4m3_encode_n(_ptr(out), _ptr(v), v.size)
+        return out
+
+    def e2m1_decode(self, codes) -> np.ndarray:
+        c = np.ascontiguousarray(codes, dtype=np.uint8)
+        out = np.empty(c.shape, np.float64)
+        self.lib.orc_e2m1_decode_n(_ptr(out), _ptr(c), c.size)
+        return out
+
+    def e2m1_encode(self, values) -> np.ndarray:
+        v = np.ascontiguousarray(values, dtype=np.float64)
+        out = np.empty(v.shape, np.uint8)
+        self.lib.orc_e2m1_encode_n(_ptr(out), _ptr(v), v.size)
         return out
 
     def amax_floor(self) -> float:
@@ -177,6 +199,40 @@ class Oracle:
             raise ValueError(f"oracle rejected the arguments (rc={rc})")
         return {"q": q, "scale": s, "v": v}
 
+
+    def fused_add_rms_norm_nvfp4(self, x, residual, weight, eps: float, global_scale: float,
+                                 want_v: bool = True):
+        """fused_add_rms_norm(x, residual) -> NVFP4 (residual None: the plain
+        variant).  Returns dict(q4 uint8 [T,H/2] (column 2i in the low
+        nibble), sf uint8 [T,H/16] E4M3 block codes, residual_out, v)."""
+        x = _u16(x)
+        T, H = x.shape
+        w = _u16(weight).reshape(H)
+        res = None if residual is None else _u16(residual).reshape(T, H)
+        q4 = np.empty((T, H // 2), np.uint8)
+        sf = np.empty((T, H // 16), np.uint8)
+        r_out = None if res is None else np.empty((T, H), np.uint16)
+        v = np.empty((T, H), np.float64) if want_v else None
+        rc = self.lib.orc_fused_add_rms_norm_nvfp4(_ptr(q4), _ptr(sf), _ptr(r_out), _ptr(v), _ptr(x),
+                                                   _ptr(res), _ptr(w), ctypes.c_float(global_scale),
+                                                   T, H, ctypes.c_float(eps))
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (rc={rc})")
+        return {"q4": q4, "sf": sf, "residual_out": r_out, "v": v}
+
+    def silu_mul_nvfp4(self, gate_up, global_scale: float, want_v: bool = True):
+        """silu_and_mul(gate_up) -> NVFP4.  Returns dict(q4 [T,I/2], sf [T,I/16], v)."""
+        gu = _u16(gate_up)
+        T, two_i = gu.shape
+        I = two_i // 2
+        q4 = np.empty((T, I // 2), np.uint8)
+        sf = np.empty((T, I // 16), np.uint8)
+        v = np.empty((T, I), np.float64) if want_v else None
+        rc = self.lib.orc_silu_mul_nvfp4(_ptr(q4), _ptr(sf), _ptr(v), _ptr(gu),
+                                         ctypes.c_float(global_scale), T, I)
+        if rc != 0:
+            raise ValueError(f"oracle rejected the arguments (rc={rc})")
+        return {"q4": q4, "sf": sf, "v": v}
 
     def rms_norm_bf16(self, x, weight, eps: float, want_y: bool = True):
         """rms_norm(x, weight, eps) with the output rounded once to bf16.
@@ -344,3 +400,19 @@ def fused_add_rms_norm_pad(*args, **kwargs):
 
 def qk_norm_rope(*args, **kwargs):
     return default().qk_norm_rope(*args, **kwargs)
+
+
+def fused_add_rms_norm_nvfp4(*args, **kwargs):
+    return default().fused_add_rms_norm_nvfp4(*args, **kwargs)
+
+
+def silu_mul_nvfp4(*args, **kwargs):
+    return default().silu_mul_nvfp4(*args, **kwargs)
+
+
+def e2m1_decode(codes):
+    return default().e2m1_decode(codes)
+
+
+def e2m1_encode(values):
+    return default().e2m1_encode(values)

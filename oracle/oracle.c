@@ -28,6 +28,12 @@
  *         Section "QK Norm + RoPE (enable_qk_norm_rope_fusion)" -- split
  *         QKV, per-head RMSNorm of Q and K, then rotary embedding, in one
  *         kernel (models that normalise Q and K per head before RoPE).
+ *  [NVFP4] NVIDIA's NVFP4 format ([FUS] "Quick Reference" names FP4 for both
+ *         fusions and the "Support Matrix" NVFP4 dynamic on sm100+, but the
+ *         pages define neither): E2M1 elements (the OCP Microscaling spec's
+ *         FP4: sign, 2 exponent bits with bias 1, 1 mantissa bit; values
+ *         +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}), blocks of 16 consecutive
+ *         elements, an E4M3 scale per block and an fp32 scale per tensor.
  *  [OFP8] OCP 8-bit Floating Point Specification (OFP8), E4M3 encoding:
  *         bias 7, no infinities, S.1111.111 is NaN, max normal 448
  *         (S.1111.110), min normal 2^-6, min subnormal 2^-9.
@@ -148,6 +154,44 @@ uint8_t orc_e4m3_encode(double v)
     return (uint8_t)(sign | (uint8_t)(((e + 7) << 3) | mant));
 }
 
+/* e2m1 ([NVFP4] elements): 2 significant bits, emin 0 (subnormal spacing
+ * 0.5), no infinities or NaN; RNE with saturation at 6.  Code: sign bit 3,
+ * exponent bits 2..1, mantissa bit 0. */
+double orc_e2m1_decode(uint8_t c)
+{
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double mag = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -mag : mag;
+}
+
+uint8_t orc_e2m1_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs(v);
+    double r = isinf(a) ? 6.0 : round_to_precision(a, 2, 0);
+    if (r > 6.0)
+        r = 6.0;
+    if (r == 0.0) /* keeps the sign of zero */
+        return sign;
+    int e = ilogb(r);
+    if (e < 0) /* subnormal: 0.5 */
+        return (uint8_t)(sign | 0x1);
+    int mant = (int)((r / ldexp(1.0, e) - 1.0) * 2.0);
+    return (uint8_t)(sign | (uint8_t)(((e + 1) << 1) | mant));
+}
+
+void orc_e2m1_decode_n(double *out, const uint8_t *in, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e2m1_decode(in[i]);
+}
+
+void orc_e2m1_encode_n(uint8_t *out, const double *in, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e2m1_encode(in[i]);
+}
+
 void orc_bf16_decode_n(double *out, const uint16_t *in, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
@@ -254,6 +298,38 @@ static int check_mode(int mode, int64_t n, int64_t G)
     if (mode == ORC_PER_GROUP && G > 0 && n % G == 0)
         return 0;
     return -1;
+}
+
+/* NVFP4 quantisation of one row y[0..n), n % 16 == 0 ([NVFP4]):
+ *   for each block b of 16 columns:
+ *     sf_b = e4m3(gs * max_j |y_j| / 6)          (the stored E4M3 code)
+ *     v_j  = y_j * gs / decode(sf_b), or 0 when decode(sf_b) == 0
+ *     q_j  = e2m1(v_j)
+ * q4 packs two codes a byte, column 2i in the low nibble of byte i; sf holds
+ * the n/16 block codes; v (optional) receives v_j. */
+static void nvfp4_row(uint8_t *q4, uint8_t *sf, double *v, const double *y, int64_t n, float gs)
+{
+    for (int64_t b = 0; b < n / 16; ++b) {
+        const double *yb = y + b * 16;
+        double amax = 0.0;
+        for (int j = 0; j < 16; ++j)
+            if (fabs(yb[j]) > amax)
+                amax = fabs(yb[j]);
+        uint8_t code = orc_e4m3_encode((double)gs * amax / 6.0);
+        sf[b] = code;
+        double s = orc_e4m3_decode(code);
+        for (int j = 0; j < 16; ++j) {
+            double vj = s > 0.0 ? yb[j] * (double)gs / s : 0.0;
+            uint8_t e = orc_e2m1_encode(vj);
+            int64_t col = b * 16 + j;
+            if (col % 2 == 0)
+                q4[col / 2] = e;
+            else
+                q4[col / 2] = (uint8_t)(q4[col / 2] | (e << 4));
+            if (v)
+                v[col] = vj;
+        }
+    }
 }
 
 /* ------------------------------------------------------------------ ops */
@@ -447,6 +523,72 @@ int orc_qk_norm_rope(uint16_t *qkv, double *o, const uint16_t *q_weight,
     }
     free(y);
     free(rot);
+    return 0;
+}
+
+/* fused_add_rms_norm(x, residual) -> NVFP4 ([FUS] "RMSNorm + Quantization",
+ * the FP4 output of the "Quick Reference"; [NVFP4]): r, residual_out and y as
+ * in orc_fused_add_rms_norm_fp8, then nvfp4_row(y) with the per-tensor scale
+ * gs.  Layouts: q4 [T, H/2] bytes; sf [T, H/16] E4M3 codes; v [T, H]. */
+int orc_fused_add_rms_norm_nvfp4(uint8_t *q4, uint8_t *sf, uint16_t *residual_out, double *v,
+                                 const uint16_t *x, const uint16_t *residual,
+                                 const uint16_t *weight, float gs, int64_t T, int64_t H,
+                                 float eps)
+{
+    if (T < 0 || H <= 0 || H % 16 != 0)
+        return -1;
+    double *r = (double *)malloc((size_t)H * sizeof(double));
+    double *y = (double *)malloc((size_t)H * sizeof(double));
+    if (!r || !y) {
+        free(r);
+        free(y);
+        return -2;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t j = 0; j < H; ++j) {
+            double xj = orc_bf16_decode(x[t * H + j]);
+            if (residual) {
+                uint16_t rb = orc_bf16_encode(xj + orc_bf16_decode(residual[t * H + j]));
+                residual_out[t * H + j] = rb;
+                const double stored = orc_bf16_decode(rb); /* the stored residual */
+                r[j] = stored;
+            } else {
+                r[j] = xj;
+            }
+        }
+        double sumsq = 0.0;
+        for (int64_t j = 0; j < H; ++j)
+            sumsq += r[j] * r[j];
+        double rinv = 1.0 / sqrt(sumsq / (double)H + (double)eps);
+        for (int64_t j = 0; j < H; ++j)
+            y[j] = r[j] * rinv * orc_bf16_decode(weight[j]);
+        nvfp4_row(q4 + t * (H / 2), sf + t * (H / 16), v ? v + t * H : NULL, y, H, gs);
+    }
+    free(r);
+    free(y);
+    return 0;
+}
+
+/* silu_and_mul(gate_up) -> NVFP4 ([FUS] "SiLU+Mul + Quantization", the FP4
+ * output; [NVFP4]): a_j = silu(g_j) * u_j as in orc_silu_mul_fp8, then
+ * nvfp4_row(a).  Layouts: q4 [T, I/2]; sf [T, I/16]; v [T, I]. */
+int orc_silu_mul_nvfp4(uint8_t *q4, uint8_t *sf, double *v, const uint16_t *gate_up, float gs,
+                       int64_t T, int64_t I)
+{
+    if (T < 0 || I <= 0 || I % 16 != 0)
+        return -1;
+    double *act = (double *)malloc((size_t)I * sizeof(double));
+    if (!act)
+        return -2;
+    for (int64_t t = 0; t < T; ++t) {
+        const uint16_t *gu = gate_up + t * 2 * I;
+        for (int64_t j = 0; j < I; ++j) {
+            double g = orc_bf16_decode(gu[j]);
+            act[j] = g / (1.0 + exp(-g)) * orc_bf16_decode(gu[I + j]);
+        }
+        nvfp4_row(q4 + t * (I / 2), sf + t * (I / 16), v ? v + t * I : NULL, act, I, gs);
+    }
+    free(act);
     return 0;
 }
 

@@ -67,6 +67,56 @@ def e4m3_nearest_code_vec(v: np.ndarray) -> np.ndarray:
     return (sign | pick).astype(np.uint8)
 
 
+# --------------------------------------------------------------- e2m1 values
+
+
+def e2m1_positive_values() -> list[F]:
+    """The 8 non-negative E2M1 values in increasing order, listed as
+    significand x 2^k: the subnormal 0.5 (and zero), then 1.m x 2^e for
+    e = 0..2, m = 0..1."""
+    vals = [F(0), F(1, 2)]
+    for e in range(3):
+        for m in range(2):
+            vals.append(F(2 + m, 2) * F(2) ** e)
+    return vals
+
+
+E2M1_POS = e2m1_positive_values()
+
+
+def e2m1_nearest_code(v: F | float) -> int:
+    """Brute-force RNE-with-saturation to E2M1: the nearest value, ties to
+    the even code index (even mantissa), magnitudes above 6 clamped to 6."""
+    v = F(v)
+    sign = 0x8 if v < 0 else 0x0
+    a = abs(v)
+    if a >= E2M1_POS[-1]:
+        return sign | (len(E2M1_POS) - 1)
+    best = None
+    for k, c in enumerate(E2M1_POS):
+        d = abs(a - c)
+        if best is None or d < best[0] or (d == best[0] and k % 2 == 0):
+            best = (d, k)
+    return sign | best[1]
+
+
+def exact_nvfp4(y: list[F], gs: float):
+    """Block codes, (v, code) of one row under NVFP4 with per-tensor scale gs:
+    sf = e4m3(gs * amax / 6) per 16 columns, v = y gs / decode(sf)."""
+    gs = F(float(np.float32(gs)))
+    sf, v, codes = [], [], []
+    for b in range(len(y) // 16):
+        blk = y[16 * b:16 * b + 16]
+        code = e4m3_nearest_code(gs * max(abs(t) for t in blk) / 6)
+        sf.append(code)
+        s = E4M3_POS[code & 0x7F]
+        for t in blk:
+            vj = t * gs / s if s > 0 else F(0)
+            v.append(vj)
+            codes.append(e2m1_nearest_code(vj))
+    return sf, v, codes
+
+
 # --------------------------------------------------------------- bf16 values
 
 

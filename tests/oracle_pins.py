@@ -432,6 +432,78 @@ def check_rms_norm_bf16_brute_force(orc):
             np.testing.assert_allclose(out["y"][t], [float(v) for v in ex["y"]], rtol=1e-13)
 
 
+# ------------------------------------------------------------------ NVFP4
+
+
+def load_e2m1_points():
+    pts = []
+    with open(os.path.join(GOLDEN, "e2m1_ocp_mx_points.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                code, val, *_ = line.split()
+                pts.append((int(code, 16), float(val)))
+    return pts
+
+
+def check_e2m1_codec(orc):
+    """The OCP MX spec's E2M1 points; all 16 codes decode to the value set
+    enumerated as significand x 2^k and round-trip; the encoder equals an
+    exhaustive nearest-value search (ties to the even code, saturation at 6)
+    on every midpoint, midpoint +- 1 ulp and random values of both signs."""
+    for code, val in load_e2m1_points():
+        got = orc.e2m1_decode(np.array([code], np.uint8))[0]
+        assert got == val and np.signbit(got) == np.signbit(val), (hex(code), got, val)
+        assert orc.e2m1_encode(np.array([val]))[0] == code, (val, code)
+    codes = np.arange(16, dtype=np.uint8)
+    dec = orc.e2m1_decode(codes)
+    want = [float(v) for v in exact.E2M1_POS]
+    assert list(dec[:8]) == want and list(-dec[8:]) == want
+    assert np.array_equal(orc.e2m1_encode(dec), codes)
+    pos = [float(v) for v in exact.E2M1_POS]
+    mids = [(a + b) / 2 for a, b in zip(pos, pos[1:])] + [7.0, 6.0, 100.0]
+    rng = np.random.default_rng(29)
+    probe = np.concatenate([mids, np.nextafter(mids, 0), np.nextafter(mids, 100),
+                            rng.uniform(0, 8, 2000)])
+    probe = np.concatenate([probe, -probe])
+    got = orc.e2m1_encode(probe)
+    assert list(got) == [exact.e2m1_nearest_code(float(p)) for p in probe]
+
+
+def check_nvfp4_rows(orc):
+    """Tiny rows of both ops against exact rationals: E4M3 block scale codes
+    of gs*amax/6, E2M1 codes of y*gs/scale, two codes a byte (column 2i in
+    the low nibble); an all-zero block gives scale code 0 and zero codes."""
+    rng = np.random.default_rng(30)
+    floor = orc.amax_floor()
+    T, H = 3, 48
+    x = _rand_bf16(rng, (T, H), scale=np.exp2(rng.integers(-3, 3, (T, H))))
+    x[1, 16:32] = 0                                   # an all-zero block
+    res = _rand_bf16(rng, (T, H))
+    res[1, 16:32] = 0
+    w = _weight(rng, H)
+    gs = 448.0 * 6.0 / 5.0
+    out = orc.fused_add_rms_norm_nvfp4(x, res, w, 1e-5, gs)
+    for t in range(T):
+        ex = exact.exact_norm_row(x[t], res[t], w, 1e-5, STATIC, 0, 1.0, floor)
+        sf, v, codes = exact.exact_nvfp4(ex["y"], gs)
+        assert list(out["sf"][t]) == sf, t
+        lo, hi = out["q4"][t] & 0xF, out["q4"][t] >> 4
+        got = np.empty(H, np.int64)
+        got[0::2], got[1::2] = lo, hi
+        assert list(got) == codes, t
+        np.testing.assert_allclose(out["v"][t], [float(z) for z in v], rtol=1e-13)
+    assert out["sf"][1, 1] == 0 and np.all(out["q4"][1, 8:16] == 0)
+    gu = _rand_bf16(rng, (T, 2 * H), scale=2.0)
+    sout = orc.silu_mul_nvfp4(gu, 3.0)
+    for t in range(T):
+        ex = exact.exact_silu_row(gu[t], STATIC, 0, 1.0, floor)
+        sf, v, codes = exact.exact_nvfp4(ex["y"], 3.0)
+        got = np.empty(H, np.int64)
+        got[0::2], got[1::2] = sout["q4"][t] & 0xF, sout["q4"][t] >> 4
+        assert list(sout["sf"][t]) == sf and list(got) == codes, t
+
+
 # ------------------------------------- UE8M0 / column-major group scales
 
 UE8M0, COL_MAJOR = 0x100, 0x200
@@ -615,5 +687,5 @@ ALL_CHECKS = [
     check_silu_brute_force, check_silu_modes, check_rms_norm_bf16_closed_forms,
     check_rms_norm_bf16_invariants, check_rms_norm_bf16_brute_force, check_norm_pad,
     check_qk_norm_rope_rotations, check_qk_norm_rope_pairings, check_qk_norm_rope_brute_force,
-    check_group_scale_options,
+    check_group_scale_options, check_e2m1_codec, check_nvfp4_rows,
 ]

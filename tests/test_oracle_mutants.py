@@ -64,6 +64,15 @@ MUTANTS = {
                       "float s32 = dynamic_scale(amax);"),
     "ue8m0_wrong_floor": ("const double a = fmax(amax, orc_amax_floor());", "const double a = fmax(amax, 1e-8);"),
     "col_major_unpadded_stride": ("scale[g * ((T + 3) / 4 * 4) + t] = s32;", "scale[g * T + t] = s32;"),
+    "e2m1_ties_away": ("    double r = isinf(a) ? 6.0 : round_to_precision(a, 2, 0);",
+                       "    double r = isinf(a) ? 6.0 : ldexp(round(ldexp(a, 1)), -1);"),
+    "e2m1_max_4": ("    if (r > 6.0)\n        r = 6.0;", "    if (r > 4.0)\n        r = 4.0;"),
+    "nvfp4_block_scale_no_div6": ("uint8_t code = orc_e4m3_encode((double)gs * amax / 6.0);",
+                                  "uint8_t code = orc_e4m3_encode((double)gs * amax);"),
+    "nvfp4_nibbles_swapped": ("                q4[col / 2] = e;\n            else\n                q4[col / 2] = (uint8_t)(q4[col / 2] | (e << 4));",
+                              "                q4[col / 2] = (uint8_t)(e << 4);\n            else\n                q4[col / 2] = (uint8_t)(q4[col / 2] | e);"),
+    "nvfp4_global_scale_ignored": ("double vj = s > 0.0 ? yb[j] * (double)gs / s : 0.0;",
+                                   "double vj = s > 0.0 ? yb[j] / s : 0.0;"),
     "rope_sign": ("rot[a] = y[a] * c - y[b] * sn;", "rot[a] = y[a] * c + y[b] * sn;"),
     "rope_cos_sin_swapped": ("double c = (double)cs[i], sn = (double)cs[D / 2 + i];",
                              "double sn = (double)cs[i], c = (double)cs[D / 2 + i];"),
