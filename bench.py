@@ -65,6 +65,7 @@ STEPS.update({w.name: (w,) for w in gen.sweep()})
 STEPS.update({w.name: (w,) for w in gen.mla_workloads()})
 STEPS.update({w.name: (w,) for w in gen.pad_workloads()})
 STEPS.update({w.name: (w,) for w in gen.qk_workloads()})
+STEPS.update({w.name: (w,) for w in gen.nvfp4_workloads()})
 DEFAULT_STEP = "llama3_8b_decode"
 
 
@@ -88,6 +89,9 @@ def parse_args(argv=None):
     p.add_argument("--sweep", action="store_true",
                    help="instead of the step: time every point of the bandwidth sweep and the named "
                         "single-op configs, one JSON record per point")
+    p.add_argument("--sweep-filter", default=None,
+                   help="with --sweep: only points whose name contains one of these "
+                        "comma-separated substrings")
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -216,6 +220,10 @@ KERNEL_SOURCES = {
     "pad": [_CSRC + f for f in ("norm_fp8.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
                                 "tma.cuh", "vg_fused.cu")],
     "silu": [_CSRC + f for f in ("silu_fp8.cu", "common.cuh", "tma.cuh", "vg_fused.cu")],
+    "norm4": [_CSRC + f for f in ("norm_fp8.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
+                                  "nvfp4.cuh", "tma.cuh", "vg_fused.cu")],
+    "silu4": [_CSRC + f for f in ("silu_fp8.cu", "common.cuh", "nvfp4.cuh", "tma.cuh",
+                                  "vg_fused.cu")],
     "mla": [_CSRC + f for f in ("mla_norm.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
                                 "vg_fused.cu")],
     "qk": [_CSRC + f for f in ("qk_norm_rope.cu", "row_norm.cuh", "common.cuh", "vg_fused.cu")],
@@ -268,6 +276,20 @@ class DeviceSet:
                 q = torch.empty((w.T, w.n), dtype=torch.uint8, device=dev)
                 scale = self._scale(torch, w, dev)
                 self.ops.append(dict(w=w, q=q, res=res, scale=scale, x=x, weight=weights[w.name]))
+            elif w.op == "norm4":
+                x = torch.from_numpy(h["x"].view(np.int16)).to(dev)
+                res = torch.from_numpy(h["residual"].view(np.int16)).to(dev)
+                q4 = torch.empty((w.T, w.n // 2), dtype=torch.uint8, device=dev)
+                sf = torch.empty((w.T, w.n // 16), dtype=torch.uint8, device=dev)
+                gs = torch.full((1,), w.static_scale, dtype=torch.float32, device=dev)
+                self.ops.append(dict(w=w, q4=q4, sf=sf, gs=gs, res=res, x=x,
+                                     weight=weights[w.name]))
+            elif w.op == "silu4":
+                gu = torch.from_numpy(h["gate_up"].view(np.int16)).to(dev)
+                q4 = torch.empty((w.T, w.n // 2), dtype=torch.uint8, device=dev)
+                sf = torch.empty((w.T, w.n // 16), dtype=torch.uint8, device=dev)
+                gs = torch.full((1,), w.static_scale, dtype=torch.float32, device=dev)
+                self.ops.append(dict(w=w, q4=q4, sf=sf, gs=gs, gate_up=gu))
             elif w.op == "qk":
                 qkv = torch.from_numpy(h["qkv"].view(np.int16)).to(dev)
                 pos = torch.from_numpy(h["positions"]).to(dev)
@@ -310,7 +332,7 @@ def device_weights(torch, step, host, dev):
     """Each op's weights on the device, shared by all buffer sets."""
     out = {}
     for w, h in zip(step, host):
-        if w.op in ("norm", "pad"):
+        if w.op in ("norm", "pad", "norm4"):
             out[w.name] = torch.from_numpy(h["weight"].view(np.int16)).to(dev)
         elif w.op == "mla":
             out[w.name] = tuple(torch.from_numpy(h[k].view(np.int16)).to(dev)
@@ -329,6 +351,11 @@ def launch(vg, op):
                                      op["weight"], w.eps, w.mode, w.group_size)
     elif w.op == "pad":
         vg.vg_fused_add_rms_norm_pad(op["out"], op["res"], op["x"], op["res"], op["weight"], w.eps)
+    elif w.op == "norm4":
+        vg.vg_fused_add_rms_norm_nvfp4(op["q4"], op["sf"], op["res"], op["x"], op["res"],
+                                       op["weight"], op["gs"], w.eps)
+    elif w.op == "silu4":
+        vg.vg_silu_mul_nvfp4(op["q4"], op["sf"], op["gate_up"], op["gs"])
     elif w.op == "qk":
         vg.vg_fused_qk_norm_rope(op["qkv"], op["q_weight"], op["k_weight"], op["cache"], op["pos"],
                                  w.hq, w.hkv, w.n, w.eps, w.mode == 1)
@@ -490,6 +517,8 @@ def mode_name(w):
         return f"bf16_padded_to_{w.n2}"
     if w.op == "mla":
         return "q_fp8_per_token" if w.mode == gen.PER_TOKEN else "bf16"
+    if w.op in ("norm4", "silu4"):
+        return f"nvfp4_gs{w.static_scale:g}"
     return gen.MODE_NAMES[w.mode]
 
 
@@ -666,6 +695,13 @@ def oracle_step_runner(step, host, threads):
                                             h["k_weight"], h["cos_sin_cache"],
                                             h["positions"][r0:r1], w.hq, w.hkv, w.n, w.eps,
                                             w.mode == 1, False))
+                elif w.op == "norm4":
+                    futs.append(pool.submit(orc.fused_add_rms_norm_nvfp4, h["x"][r0:r1],
+                                            h["residual"][r0:r1], h["weight"], w.eps,
+                                            w.static_scale, False))
+                elif w.op == "silu4":
+                    futs.append(pool.submit(orc.silu_mul_nvfp4, h["gate_up"][r0:r1],
+                                            w.static_scale, False))
                 elif w.op == "pad":
                     futs.append(pool.submit(orc.fused_add_rms_norm_pad, h["x"][r0:r1],
                                             h["residual"][r0:r1], h["weight"], w.eps, w.n2, False))
@@ -787,7 +823,9 @@ def run_sweep(args):
     stream = torch.cuda.Stream(device=dev)
     cache = {}
     for w in (list(gen.NAMED.values()) + gen.sweep() + gen.mla_workloads() + gen.pad_workloads()
-              + gen.qk_workloads()):
+              + gen.qk_workloads() + gen.nvfp4_workloads()):
+        if args.sweep_filter and not any(f in w.name for f in args.sweep_filter.split(",")):
+            continue
         key = (w.op, w.T, w.n, w.n2, w.x_dist)
         if key not in cache:
             cache.clear()

@@ -130,7 +130,7 @@ def qk_inputs(T: int, hq: int, hkv: int, head_dim: int, max_pos: int, seed: int 
 class Workload:
     """One op invocation: which op, its shape, scale mode and inputs."""
     name: str
-    op: str                  # "norm", "silu", "mla", "pad" or "qk"
+    op: str                  # "norm", "silu", "mla", "pad", "qk"; NVFP4 "norm4", "silu4"
     T: int
     n: int                   # hidden (norm), intermediate (silu) or q_dim (mla)
     mode: int                # mla: PER_TOKEN = q to fp8, STATIC = bf16 q
@@ -140,14 +140,14 @@ class Workload:
     max_pos: int = 0         # qk: rows of the cos/sin cache
     group_size: int = 128
     eps: float = 1e-5
-    static_scale: float = 0.05
+    static_scale: float = 0.05   # static fp8 scale; NVFP4: the per-tensor scale gs
     x_dist: str = "normal"
     residual: bool = True
     seed: int = 0
     note: str = field(default="", compare=False)
 
     def inputs(self):
-        if self.op in ("norm", "pad"):
+        if self.op in ("norm", "pad", "norm4"):
             return norm_inputs(self.T, self.n, self.seed, self.x_dist)
         if self.op == "mla":
             return mla_inputs(self.T, self.n, self.n2, self.seed)
@@ -158,6 +158,11 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """Bytes the op must move: every row read once and written once; the
         weight and a static scale read once per launch."""
+        if self.op == "norm4":  # x, residual in; residual_out, E2M1 codes, E4M3 block scales out
+            per_row = (6 if self.residual else 2) * self.n + self.n // 2 + self.n // 16
+            return self.T * per_row + 2 * self.n + 4
+        if self.op == "silu4":
+            return self.T * (4 * self.n + self.n // 2 + self.n // 16) + 4
         s_row = {STATIC: 0, PER_TOKEN: 4, PER_GROUP: 4 * (self.n // self.group_size)}[self.mode]
         s0 = 4 if self.mode == STATIC else 0
         if self.op == "norm":
@@ -221,6 +226,20 @@ def mla_workloads():
     return [Workload(f"mla_dual_{'fp8' if m == PER_TOKEN else 'bf16'}_{T}x{MLA_Q_DIM}_{MLA_KV_DIM}",
                      "mla", T, MLA_Q_DIM, m, n2=MLA_KV_DIM, eps=1e-6)
             for m in (STATIC, PER_TOKEN) for T in MLA_T]
+
+
+# NVFP4 outputs of both fusions at Llama-3-70B's sizes (hidden 8192,
+# intermediate 28672).  gs = 448 * 6 / 16, the per-tensor scale of a tensor
+# whose amax is 16.
+NVFP4_H, NVFP4_I, NVFP4_GS = 8192, 28672, 168.0
+NVFP4_T = (1, 64, 512, 4096, 32768)
+
+
+def nvfp4_workloads():
+    return ([Workload(f"norm_nvfp4_{T}x{NVFP4_H}", "norm4", T, NVFP4_H, PER_GROUP, group_size=16,
+                      eps=1e-5, static_scale=NVFP4_GS) for T in NVFP4_T]
+            + [Workload(f"silu_nvfp4_{T}x{NVFP4_I}", "silu4", T, NVFP4_I, PER_GROUP, group_size=16,
+                        static_scale=NVFP4_GS) for T in NVFP4_T])
 
 
 SWEEP_T = (1, 8, 64, 512, 4096, 32768)

@@ -66,7 +66,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *vg_stream_t;
 
-#define VG_ABI_VERSION 2
+#define VG_ABI_VERSION 3
 #define VG_MAX_ROW 32768 /* largest hidden / inter a row-resident kernel holds */
 
 typedef enum {
@@ -143,6 +143,37 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
 vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up,
                           int64_t num_tokens, int64_t inter, int32_t mode,
                           int32_t group_size, vg_stream_t stream);
+
+/*
+ * NVFP4 outputs of both fusions.  The "Quick Reference" table names FP4 as an
+ * output of "RMSNorm + Quantization" and of "SiLU+Mul + Quantization" and the
+ * "Support Matrix" lists NVFP4 dynamic quantisation on sm100 and later; the
+ * pages define neither, so the library takes NVIDIA's public NVFP4 format:
+ *   elements  E2M1 (OCP Microscaling FP4: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}),
+ *             RNE, saturating at 6; two a byte, column 2i in the low nibble
+ *   blocks    16 consecutive columns of a row, one E4M3 code each:
+ *             sf = e4m3(gs * amax / 6), amax over the block's y (or a)
+ *   elements  q = e2m1(y * gs / decode(sf)); a block with sf == 0 gives +0
+ *   gs        the fp32 per-tensor scale, read from device memory
+ * The block code is the one the exact gs * amax / 6 rounds to.  Element codes
+ * differ from the exact value's only where it lies within ~2^-19 (relative)
+ * of an E2M1 midpoint, by one code.
+ *
+ *   q4            out uint8 [T, H/2] (or [T, I/2])  packed E2M1 codes
+ *   block_scale   out uint8 [T, H/16] (or [T, I/16]) E4M3 codes, row-major
+ *   global_scale  in  fp32 [1], device, > 0 and finite
+ *   the other arguments as for vg_fused_add_rms_norm_fp8 / vg_silu_mul_fp8;
+ *   the row length must be a multiple of 16 (else VG_ERR_BAD_SHAPE).
+ *   block_scale has no alignment rule; global_scale must be 4-byte aligned.
+ */
+vg_status vg_fused_add_rms_norm_nvfp4(uint8_t *q4, uint8_t *block_scale, uint16_t *residual_out,
+                                      const uint16_t *x, const uint16_t *residual,
+                                      const uint16_t *weight, const float *global_scale,
+                                      int64_t num_tokens, int64_t hidden, float eps,
+                                      vg_stream_t stream);
+vg_status vg_silu_mul_nvfp4(uint8_t *q4, uint8_t *block_scale, const uint16_t *gate_up,
+                            const float *global_scale, int64_t num_tokens, int64_t inter,
+                            vg_stream_t stream);
 
 /*
  * Residual add + RMSNorm into a padded bf16 row ("RMSNorm + Padding

@@ -19,11 +19,16 @@ Entry points (same names and argument order as the C ABI):
   vg_fused_mla_dual_rms_norm_per_token_quant(q_fp8, q_scale, kv_out, q_c,
                              q_weight, kv_c, kv_weight, eps_q, eps_kv, stream=None)
   (the MLA inputs may be column-slice views: their row stride is passed on)
+  vg_fused_add_rms_norm_nvfp4(q4, block_scale, residual_out, x, residual, weight,
+                              global_scale, eps, stream=None)
+  vg_silu_mul_nvfp4(q4, block_scale, gate_up, global_scale, stream=None)
 Convenience wrappers that allocate the outputs with torch:
   fused_add_rms_norm_fp8(x, residual, weight, eps, mode, ...)
   silu_mul_fp8(gate_up, mode, ...)
   fused_add_rms_norm_pad(x, residual, weight, eps, padded_hidden, ...)
   mla_dual_rms_norm(q_c, q_weight, kv_c, kv_weight, eps_q, eps_kv, q_fp8=False)
+  fused_add_rms_norm_nvfp4(x, residual, weight, eps, global_scale, ...)
+  silu_mul_nvfp4(gate_up, global_scale, ...)
 """
 from __future__ import annotations
 
@@ -44,7 +49,8 @@ STATUS_NAMES = {
 
 EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_fused_add_rms_norm_pad",
                     "vg_fused_mla_dual_rms_norm", "vg_fused_qk_norm_rope",
-                    "vg_fused_mla_dual_rms_norm_per_token_quant", "vg_device_status",
+                    "vg_fused_mla_dual_rms_norm_per_token_quant", "vg_fused_add_rms_norm_nvfp4",
+                    "vg_silu_mul_nvfp4", "vg_device_status",
                     "vg_status_string", "vg_abi_version")
 DEVICE_WAIT_TIMEOUT = 1
 DEVICE_BAD_POSITION = 2
@@ -90,6 +96,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.vg_fused_mla_dual_rms_norm_per_token_quant.argtypes = [P, P, P, P, i64, P, P, i64, P,
                                                                    i64, i64, i64, f32, f32, P]
         lib.vg_fused_mla_dual_rms_norm_per_token_quant.restype = ctypes.c_int
+        lib.vg_fused_add_rms_norm_nvfp4.argtypes = [P, P, P, P, P, P, P, i64, i64, f32, P]
+        lib.vg_fused_add_rms_norm_nvfp4.restype = ctypes.c_int
+        lib.vg_silu_mul_nvfp4.argtypes = [P, P, P, P, i64, i64, P]
+        lib.vg_silu_mul_nvfp4.restype = ctypes.c_int
         lib.vg_status_string.argtypes = [ctypes.c_int]
         lib.vg_status_string.restype = ctypes.c_char_p
         lib.vg_abi_version.argtypes = []
@@ -270,6 +280,45 @@ def vg_fused_mla_dual_rms_norm_per_token_quant(q_fp8, q_scale, kv_out, q_c, q_we
         T, q_dim, kv_dim, ctypes.c_float(eps_q), ctypes.c_float(eps_kv), _stream(stream)))
 
 
+def vg_fused_add_rms_norm_nvfp4(q4, block_scale, residual_out, x, residual, weight,
+                                global_scale, eps: float, stream=None,
+                                num_tokens: int | None = None, hidden: int | None = None):
+    """Residual add + RMSNorm -> NVFP4 through the C ABI (outputs preallocated).
+
+    q4 [T,H/2] uint8 (two E2M1 codes a byte, column 2i in the low nibble);
+    block_scale [T,H/16] uint8 E4M3 codes; residual_out as for the FP8 op;
+    global_scale fp32 [1] on the device."""
+    import torch
+    bf16, fp8, f32 = _dtypes()
+    u8 = (torch.uint8,)
+    if num_tokens is None or hidden is None:
+        num_tokens, hidden = _rows(x, "x")
+    _check(load().vg_fused_add_rms_norm_nvfp4(
+        _ptr(q4, u8, "q4"), _ptr(block_scale, fp8, "block_scale"),
+        _ptr(residual_out, bf16, "residual_out"), _ptr(x, bf16, "x"),
+        _ptr(residual, bf16, "residual"), _ptr(weight, bf16, "weight"),
+        _ptr(global_scale, f32, "global_scale"), num_tokens, hidden, ctypes.c_float(eps),
+        _stream(stream)))
+
+
+def vg_silu_mul_nvfp4(q4, block_scale, gate_up, global_scale, stream=None,
+                      num_tokens: int | None = None, inter: int | None = None):
+    """SiLU(gate) * up -> NVFP4 through the C ABI: q4 [T,I/2] uint8,
+    block_scale [T,I/16] E4M3 codes, gate_up [T,2I] bf16, global_scale fp32
+    [1] on the device."""
+    import torch
+    bf16, fp8, f32 = _dtypes()
+    if num_tokens is None or inter is None:
+        num_tokens, two_i = _rows(gate_up, "gate_up")
+        if two_i % 2:
+            raise ValueError("gate_up must have an even number of columns")
+        inter = two_i // 2
+    _check(load().vg_silu_mul_nvfp4(
+        _ptr(q4, (torch.uint8,), "q4"), _ptr(block_scale, fp8, "block_scale"),
+        _ptr(gate_up, bf16, "gate_up"), _ptr(global_scale, f32, "global_scale"), num_tokens,
+        inter, _stream(stream)))
+
+
 def vg_device_status(reset: bool = False) -> int:
     """Flags the library's kernels left on the current device
     (DEVICE_WAIT_TIMEOUT: a bounded wait gave up; that call's outputs are
@@ -349,3 +398,28 @@ def fused_add_rms_norm_pad(x, residual, weight, eps: float, padded_hidden: int,
         r_out = residual if inplace else torch.empty_like(residual)
     vg_fused_add_rms_norm_pad(out, r_out, x, residual, weight, eps, stream)
     return out, r_out
+
+
+def fused_add_rms_norm_nvfp4(x, residual, weight, eps: float, global_scale, inplace: bool = True,
+                             stream=None):
+    """Returns (q4 uint8 [T,H/2], block_scale float8_e4m3fn [T,H/16],
+    residual_out); global_scale is an fp32 [1] device tensor."""
+    import torch
+    T, H = x.shape
+    q4 = torch.empty((T, H // 2), dtype=torch.uint8, device=x.device)
+    sf = torch.empty((T, H // 16), dtype=torch.float8_e4m3fn, device=x.device)
+    r_out = None
+    if residual is not None:
+        r_out = residual if inplace else torch.empty_like(residual)
+    vg_fused_add_rms_norm_nvfp4(q4, sf, r_out, x, residual, weight, global_scale, eps, stream)
+    return q4, sf, r_out
+
+
+def silu_mul_nvfp4(gate_up, global_scale, stream=None):
+    """Returns (q4 uint8 [T,I/2], block_scale float8_e4m3fn [T,I/16])."""
+    import torch
+    T, two_i = gate_up.shape
+    q4 = torch.empty((T, two_i // 4), dtype=torch.uint8, device=gate_up.device)
+    sf = torch.empty((T, two_i // 32), dtype=torch.float8_e4m3fn, device=gate_up.device)
+    vg_silu_mul_nvfp4(q4, sf, gate_up, global_scale, stream)
+    return q4, sf

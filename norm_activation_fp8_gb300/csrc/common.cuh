@@ -90,6 +90,10 @@ __device__ __forceinline__ void st_stream(void *p, uint2 v) {
   asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+__device__ __forceinline__ void st_stream(void *p, uint32_t v) {
+  asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // --------------------------------------------------------------- reductions
 
 // Butterfly reductions: every participating lane ends with the bit-identical

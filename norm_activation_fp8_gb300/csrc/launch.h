@@ -10,7 +10,8 @@ namespace vg {
 // norm's bf16 output into a padded row (no quantisation); kPerGroupX is
 // per-group with scale options (UE8M0 scales and/or the column-major
 // layout), kept apart so that plain per-group code stays as it is.
-enum ScaleMode : int { kStatic = 0, kPerToken = 1, kPerGroup = 2, kBf16Pad = 3, kPerGroupX = 4 };
+enum ScaleMode : int { kStatic = 0, kPerToken = 1, kPerGroup = 2, kBf16Pad = 3, kPerGroupX = 4,
+                       kNvfp4 = 5 /* E2M1 codes, E4M3 scales per 16 columns */ };
 
 // How a row-wise kernel covers a [T, n] tensor: each row is split into
 // nch = n/8 chunks of 16 bytes; `ntr` threads (a multiple of 32) own a row,
@@ -57,6 +58,7 @@ struct NormArgs {
   int32_t s_ts;
   int32_t s_gs;
   int32_t ue8m0;
+  uint8_t *sf8;    // kNvfp4: E4M3 block scale codes [T, H/16]; q holds [T, H/2]
 };
 
 struct SiluArgs {
@@ -73,6 +75,7 @@ struct SiluArgs {
   int32_t s_ts;    // per-group scale (t, g) at scale[t * s_ts + g * s_gs]
   int32_t s_gs;
   int32_t ue8m0;   // power-of-two per-group scales
+  uint8_t *sf8;    // kNvfp4: E4M3 block scale codes [T, I/16]; q holds [T, I/2]
 };
 
 cudaError_t launch_norm_fp8(NormArgs a, int mode, const RowPlan &plan, cudaStream_t stream);

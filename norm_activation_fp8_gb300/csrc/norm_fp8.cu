@@ -35,6 +35,7 @@
 #include "common.cuh"
 #include "dyn_scale.cuh"
 #include "launch.h"
+#include "nvfp4.cuh"
 #include "row_norm.cuh"
 #include "tma.cuh"
 
@@ -51,7 +52,7 @@ namespace {
 struct RowSmem {
   float4 *red;    // [2][16] per-warp partials, double-buffered by row parity
   float *cmax;    // [rpc][ntr * VPT] chunk amax (per-group)
-  DynScale *dyn;  // [rpc][nslots]
+  DynScale *dyn;  // [rpc][nslots]; NVFP4 keeps float2 {s, gs * inv / s} per block
 };
 
 // Row reduction, scales and pass 2 (quantise + store q).  Called by every
@@ -94,7 +95,7 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
   // by the slot's thread, from the warp partials and chunk amaxes.  The bf16
   // output has one slot per row holding inv = y + dy.
   const int row_chunks = a.ntr * VPT;
-  constexpr bool PG = MODE == kPerGroup || MODE == kPerGroupX;
+  constexpr bool PG = MODE == kPerGroup || MODE == kPerGroupX || MODE == kNvfp4;
   const int nslots = PG ? a.ngroups : 1;
   float hi = acc.ss.x, lo = acc.lo.x + acc.lo.y;
   two_sum_acc(hi, lo, acc.ss.y);
@@ -122,6 +123,32 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
     rsqrt_df(h, l, (float)a.H, a.inv_h, a.eps, y, dy);
     if (MODE == kBf16Pad) {
       sm.dyn[slot] = DynScale{y, dy, 0.f, 0.f};
+    } else if (MODE == kNvfp4) {
+      // a block scale for every 16 columns: more blocks than threads when a
+      // thread holds more than two chunks.  x = amax * (y gs / 6) in fp32 is
+      // within 2^-22 of X = gs * amax * inv / 6; a block whose x lies near an
+      // E4M3 midpoint gets the code of X in double-float.
+      const float gs = __ldg(a.scale);
+      const float ygs = y * gs, ygs6 = ygs * (1.0f / 6.0f);
+      for (int g = lr; g < nslots; g += a.ntr) {
+        float bm = 0.f;
+#pragma unroll
+        for (int i = 0; i < GCH; ++i) bm = fmaxf(bm, sm.cmax[slot * row_chunks + g * GCH + i]);
+        const uint32_t code = e4m3_code_settled(bm * ygs6, [&] {
+          // amax * gs exactly, times y + dy, then a division by 6 with its
+          // exact remainder
+          const float p = bm * gs, pe = fmaf(bm, gs, -p);
+          const float xh = p * y, xl = fmaf(p, y, -xh) + (p * dy + pe * y);
+          const float qh = __fdiv_rn(xh, 6.0f);
+          const float ql = __fdiv_rn(fmaf(-qh, 6.0f, xh) + xl, 6.0f);
+          const float qs = qh + ql;
+          return e4m3_code_df(qs, ql - (qs - qh));
+        });
+        const float sv = e4m3_value(code);
+        if (live) a.sf8[row * nslots + g] = (uint8_t)code;
+        reinterpret_cast<float2 *>(sm.dyn)[slot * nslots + g] =
+            make_float2(sv, sv > 0.f ? ygs * __frcp_rn(sv) : 0.f);
+      }
     } else {
       if (PG) {
         amr = 0.f;
@@ -140,6 +167,25 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
     }
   }
   __syncthreads();
+  if (MODE == kNvfp4) {  // v = t * y * gs / s, E2M1 codes; a zero scale gives +0 codes
+    uint8_t *out = a.q + (live ? row * (int64_t)(a.H / 2) : 0);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int c = lr + k * a.ntr;
+      const float2 d = reinterpret_cast<const float2 *>(sm.dyn)[slot * nslots + (c >= a.nch ? 0 : c / GCH)];
+      const float2 m2 = make_float2(d.y, d.y);
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 q = f2_mul(t[k][i], m2);
+        v[2 * i] = q.x;
+        v[2 * i + 1] = q.y;
+      }
+      const uint32_t codes = quant_e2m1x8(v) & (d.x > 0.f ? 0xFFFFFFFFu : 0u);  // +0 codes
+      if (live && c < a.nch) st_stream(out + c * 4, codes);
+    }
+    return;
+  }
   if (MODE == kBf16Pad) {
     const DynScale d = sm.dyn[slot];  // s = y, a = dy
     uint16_t *out = a.out16 + (live ? row * (int64_t)a.nch_pad * kElemsPerChunk : 0);
@@ -181,6 +227,14 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
 }
 
 __host__ __device__ inline size_t align128(size_t x) { return (x + 127) & ~size_t(127); }
+
+// DynScale-sized entries a row needs for its scales (NVFP4's float2 pairs
+// take half an entry each).
+__host__ __device__ inline int scale_slots(int mode, int ngroups) {
+  return mode == kStatic ? 0
+                         : (mode == kPerGroup || mode == kPerGroupX ? ngroups
+                                                                    : (mode == kNvfp4 ? (ngroups + 1) / 2 : 1));
+}
 
 // Dynamic shared memory of the row logic: red, cmax, dyn.
 __host__ __device__ inline size_t row_smem_bytes(int block, int vpt, int slots) {
@@ -260,7 +314,7 @@ template <int VPT, int MODE, int GCH, bool RES>
 __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, const int stages) {
   constexpr bool DYN = MODE != kStatic;
   extern __shared__ __align__(128) unsigned char dsm[];
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup || MODE == kPerGroupX ? a.ngroups : 1);
+  const int slots = scale_slots(MODE, a.ngroups);
   const TmaLayout L(a.H, RES, stages, blockDim.x, VPT, slots);
   const RowSmem sm = carve_row_smem(dsm + L.row_off, blockDim.x, VPT);
   unsigned char *wbuf = dsm + L.w_off;
@@ -343,7 +397,7 @@ __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, con
 
 template <int VPT, int MODE, int GCH>
 cudaError_t launch_res(const NormArgs &a, const RowPlan &p, cudaStream_t s) {
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup || MODE == kPerGroupX ? a.ngroups : 1) * p.rpc;
+  const int slots = scale_slots(MODE, a.ngroups) * p.rpc;
   const size_t smem = row_smem_bytes(p.block(), VPT, slots);
   if (a.res != nullptr)
     norm_fp8_kernel<VPT, MODE, GCH, true><<<(unsigned)p.grid, p.block(), smem, s>>>(a);
@@ -354,7 +408,7 @@ cudaError_t launch_res(const NormArgs &a, const RowPlan &p, cudaStream_t s) {
 
 template <int VPT, int MODE, int GCH, bool RES>
 cudaError_t launch_tma_res(const NormArgs &a, const TmaPlan &p, cudaStream_t s) {
-  const int slots = MODE == kStatic ? 0 : (MODE == kPerGroup || MODE == kPerGroupX ? a.ngroups : 1);
+  const int slots = scale_slots(MODE, a.ngroups);
   const TmaLayout L(a.H, RES, p.stages, p.block, VPT, slots);
   auto kern = norm_fp8_tma_kernel<VPT, MODE, GCH, RES>;
   // opt in to large dynamic shared memory once per instantiation and device
@@ -384,6 +438,7 @@ cudaError_t launch_mode(const NormArgs &a, int mode, const RowPlan &p, cudaStrea
     case kStatic: return launch_res<VPT, kStatic, 1>(a, p, s);
     case kPerToken: return launch_res<VPT, kPerToken, 1>(a, p, s);
     case kBf16Pad: return launch_res<VPT, kBf16Pad, 1>(a, p, s);
+    case kNvfp4: return launch_res<VPT, kNvfp4, 2>(a, p, s);
     default:
       if (a.ue8m0 || a.s_gs != 1)
         return a.gch == 8 ? launch_res<VPT, kPerGroupX, 8>(a, p, s)
@@ -400,6 +455,7 @@ cudaError_t launch_tma_vpt(const NormArgs &a, int mode, const TmaPlan &p, cudaSt
   switch (mode) {
     case kPerToken: return launch_tma_mode<VPT, kPerToken, 1>(a, p, s);
     case kBf16Pad: return launch_tma_mode<VPT, kBf16Pad, 1>(a, p, s);
+    case kNvfp4: return launch_tma_mode<VPT, kNvfp4, 2>(a, p, s);
     default:
       if (a.ue8m0 || a.s_gs != 1)
         return a.gch == 8 ? launch_tma_mode<VPT, kPerGroupX, 8>(a, p, s)

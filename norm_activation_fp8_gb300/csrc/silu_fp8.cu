@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "nvfp4.cuh"
 #include "tma.cuh"
 
 namespace vg {
@@ -110,6 +111,46 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
   return m;
 }
 
+// Rewrites one NVFP4 block whose fp32 value gs * amax / 6 lay near an E4M3
+// midpoint, with the code the exact value rounds to; called by the whole warp
+// after its fast stores (so little is live across the call), `near` the same
+// in both lanes of a block.  The lane reloads its chunk c of the row; only
+// candidates for the block's maximum go to fp64: an element whose fp32 |a|
+// is below am (1 - 2^-15) (am the fp32 block amax; both carry under 2^-19 of
+// error) cannot be it.
+__device__ __noinline__ void nvfp4_silu_settle(const uint16_t *gate_up, uint8_t *q4, uint8_t *sf,
+                                               int32_t I, int64_t row, int c, float gs, bool near) {
+  uint4 gv = make_uint4(0, 0, 0, 0), uv = gv;
+  if (near) {
+    gv = ld_stream_ro(gate_up + row * 2 * I + c * kElemsPerChunk);
+    uv = ld_stream_ro(gate_up + row * 2 * I + I + c * kElemsPerChunk);
+  }
+  float v[8];
+  silu_chunk(gv, uv, v);
+  const float am = lanes_max(amax8(v), 2);
+  double m = 0.0;
+  if (near) {
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    const float cut = am * (1.0f - 1.0f / 32768.0f);
+#pragma unroll 1
+    for (int i = 0; i < 4; ++i) {
+      const float2 g = bf16x2_to_f2(gw[i]), u = bf16x2_to_f2(uw[i]);
+      if (fabsf(v[2 * i]) >= cut) m = fmax(m, fabs((double)g.x / (1.0 + exp(-(double)g.x)) * (double)u.x));
+      if (fabsf(v[2 * i + 1]) >= cut) m = fmax(m, fabs((double)g.y / (1.0 + exp(-(double)g.y)) * (double)u.y));
+    }
+  }
+  m = fmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  if (!near) return;
+  const double x = (double)gs * m / (double)kE2M1Max;
+  const float xh = (float)x;
+  const uint32_t code = e4m3_code_df(xh, (float)(x - (double)xh));
+  const float sv = e4m3_value(code);
+  scale8(v, sv > 0.f ? gs * fast_rcp(sv) : 0.f);
+  if ((c & 1) == 0) sf[row * (int64_t)(I / kNvfp4Block) + c / 2] = (uint8_t)code;
+  st_stream(q4 + row * (int64_t)(I / 2) + c * 4, quant_e2m1x8(v) & (sv > 0.f ? 0xFFFFFFFFu : 0u));
+}
+
 // A row is covered by ntr * VPT chunks per CTA.  Static and per-group modes
 // keep no row state, so longer rows are split into column segments
 // (blockIdx.y), independent CTAs.  Per-token needs the amax of the whole row
@@ -148,6 +189,40 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
     }
   }
 
+  if constexpr (MODE == kNvfp4) {
+    // 16-column blocks = chunk pairs (2b, 2b + 1), held by lanes lr, lr ^ 1.
+    // x = gs * amax / 6 in fp32 is within ~2^-19 of the exact value (the
+    // activations' error); where x(1 - 2^-17) and x(1 + 2^-17) round to
+    // different E4M3 codes the block is settled in fp64 after the loop, so
+    // that its code is the exact value's.
+    const float gs = __ldg(a.scale);
+    const float gs6 = gs * (1.0f / kE2M1Max);
+    uint8_t *out = a.q + (live ? row * (int64_t)(a.I / 2) : 0);
+    uint32_t near_k = 0;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int c = lr + k * a.ntr;
+      float v[8];
+      silu_chunk(gv[k], uv[k], v);
+      const float am = lanes_max(amax8(v), 2);
+      const float x = am * gs6;
+      const uint32_t cc = cvt_e4m3x2(x * (1.0f - 1.0f / 131072.0f), x * (1.0f + 1.0f / 131072.0f));
+      const uint32_t code = cc & 0xFFu;
+      if ((cc >> 8) != code) near_k |= 1u << k;
+      const float sv = e4m3_value(code);
+      scale8(v, sv > 0.f ? gs * fast_rcp(sv) : 0.f);
+      const uint32_t codes = quant_e2m1x8(v) & (sv > 0.f ? 0xFFFFFFFFu : 0u);  // +0 codes
+      if (live && c < a.nch) {
+        if ((c & 1) == 0) a.sf8[row * (int64_t)(a.I / kNvfp4Block) + c / 2] = (uint8_t)code;
+        st_stream(out + c * 4, codes);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+      if (__any_sync(0xFFFFFFFFu, (near_k >> k) & 1u))
+        nvfp4_silu_settle(a.gate_up, a.q, a.sf8, a.I, row, lr + k * a.ntr, gs, (near_k >> k) & 1u);
+    return;
+  }
   if (MODE != kPerToken) {
     const float inv_static = (MODE == kStatic) ? __frcp_rn(__ldg(a.scale)) : 0.f;
 #pragma unroll
@@ -345,6 +420,10 @@ cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStrea
   const dim3 g((unsigned)p.grid, (unsigned)p.segs), b((unsigned)p.block());
   switch (mode) {
     case kStatic: silu_fp8_kernel<VPT, kStatic, 1, false><<<g, b, 0, s>>>(a); break;
+    case kNvfp4:  // the per-group plan: at most two chunks a thread
+      if constexpr (VPT <= 2) silu_fp8_kernel<VPT, kNvfp4, 2, false><<<g, b, 0, s>>>(a);
+      else return cudaErrorInvalidConfiguration;
+      break;
     case kPerToken:
       if (p.block() > 512)
         silu_fp8_kernel<VPT, kPerToken, 1, true><<<g, b, 0, s>>>(a);

@@ -332,6 +332,55 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
                                                                                    : VG_ERR_CUDA;
 }
 
+vg_status vg_fused_add_rms_norm_nvfp4(uint8_t *q4, uint8_t *block_scale, uint16_t *residual_out,
+                                      const uint16_t *x, const uint16_t *residual,
+                                      const uint16_t *weight, const float *global_scale,
+                                      int64_t num_tokens, int64_t hidden, float eps,
+                                      vg_stream_t stream) {
+  vg_status st = vg::check_row(num_tokens, hidden, VG_SCALE_PER_TOKEN, 0);
+  if (st != VG_OK) return st;
+  if (hidden % 16 != 0) return VG_ERR_BAD_SHAPE;
+  if (num_tokens == 0) return VG_OK;
+  if (!q4 || !block_scale || !x || !weight || !global_scale ||
+      ((residual == nullptr) != (residual_out == nullptr)))
+    return VG_ERR_NULL_PTR;
+  if (vg::misaligned(q4, 16) || vg::misaligned(x, 16) || vg::misaligned(weight, 16) ||
+      vg::misaligned(residual, 16) || vg::misaligned(residual_out, 16) ||
+      vg::misaligned(global_scale, 4))
+    return VG_ERR_MISALIGNED;
+  int sms = 0;
+  if ((st = vg::check_device(&sms)) != VG_OK) return st;
+  vg::clear_stale_error();
+
+  vg::NormArgs a{};
+  a.q = q4;
+  a.sf8 = block_scale;
+  a.res_out = residual_out;
+  a.scale = const_cast<float *>(global_scale);  // read only in this mode
+  a.x = x;
+  a.res = residual;
+  a.w = weight;
+  a.T = num_tokens;
+  a.H = (int32_t)hidden;
+  a.nch = (int32_t)(hidden / 8);
+  a.gch = 2;
+  a.ngroups = (int32_t)(hidden / 16);
+  a.eps = eps;
+  a.inv_h = 1.0f / (float)hidden;
+  vg::set_scale_layout(a, VG_SCALE_PER_TOKEN, num_tokens);
+  // the dynamic norm's plans; the block scales take half a DynScale each
+  vg::TmaPlan tp;
+  if (vg::plan_norm_tma(num_tokens, (int)hidden, residual != nullptr, vg::kNvfp4,
+                        (a.ngroups + 1) / 2, sms, &tp))
+    return vg::launch_norm_fp8_tma(a, vg::kNvfp4, tp, (cudaStream_t)stream) == cudaSuccess
+               ? VG_OK
+               : VG_ERR_CUDA;
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, 4, sms);
+  return vg::launch_norm_fp8(a, vg::kNvfp4, plan, (cudaStream_t)stream) == cudaSuccess
+             ? VG_OK
+             : VG_ERR_CUDA;
+}
+
 vg_status vg_fused_add_rms_norm_pad(uint16_t *out, uint16_t *residual_out, const uint16_t *x,
                                     const uint16_t *residual, const uint16_t *weight,
                                     int64_t num_tokens, int64_t hidden, int64_t padded_hidden,
@@ -446,6 +495,38 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
   const vg::RowPlan plan = vg::plan_silu(num_tokens, a.nch, mode, sms);
   return vg::launch_silu_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                  : VG_ERR_CUDA;
+}
+
+vg_status vg_silu_mul_nvfp4(uint8_t *q4, uint8_t *block_scale, const uint16_t *gate_up,
+                            const float *global_scale, int64_t num_tokens, int64_t inter,
+                            vg_stream_t stream) {
+  vg_status st = vg::check_row(num_tokens, inter, VG_SCALE_PER_TOKEN, 0);
+  if (st != VG_OK) return st;
+  if (inter % 16 != 0) return VG_ERR_BAD_SHAPE;
+  if (num_tokens == 0) return VG_OK;
+  if (!q4 || !block_scale || !gate_up || !global_scale) return VG_ERR_NULL_PTR;
+  if (vg::misaligned(q4, 16) || vg::misaligned(gate_up, 16) || vg::misaligned(global_scale, 4))
+    return VG_ERR_MISALIGNED;
+  int sms = 0;
+  if ((st = vg::check_device(&sms)) != VG_OK) return st;
+  vg::clear_stale_error();
+
+  vg::SiluArgs a{};
+  a.q = q4;
+  a.sf8 = block_scale;
+  a.scale = const_cast<float *>(global_scale);  // read only in this mode
+  a.gate_up = gate_up;
+  a.T = num_tokens;
+  a.I = (int32_t)inter;
+  a.nch = (int32_t)(inter / 8);
+  a.gch = 2;
+  a.ngroups = (int32_t)(inter / 16);
+  vg::set_scale_layout(a, VG_SCALE_PER_TOKEN, num_tokens);
+  // no row state: the per-group plan (column segments, two chunks a thread)
+  const vg::RowPlan plan = vg::plan_silu(num_tokens, a.nch, VG_SCALE_PER_GROUP, sms);
+  return vg::launch_silu_fp8(a, vg::kNvfp4, plan, (cudaStream_t)stream) == cudaSuccess
+             ? VG_OK
+             : VG_ERR_CUDA;
 }
 
 vg_status vg_device_status(uint32_t *flags, int32_t reset) {

@@ -12,6 +12,9 @@ seeded bytes, and compare them with the tolerance the benchmark spec fixes:
                 within 1e-3 relative of the midpoint of the two codes; such
                 flips may be at most 0.01 % of the elements; wherever
                 |v| >= 448 (saturation) the codes agree exactly.
+  NVFP4         block scale codes bit-exact; E2M1 element codes under the
+                same rule (adjacent codes near a midpoint, at most 0.01 %,
+                exact wherever |v| >= 6)
 """
 from __future__ import annotations
 
@@ -108,6 +111,43 @@ def oracle_silu(gate_up, mode, group_size=128, scale=None, want_v=True):
     return out
 
 
+def oracle_nvfp4_norm(x, residual, weight, eps, gs, want_v=True):
+    T, H = x.shape
+    out = {"q4": np.empty((T, H // 2), np.uint8), "sf": np.empty((T, H // 16), np.uint8),
+           "residual_out": None if residual is None else np.empty((T, H), np.uint16),
+           "v": np.empty((T, H), np.float64) if want_v else None}
+
+    def work(b):
+        r0, r1 = b
+        o = oracle.fused_add_rms_norm_nvfp4(x[r0:r1], None if residual is None else residual[r0:r1],
+                                            weight, eps, gs, want_v=want_v)
+        for k in ("q4", "sf", "residual_out", "v"):
+            if out[k] is not None:
+                out[k][r0:r1] = o[k]
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(work, _blocks(T, 4 * _threads())))
+    return out
+
+
+def oracle_nvfp4_silu(gate_up, gs, want_v=True):
+    T, two_i = gate_up.shape
+    I = two_i // 2
+    out = {"q4": np.empty((T, I // 2), np.uint8), "sf": np.empty((T, I // 16), np.uint8),
+           "v": np.empty((T, I), np.float64) if want_v else None}
+
+    def work(b):
+        r0, r1 = b
+        o = oracle.silu_mul_nvfp4(gate_up[r0:r1], gs, want_v=want_v)
+        for k in ("q4", "sf", "v"):
+            if out[k] is not None:
+                out[k][r0:r1] = o[k]
+
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(work, _blocks(T, 4 * _threads())))
+    return out
+
+
 # ------------------------------------------------------------------ compare
 
 class ParityError(AssertionError):
@@ -195,6 +235,55 @@ def compare_bf16(g, o, v, what="bf16"):
     if diff.size > BF16_FLIP_FRACTION * g.size:
         raise ParityError(f"{what}: {diff.size} near-midpoint flips in {g.size} elements")
     return {"elements": g.size, "flips": int(diff.size), "max_rel": float(rel.max())}
+
+
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def unpack_e2m1(q4):
+    """[T, n/2] packed bytes -> [T, n] E2M1 codes (column 2i = low nibble)."""
+    q4 = np.asarray(q4, np.uint8)
+    out = np.empty(q4.shape[:-1] + (2 * q4.shape[-1],), np.uint8)
+    out[..., 0::2] = q4 & 0xF
+    out[..., 1::2] = q4 >> 4
+    return out
+
+
+def compare_e2m1(q4_gpu, q4_orc, v_orc, what="q4"):
+    """The code rule for E2M1: identical codes, except codes adjacent in value
+    (same sign) where the oracle's v lies within 1e-3 relative of their
+    midpoint, at most 0.01 % of the elements; exact wherever |v| >= 6."""
+    a = unpack_e2m1(q4_gpu).reshape(-1)
+    b = unpack_e2m1(q4_orc).reshape(-1)
+    v = np.asarray(v_orc, np.float64).reshape(-1)
+    diff = np.flatnonzero(a != b)
+    stats = {"elements": b.size, "flips": int(diff.size)}
+    if diff.size == 0:
+        return stats
+    ca, cb, vv = a[diff], b[diff], v[diff]
+    ma, mb = (ca & 7).astype(np.int32), (cb & 7).astype(np.int32)
+    adjacent = ((ca & 8) == (cb & 8)) & (np.abs(ma - mb) == 1)
+    mid = (_E2M1_MAG[ma] + _E2M1_MAG[mb]) / 2.0
+    rel = np.where(adjacent, np.abs(np.abs(vv) - mid) / np.maximum(mid, 1e-300), np.inf)
+    bad = ~adjacent | (rel > MIDPOINT_RTOL) | (np.abs(vv) >= 6.0)
+    if np.any(bad):
+        k = diff[np.flatnonzero(bad)[:8]]
+        raise ParityError(f"{what}: {int(bad.sum())} codes outside tolerance, e.g. "
+                          + ", ".join(f"[{j}] gpu={a[j]:#x} oracle={b[j]:#x} v={v[j]!r}" for j in k))
+    if diff.size > FLIP_FRACTION * b.size:
+        raise ParityError(f"{what}: {diff.size} near-midpoint flips in {b.size} elements")
+    stats["max_flip_rel_dist"] = float(rel.max())
+    return stats
+
+
+def check_nvfp4(gpu, orc, rows=None):
+    """gpu/orc: dicts with q4, sf (and residual_out, orc['v'])."""
+    sel = (lambda a: a) if rows is None else (lambda a: a[rows])
+    compare_exact(sel(gpu["sf"]), orc["sf"], "block_scale")
+    stats = compare_e2m1(sel(gpu["q4"]), orc["q4"], orc["v"])
+    if orc.get("residual_out") is not None:
+        compare_exact(sel(gpu["residual_out"]), orc["residual_out"], "residual_out")
+    return stats
 
 
 def compare_exact(a, b, what):
@@ -520,3 +609,53 @@ def gpu_qk(d, hq, hkv, head_dim, eps, neox, device="cuda"):
     torch.cuda.synchronize()
     _check_guards(qbuf, T * row * 2, "qkv")
     return qt.cpu().numpy().view(np.uint16)
+
+
+def _gs_tensor(torch, gs, device):
+    return torch.tensor([float(np.float32(gs))], dtype=torch.float32, device=device)
+
+
+def gpu_nvfp4_norm(x, residual, weight, eps, gs, inplace=True, device="cuda"):
+    """The NVFP4 norm through the C ABI, outputs between guard bands."""
+    import torch
+    import norm_activation_fp8_gb300 as vg
+    T, H = x.shape
+    xt = torch.from_numpy(x.view(np.int16)).to(device)
+    wt = torch.from_numpy(np.ascontiguousarray(weight).view(np.int16)).to(device)
+    qbuf, q4 = _guarded(torch, T * H // 2, device)
+    fbuf, sf = _guarded(torch, T * H // 16, device)
+    rt = rbuf = r_out = None
+    if residual is not None:
+        rbuf, rraw = _guarded(torch, T * H * 2, device)
+        r_out = rraw.view(torch.int16).view(T, H)
+        if inplace:
+            r_out.copy_(torch.from_numpy(residual.view(np.int16)))
+            rt = r_out
+        else:
+            rt = torch.from_numpy(residual.view(np.int16)).to(device)
+    vg.vg_fused_add_rms_norm_nvfp4(q4.view(T, H // 2), sf.view(T, H // 16), r_out, xt, rt, wt,
+                                   _gs_tensor(torch, gs, device), eps)
+    torch.cuda.synchronize()
+    _check_guards(qbuf, T * H // 2, "q4")
+    _check_guards(fbuf, T * H // 16, "block_scale")
+    out = {"q4": q4.view(T, H // 2).cpu().numpy(), "sf": sf.view(T, H // 16).cpu().numpy(),
+           "residual_out": None}
+    if residual is not None:
+        _check_guards(rbuf, T * H * 2, "residual_out")
+        out["residual_out"] = r_out.cpu().numpy().view(np.uint16)
+    return out
+
+
+def gpu_nvfp4_silu(gate_up, gs, device="cuda"):
+    import torch
+    import norm_activation_fp8_gb300 as vg
+    T, two_i = gate_up.shape
+    I = two_i // 2
+    gt = torch.from_numpy(gate_up.view(np.int16)).to(device)
+    qbuf, q4 = _guarded(torch, T * I // 2, device)
+    fbuf, sf = _guarded(torch, T * I // 16, device)
+    vg.vg_silu_mul_nvfp4(q4.view(T, I // 2), sf.view(T, I // 16), gt, _gs_tensor(torch, gs, device))
+    torch.cuda.synchronize()
+    _check_guards(qbuf, T * I // 2, "q4")
+    _check_guards(fbuf, T * I // 16, "block_scale")
+    return {"q4": q4.view(T, I // 2).cpu().numpy(), "sf": sf.view(T, I // 16).cpu().numpy()}

@@ -50,7 +50,7 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert name in exported, name
         assert getattr(lib, name) is not None
-    assert lib.vg_abi_version() == 2
+    assert lib.vg_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -219,3 +219,36 @@ def test_qk_validation(lib):
     for k in ("qkv", "qw", "kw", "cache"):
         assert qk(lib, **{k: A + 8}) == ALIGN, k
     assert qk(lib, pos=A + 4) == ALIGN
+
+
+def nf_norm(lib, q4=A, sf=A, r_out=A, x=A, res=A, w=A, gs=A, T=4, H=4096):
+    return lib.vg_fused_add_rms_norm_nvfp4(q4, sf, r_out, x, res, w, gs, T, H,
+                                           ctypes.c_float(1e-6), None)
+
+
+def nf_silu(lib, q4=A, sf=A, gu=A, gs=A, T=4, I=4096):
+    return lib.vg_silu_mul_nvfp4(q4, sf, gu, gs, T, I, None)
+
+
+def test_nvfp4_validation(lib):
+    # row length: a multiple of 16 within [16, VG_MAX_ROW]
+    for n in (0, 8, 24, 4104, 32784):
+        assert nf_norm(lib, H=n) == SHAPE, n
+        assert nf_silu(lib, I=n) == SHAPE, n
+    assert nf_norm(lib, T=-1) == SHAPE
+    assert nf_silu(lib, T=-1) == SHAPE
+    for k in ("q4", "sf", "x", "w", "gs"):
+        assert nf_norm(lib, **{k: None}) == NULL, k
+    assert nf_norm(lib, res=None) == NULL
+    assert nf_norm(lib, r_out=None) == NULL
+    for k in ("q4", "sf", "gu", "gs"):
+        assert nf_silu(lib, **{k: None}) == NULL, k
+    assert nf_norm(lib, q4=None, sf=None, r_out=None, x=None, res=None, w=None, gs=None,
+                   T=0) == OK
+    assert nf_silu(lib, q4=None, sf=None, gu=None, gs=None, T=0) == OK
+    for k in ("q4", "r_out", "x", "res", "w"):
+        assert nf_norm(lib, **{k: A + 8}) == ALIGN, k
+    assert nf_norm(lib, gs=A + 2) == ALIGN
+    for k in ("q4", "gu"):
+        assert nf_silu(lib, **{k: A + 8}) == ALIGN, k
+    assert nf_silu(lib, gs=A + 2) == ALIGN

@@ -111,3 +111,44 @@ def test_bf16_checker_accepts_near_midpoint_flips_only():
     with pytest.raises(parity.ParityError):
         parity.compare_bf16(g3, o, v)
     assert ex.bf16_bits_to_f64(np.array([0x3F81], np.uint16))[0] == 1.0078125
+
+
+def _e2m1_case(n=40000, seed=1):
+    """Oracle-coded E2M1 values, packed the NVFP4 way, and their v."""
+    rng = np.random.default_rng(seed)
+    v = rng.standard_normal(n) * 2.5
+    codes = oracle.e2m1_encode(v)
+    return v, codes, (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+
+
+def _pack(codes):
+    return (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+
+
+def test_e2m1_unpack_order():
+    assert parity.unpack_e2m1(np.array([0x71], np.uint8)).tolist() == [1, 7]
+
+
+def test_e2m1_checker():
+    v, c, q4 = _e2m1_case()
+    assert parity.compare_e2m1(q4, q4, v)["flips"] == 0
+    # near the 1.0 / 1.5 midpoint (1.25): an adjacent flip passes
+    v2, g = v.copy(), c.copy()
+    v2[0], c2 = 1.25 * (1 + 1e-6), c.copy()
+    c2[0], g[0] = 0x3, 0x2
+    assert parity.compare_e2m1(_pack(g), _pack(c2), v2)["flips"] == 1
+    # far from a midpoint, two codes apart, across the sign, or saturated: fail
+    for vk, ok_code, bad_code in ((1.4, 0x3, 0x2), (1.25, 0x3, 0x1), (0.1, 0x0, 0x8),
+                                  (6.5, 0x7, 0x6), (-1.25 * (1 + 1e-6), 0xB, 0x3)):
+        v3, o, g = v.copy(), c.copy(), c.copy()
+        v3[0], o[0], g[0] = vk, ok_code, bad_code
+        with pytest.raises(parity.ParityError, match="outside tolerance"):
+            parity.compare_e2m1(_pack(g), _pack(o), v3)
+    # too many flips
+    near = np.flatnonzero(np.isin(c & 7, [2, 3]))[:20]
+    v4, o, g = v.copy(), c.copy(), c.copy()
+    v4[near] = np.sign(v4[near]) * 1.25
+    o[near] = (c[near] & 8) | 2
+    g[near] = (c[near] & 8) | 3
+    with pytest.raises(parity.ParityError, match="flips"):
+        parity.compare_e2m1(_pack(g), _pack(o), v4)
