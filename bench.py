@@ -66,6 +66,7 @@ STEPS.update({w.name: (w,) for w in gen.mla_workloads()})
 STEPS.update({w.name: (w,) for w in gen.pad_workloads()})
 STEPS.update({w.name: (w,) for w in gen.qk_workloads()})
 STEPS.update({w.name: (w,) for w in gen.nvfp4_workloads()})
+STEPS.update({w.name: (w,) for w in gen.group_option_workloads()})
 DEFAULT_STEP = "llama3_8b_decode"
 
 
@@ -325,6 +326,9 @@ class DeviceSet:
             return torch.full((1,), w.static_scale, dtype=torch.float32, device=dev)
         if w.mode == gen.PER_TOKEN:
             return torch.empty((w.T,), dtype=torch.float32, device=dev)
+        if w.flags & gen.COL_MAJOR:
+            return torch.empty((w.n // w.group_size, (w.T + 3) // 4 * 4), dtype=torch.float32,
+                               device=dev)
         return torch.empty((w.T, w.n // w.group_size), dtype=torch.float32, device=dev)
 
 
@@ -348,7 +352,7 @@ def launch(vg, op):
     w = op["w"]
     if w.op == "norm":
         vg.vg_fused_add_rms_norm_fp8(op["q"], op["res"], op["scale"], op["x"], op["res"],
-                                     op["weight"], w.eps, w.mode, w.group_size)
+                                     op["weight"], w.eps, w.mode | w.flags, w.group_size)
     elif w.op == "pad":
         vg.vg_fused_add_rms_norm_pad(op["out"], op["res"], op["x"], op["res"], op["weight"], w.eps)
     elif w.op == "norm4":
@@ -368,7 +372,7 @@ def launch(vg, op):
             vg.vg_fused_mla_dual_rms_norm(op["q"], op["kv"], op["q_c"], op["q_weight"], op["kv_c"],
                                           op["kv_weight"], w.eps, w.eps)
     else:
-        vg.vg_silu_mul_fp8(op["q"], op["scale"], op["gate_up"], w.mode, w.group_size)
+        vg.vg_silu_mul_fp8(op["q"], op["scale"], op["gate_up"], w.mode | w.flags, w.group_size)
 
 
 def run_gpu(args, dist):
@@ -519,7 +523,9 @@ def mode_name(w):
         return "q_fp8_per_token" if w.mode == gen.PER_TOKEN else "bf16"
     if w.op in ("norm4", "silu4"):
         return f"nvfp4_gs{w.static_scale:g}"
-    return gen.MODE_NAMES[w.mode]
+    opts = "".join(f"_{n}" for f, n in ((gen.UE8M0, "ue8m0"), (gen.COL_MAJOR, "colmajor"))
+                   if w.flags & f)
+    return gen.MODE_NAMES[w.mode] + opts
 
 
 def describe(w):
@@ -688,7 +694,8 @@ def oracle_step_runner(step, host, threads):
             for r0, r1 in blocks(w.T):
                 if w.op == "norm":
                     futs.append(pool.submit(orc.fused_add_rms_norm_fp8, h["x"][r0:r1],
-                                            h["residual"][r0:r1], h["weight"], w.eps, w.mode,
+                                            h["residual"][r0:r1], h["weight"], w.eps,
+                                            w.mode | w.flags,
                                             w.group_size, w.static_scale, False))
                 elif w.op == "qk":
                     futs.append(pool.submit(orc.qk_norm_rope, h["qkv"][r0:r1], h["q_weight"],
@@ -710,7 +717,7 @@ def oracle_step_runner(step, host, threads):
                                             h["kv_c"][r0:r1], h["kv_weight"], w.eps, w.eps,
                                             w.mode == gen.PER_TOKEN, False))
                 else:
-                    futs.append(pool.submit(orc.silu_mul_fp8, h["gate_up"][r0:r1], w.mode,
+                    futs.append(pool.submit(orc.silu_mul_fp8, h["gate_up"][r0:r1], w.mode | w.flags,
                                             w.group_size, w.static_scale, False))
         for f in futs:
             f.result()
@@ -823,7 +830,7 @@ def run_sweep(args):
     stream = torch.cuda.Stream(device=dev)
     cache = {}
     for w in (list(gen.NAMED.values()) + gen.sweep() + gen.mla_workloads() + gen.pad_workloads()
-              + gen.qk_workloads() + gen.nvfp4_workloads()):
+              + gen.qk_workloads() + gen.nvfp4_workloads() + gen.group_option_workloads()):
         if args.sweep_filter and not any(f in w.name for f in args.sweep_filter.split(",")):
             continue
         key = (w.op, w.T, w.n, w.n2, w.x_dist)

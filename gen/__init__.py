@@ -28,6 +28,7 @@ TENSOR_QKV, TENSOR_POSITIONS = 9, 10
 _ROW_BLOCK = 64
 
 STATIC, PER_TOKEN, PER_GROUP = 0, 1, 2
+UE8M0, COL_MAJOR = 0x100, 0x200  # per-group scale options, or-ed into the mode
 MODE_NAMES = {STATIC: "static", PER_TOKEN: "per_token", PER_GROUP: "per_group"}
 
 
@@ -139,6 +140,7 @@ class Workload:
     hkv: int = 0             # qk: key/value heads
     max_pos: int = 0         # qk: rows of the cos/sin cache
     group_size: int = 128
+    flags: int = 0               # per-group options (UE8M0, COL_MAJOR)
     eps: float = 1e-5
     static_scale: float = 0.05   # static fp8 scale; NVFP4: the per-tensor scale gs
     x_dist: str = "normal"
@@ -240,6 +242,16 @@ def nvfp4_workloads():
                       eps=1e-5, static_scale=NVFP4_GS) for T in NVFP4_T]
             + [Workload(f"silu_nvfp4_{T}x{NVFP4_I}", "silu4", T, NVFP4_I, PER_GROUP, group_size=16,
                         static_scale=NVFP4_GS) for T in NVFP4_T])
+
+
+# Per-group 128 scales in the format a DeepGEMM-style FP8 GEMM on sm100
+# consumes: powers of two (UE8M0), stored column-major.
+def group_option_workloads():
+    f = UE8M0 | COL_MAJOR
+    return ([Workload(f"norm_per_group128_ue8m0_colmajor_{T}x8192", "norm", T, 8192, PER_GROUP,
+                      flags=f, eps=1e-5) for T in (512, 4096, 32768)]
+            + [Workload(f"silu_per_group128_ue8m0_colmajor_{T}x14336", "silu", T, 14336, PER_GROUP,
+                        flags=f) for T in (512, 4096, 32768)])
 
 
 SWEEP_T = (1, 8, 64, 512, 4096, 32768)

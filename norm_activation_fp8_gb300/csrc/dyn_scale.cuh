@@ -69,6 +69,24 @@ __device__ __forceinline__ bool df_at_most(float xh, float xl, float p) {
   return d < 0.f || (d == 0.f && xl <= 0.f);
 }
 
+// The smallest k with 448 * 2^k >= a, for a normal fp32 a > 0, from its
+// bits: 448 = 1.75 * 2^8, so with a = m * 2^e (1 <= m < 2), k = e - 8 when
+// m <= 1.75 and e - 7 otherwise.  Exact.
+__device__ __forceinline__ int pow2_exponent_448(float a) {
+  const uint32_t b = __float_as_uint(a);
+  return (int)(b >> 23) - 127 - 8 + ((b & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+}
+
+// Whether a lies within 2^-18 (relative) of a boundary 448 * 2^k: its
+// significand within 56 units of the last place of 1.75.
+__device__ __forceinline__ bool near_pow2_boundary_448(float a) {
+  const int d = (int)(__float_as_uint(a) & 0x7FFFFFu) - 0x600000;
+  return d >= -56 && d <= 56;
+}
+
+// 2^k for -126 <= k <= 127.
+__device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
 __device__ __forceinline__ DynScale make_pow2_scale(float amax, float y, float dy) {
   float xh = amax * y;
   float xl = fmaf(amax, y, -xh) + amax * dy;
@@ -76,16 +94,14 @@ __device__ __forceinline__ DynScale make_pow2_scale(float amax, float y, float d
     xh = kAmaxFloor;
     xl = 0.f;
   }
-  int k;
-  frexpf(xh * kInv448, &k);  // 2^(k-1) <= ~X/448 < 2^k, possibly off by one
-  for (int it = 0; it < 2; ++it) {
-    if (!df_at_most(xh, xl, ldexpf(kE4M3Max, k))) ++k;
-    else if (df_at_most(xh, xl, ldexpf(kE4M3Max, k - 1))) --k;
-  }
+  // X = xh + xl with |xl| <= ulp(xh) / 2 and every boundary representable:
+  // only an xh exactly on a boundary lets xl decide
+  int k = pow2_exponent_448(xh);
+  if ((__float_as_uint(xh) & 0x7FFFFFu) == 0x600000u && xl > 0.f) ++k;
   DynScale d;
-  d.s = ldexpf(1.0f, k);
+  d.s = exp2i(k);
   d.a = 0.f;
-  d.ra = ldexpf(y, -k);
+  d.ra = y * exp2i(-k);  // exact: a power-of-two scaling
   d.f = 1.0f;
   return d;
 }

@@ -24,6 +24,7 @@
 #include <atomic>
 
 #include "common.cuh"
+#include "dyn_scale.cuh"
 #include "launch.h"
 #include "nvfp4.cuh"
 #include "tma.cuh"
@@ -111,6 +112,49 @@ __device__ __forceinline__ float amax8(const float (&v)[8]) {
   return m;
 }
 
+// The largest |silu(g) u| in fp64 over the chunk's elements whose fp32 value
+// v is at least am (1 - 2^-15): with both v and am within 2^-19 of the exact
+// values, no other element can hold the group's maximum.
+__device__ __forceinline__ double candidates_amax_f64(uint4 gv, uint4 uv, const float (&v)[8],
+                                                      float am) {
+  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+  const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+  const float cut = am * (1.0f - 1.0f / 32768.0f);
+  double m = 0.0;
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i) {
+    const float2 g = bf16x2_to_f2(gw[i]), u = bf16x2_to_f2(uw[i]);
+    if (fabsf(v[2 * i]) >= cut) m = fmax(m, fabs((double)g.x / (1.0 + exp(-(double)g.x)) * (double)u.x));
+    if (fabsf(v[2 * i + 1]) >= cut) m = fmax(m, fabs((double)g.y / (1.0 + exp(-(double)g.y)) * (double)u.y));
+  }
+  return m;
+}
+
+// Rewrites one per-group UE8M0 group whose fp32 amax lay within 2^-18 of a
+// power-of-two boundary, with the exponent of the fp64 amax; called by the
+// whole warp after its fast stores, `near` the same in all GCH lanes of a
+// group (a near group is a live one: padding groups have amax 0).
+template <int GCH>
+__device__ __noinline__ void pow2_group_settle(const uint16_t *gate_up, uint8_t *q, float *scale,
+                                               int32_t I, int32_t s_ts, int32_t s_gs, int64_t row,
+                                               int c, bool near) {
+  uint4 gv = make_uint4(0, 0, 0, 0), uv = gv;
+  if (near) {
+    gv = ld_stream_ro(gate_up + row * 2 * I + c * kElemsPerChunk);
+    uv = ld_stream_ro(gate_up + row * 2 * I + I + c * kElemsPerChunk);
+  }
+  float v[8];
+  silu_chunk(gv, uv, v);
+  const float am = lanes_max(amax8(v), GCH);
+  double m = near ? candidates_amax_f64(gv, uv, v, am) : 0.0;
+  for (int o = GCH >> 1; o > 0; o >>= 1) m = fmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (!near) return;
+  const int e = pow2_exponent(m);
+  if ((c & (GCH - 1)) == 0) scale[row * s_ts + (int64_t)(c / GCH) * s_gs] = exp2i(e);
+  scale8(v, exp2i(-e));
+  st_stream(q + row * (int64_t)I + c * kElemsPerChunk, quant8(v));
+}
+
 // Rewrites one NVFP4 block whose fp32 value gs * amax / 6 lay near an E4M3
 // midpoint, with the code the exact value rounds to; called by the whole warp
 // after its fast stores (so little is live across the call), `near` the same
@@ -128,18 +172,7 @@ __device__ __noinline__ void nvfp4_silu_settle(const uint16_t *gate_up, uint8_t 
   float v[8];
   silu_chunk(gv, uv, v);
   const float am = lanes_max(amax8(v), 2);
-  double m = 0.0;
-  if (near) {
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-    const float cut = am * (1.0f - 1.0f / 32768.0f);
-#pragma unroll 1
-    for (int i = 0; i < 4; ++i) {
-      const float2 g = bf16x2_to_f2(gw[i]), u = bf16x2_to_f2(uw[i]);
-      if (fabsf(v[2 * i]) >= cut) m = fmax(m, fabs((double)g.x / (1.0 + exp(-(double)g.x)) * (double)u.x));
-      if (fabsf(v[2 * i + 1]) >= cut) m = fmax(m, fabs((double)g.y / (1.0 + exp(-(double)g.y)) * (double)u.y));
-    }
-  }
+  double m = near ? candidates_amax_f64(gv, uv, v, am) : 0.0;
   m = fmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
   if (!near) return;
   const double x = (double)gs * m / (double)kE2M1Max;
@@ -223,6 +256,41 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
         nvfp4_silu_settle(a.gate_up, a.q, a.sf8, a.I, row, lr + k * a.ntr, gs, (near_k >> k) & 1u);
     return;
   }
+  if constexpr (OPT) {
+    uint32_t near_k = 0;
+    // Per-group with scale options.  UE8M0: s = 2^e, the smallest power of
+    // two with 448 s >= max(amax, A_MIN).  The fp32 amax is within ~2^-19
+    // of the exact one, so a group whose amax lies within 2^-18 of a
+    // boundary 448 * 2^k is settled in fp64 after the loop.
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int c = lr + k * a.ntr;
+      float v[8];
+      silu_chunk(gv[k], uv[k], v);
+      const float am = lanes_max(amax8(v), GCH);
+      float s, m;
+      if (a.ue8m0) {
+        const float fa = fmaxf(am, kAmaxFloor);
+        const int e = pow2_exponent_448(fa);
+        if (near_pow2_boundary_448(fa)) near_k |= 1u << k;
+        s = exp2i(e);
+        m = exp2i(-e);
+      } else {
+        s = silu_scale(am);
+        m = fast_rcp(s);
+      }
+      if (live && c < a.nch && (c & (GCH - 1)) == 0)
+        a.scale[row * a.s_ts + (int64_t)(c / GCH) * a.s_gs] = s;
+      scale8(v, m);
+      if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
+    }
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+      if (__any_sync(0xFFFFFFFFu, (near_k >> k) & 1u))
+        pow2_group_settle<GCH>(a.gate_up, a.q, a.scale, a.I, a.s_ts, a.s_gs, row, lr + k * a.ntr,
+                               (near_k >> k) & 1u);
+    return;
+  }
   if (MODE != kPerToken) {
     const float inv_static = (MODE == kStatic) ? __frcp_rn(__ldg(a.scale)) : 0.f;
 #pragma unroll
@@ -232,35 +300,9 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
       silu_chunk(gv[k], uv[k], v);
       float m = inv_static;
       if (MODE == kPerGroup) {
-        if constexpr (OPT) {
-          const float am = lanes_max(amax8(v), GCH);
-          float s;
-          if (a.ue8m0) {
-            // power-of-two scale; the fp32 amax is within ~3 ulps of the
-            // exact one, so a boundary that close is settled in fp64
-            int e = pow2_exponent((double)am);
-            const float fa = fmaxf(am, kAmaxFloor);
-            const bool near = fa <= ldexpf(kE4M3Max, e - 1) * (1.0f + 1.0f / 262144.0f) ||
-                              fa >= ldexpf(kE4M3Max, e) * (1.0f - 1.0f / 262144.0f);
-            if (__any_sync(0xFFFFFFFFu, near)) {
-              double am64 = silu_amax8_f64(gv[k], uv[k]);
-              for (int o = GCH >> 1; o > 0; o >>= 1)
-                am64 = fmax(am64, __shfl_xor_sync(0xFFFFFFFFu, am64, o));
-              e = pow2_exponent(am64);
-            }
-            s = ldexpf(1.0f, e);
-            m = ldexpf(1.0f, -e);
-          } else {
-            s = silu_scale(am);
-            m = fast_rcp(s);
-          }
-          if (live && c < a.nch && (c & (GCH - 1)) == 0)
-            a.scale[row * a.s_ts + (int64_t)(c / GCH) * a.s_gs] = s;
-        } else {
-          const float s = silu_scale(lanes_max(amax8(v), GCH));
-          if (live && c < a.nch && (c & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
-          m = fast_rcp(s);
-        }
+        const float s = silu_scale(lanes_max(amax8(v), GCH));
+        if (live && c < a.nch && (c & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
+        m = fast_rcp(s);
       }
       scale8(v, m);
       if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));

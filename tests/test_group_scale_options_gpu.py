@@ -91,3 +91,24 @@ def test_norm_ue8m0_colmajor_prefill_sampled():
     o = parity.oracle_norm(d["x"][rows], d["residual"][rows], d["weight"], 1e-5, mode, 128)
     parity.check_norm(g, o, mode, rows=rows)
     assert np.array_equal(g["scale"][rows], o["scale"])
+
+
+def test_group_options_sweep_full_size_sampled():
+    """The sweep's largest UE8M0 + column-major points (32768 tokens) in the
+    launch configuration it times; the oracle checks every 41st row."""
+    T = 32768
+    rows = np.arange(0, T, 41)
+    mode = PG | UE | CM
+    w = next(x for x in gen.group_option_workloads() if x.op == "norm" and x.T == T)
+    d = w.inputs()
+    g = parity.gpu_norm(d["x"], d["residual"], d["weight"], w.eps, mode, 128)
+    o = parity.oracle_norm(d["x"][rows], d["residual"][rows], d["weight"], w.eps, mode, 128)
+    parity.check_norm(g, o, mode, rows=rows)
+    assert np.array_equal(g["scale"][rows], o["scale"])
+    del d, g
+    w = next(x for x in gen.group_option_workloads() if x.op == "silu" and x.T == T)
+    gu = w.inputs()["gate_up"]
+    g = parity.gpu_silu(gu, mode, 128)
+    o = parity.oracle_silu(gu[rows], mode, 128)
+    parity.check_silu(g, o, mode, rows=rows)
+    assert np.array_equal(g["scale"][rows], o["scale"])
