@@ -725,8 +725,7 @@ def oracle_step_runner(step, host, threads):
     return one, pool
 
 
-def run_cpu_baseline(step, host, seconds):
-    threads = os.cpu_count() or 1
+def _time_oracle(step, host, threads, seconds):
     one, pool = oracle_step_runner(step, host, threads)
     one()  # builds/loads the oracle library, warms caches
     n, t0 = 0, time.perf_counter()
@@ -737,11 +736,22 @@ def run_cpu_baseline(step, host, seconds):
         if el >= seconds or n >= 1000:
             break
     pool.shutdown()
-    value = step_bytes(step) * n / el / 1e9
-    return {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+    return n, el
+
+
+def run_cpu_baseline(step, host, seconds):
+    """The oracle on all host cores (rows split over threads), then on one
+    thread for a third of the time."""
+    threads = os.cpu_count() or 1
+    n, el = _time_oracle(step, host, threads, seconds)
+    n1, el1 = _time_oracle(step, host, 1, seconds / 3)
+    return {"value": round(step_bytes(step) * n / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
             "sample": f"{n} whole steps of this workload ({el:.1f} s of CPU work), rows split "
                       f"over {threads} threads",
-            "tokens_per_s": round(step_tokens(step) * n / el, 2)}
+            "tokens_per_s": round(step_tokens(step) * n / el, 2),
+            "single_thread": {"value": round(step_bytes(step) * n1 / el1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"{n1} whole steps on one thread ({el1:.1f} s)"}}
 
 
 def run_reference(args, dist):

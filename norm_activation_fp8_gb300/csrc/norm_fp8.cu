@@ -21,6 +21,14 @@
 // computed once, by the slot's own thread, through shared memory; r^2 is
 // summed in double-float (TwoSum; r^2 is exact in fp32).
 //
+// The same row logic writes three more outputs (internal modes):
+//   kBf16Pad    bf16(y), correctly rounded, into a zero-padded row
+//               ("RMSNorm + Padding (fuse_act_padding)");
+//   kPerGroupX  per-group scales as powers of two (UE8M0) and/or stored
+//               column-major: the scale formats sm100 FP8 GEMMs read;
+//   kNvfp4      NVFP4: E4M3 scale codes per 16 columns under a per-tensor
+//               scale, E2M1 element codes two a byte (nvfp4.cuh).
+//
 // Two kernels share that row logic:
 //   norm_fp8_kernel      one CTA per row group, inputs loaded straight into
 //                        registers with 16-byte loads issued up front (small

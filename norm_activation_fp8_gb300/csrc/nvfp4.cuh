@@ -72,15 +72,4 @@ __device__ __forceinline__ uint32_t e4m3_code_settled(float x, Exact exact) {
   return (cc >> 8) == (cc & 0xFFu) ? (cc & 0xFFu) : exact();
 }
 
-// The midpoint next to x between its two E4M3 neighbours (for deciding
-// whether an fp32 x that carries an error can be trusted), or -1 when x is
-// on a value or saturated.
-__device__ __forceinline__ float e4m3_nearest_midpoint(float x) {
-  const uint32_t c = e4m3_code(x);
-  const float v = e4m3_value(c);
-  if (v == x || c == 0x7Eu && x > v) return -1.f;
-  const uint32_t lo = v < x ? c : c - 1;
-  return 0.5f * (e4m3_value(lo) + e4m3_value(lo + 1));
-}
-
 }  // namespace vg

@@ -21,6 +21,13 @@
 // midpoint and an ulp or two in s or 1/s only moves codes whose value is
 // within ~1e-6 of a midpoint (both are far inside the parity tolerance:
 // scales within 1e-6, near-midpoint flips rare).
+//
+// Decisions the pages' formats make exactly -- a power-of-two (UE8M0)
+// group exponent, an NVFP4 block's E4M3 scale code -- are taken from the
+// fp32 values wherever those are far enough from the decision boundary; the
+// rare groups or blocks that are not are settled in fp64 after the chunk
+// loop (the warp reloads their chunks and rewrites them), so that the fp64
+// work and its registers stay off the streaming path.
 #include <atomic>
 
 #include "common.cuh"
@@ -74,23 +81,6 @@ __device__ __forceinline__ void scale8(float (&v)[8], float m) {
 // fp32(max(amax, floor) / 448) to within an ulp: one multiply.
 __device__ __forceinline__ float silu_scale(float amax) {
   return fmaxf(amax, kAmaxFloor) * (1.0f / kE4M3Max);
-}
-
-// The SiLU values of a chunk in fp64 (the exponential by CUDA's double exp):
-// used only to settle a power-of-two scale whose fp32 amax lies within a few
-// ulps of a boundary.
-__device__ __noinline__ double silu_amax8_f64(uint4 gv, uint4 uv) {
-  const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-  const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-  double m = 0.0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 g = bf16x2_to_f2(gw[i]), u = bf16x2_to_f2(uw[i]);
-    const double a0 = (double)g.x / (1.0 + exp(-(double)g.x)) * (double)u.x;
-    const double a1 = (double)g.y / (1.0 + exp(-(double)g.y)) * (double)u.y;
-    m = fmax(m, fmax(fabs(a0), fabs(a1)));
-  }
-  return m;
 }
 
 // The smallest k with 448 * 2^k >= max(amax, A_MIN) (exact comparisons).
