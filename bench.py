@@ -143,6 +143,16 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def whole_job(dist, bytes_per_step, tokens_per_step, steps, ms_local):
+    """Weak scaling over replicas: every rank runs the same step on its own
+    copy of the data, the job's time is the slowest rank's and its work the
+    sum over ranks.  Returns (ms, GB/s, tokens/s) of the whole job."""
+    ms = dist.max(ms_local)
+    secs = ms * 1e-3
+    return (ms, bytes_per_step * steps * dist.world / secs / 1e9,
+            tokens_per_step * steps * dist.world / secs)
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -438,7 +448,7 @@ def run_gpu(args, dist):
     torch.cuda.synchronize()
     dist.barrier()
     ms_local = start.elapsed_time(end)
-    ms = dist.max(ms_local)
+    ms, value, tokens_s = whole_job(dist, nbytes, step_tokens(step), args.steps, ms_local)
 
     per_kernel = {}
     for w, g in zip(step, op_graphs):
@@ -451,9 +461,6 @@ def run_gpu(args, dist):
         per_kernel[w.name] = s0.elapsed_time(s1) / args.steps
     clk = clocks.stop()
 
-    total_bytes = nbytes * args.steps * dist.world
-    value = total_bytes / (ms * 1e-3) / 1e9
-    tokens_s = step_tokens(step) * args.steps * dist.world / (ms * 1e-3)
 
     dom = max(step, key=lambda w: per_kernel[w.name])
     dom_ms = per_kernel[dom.name]
