@@ -130,13 +130,16 @@ RowPlan plan_silu(int64_t T, int nch, int mode, int sms) {
   return p;
 }
 
-// Per-token SiLU at large T streams through the persistent TMA kernel.  A
-// row of at least 1024 chunks, an even number of them, is two half-row
-// stages, so each half's copy overlaps work on the other; other rows are one
-// stage.  Rows of up to 448 x 4 chunks run two CTAs per SM, longer ones one
-// CTA of up to 1024 threads.
+// Per-token SiLU from two rows per SM streams through the persistent TMA
+// kernel (measured on GB300: from T ~ 300 at I = 14336 and T ~ 256 at
+// I = 28672 it beats the register kernel, by up to 18 % at I = 28672; below
+// that the register kernel's shorter chain wins).  A row of at least 1024
+// chunks, an even number of them, is two half-row stages, so each half's
+// copy overlaps work on the other; other rows are one stage.  Rows of up to
+// 448 x 4 chunks run two CTAs per SM, longer ones one CTA of up to 1024
+// threads.
 bool plan_silu_tma_token(int64_t T, int nch, int mode, int sms, SiluTmaPlan *out) {
-  if (mode != VG_SCALE_PER_TOKEN || T < 4LL * sms || nch < 512) return false;
+  if (mode != VG_SCALE_PER_TOKEN || T < 2LL * sms || nch < 512) return false;
   SiluTmaPlan p;
   p.vpt = 4;
   p.nseg = (nch >= 1024 && nch % 2 == 0) ? 2 : 1;

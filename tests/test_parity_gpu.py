@@ -290,7 +290,8 @@ TMA_SILU = [(2048, 5120, PER_GROUP, 128), (2048, 5120, PER_GROUP, 64), (1500, 41
             (1500, 12352, STATIC, 128), (640, 28672, PER_GROUP, 128),
             (1000, 4104, PER_TOKEN, 128), (700, 28672, PER_TOKEN, 128), (1200, 12352, PER_TOKEN, 128),
             (650, 32768, PER_TOKEN, 128), (640, 14344, PER_TOKEN, 128), (620, 14352, PER_TOKEN, 128),
-            (700, 18440, PER_TOKEN, 128), (1777, 4160, PER_GROUP, 64), (1777, 4160, STATIC, 128)]
+            (700, 18440, PER_TOKEN, 128), (1777, 4160, PER_GROUP, 64), (1777, 4160, STATIC, 128),
+            (305, 28672, PER_TOKEN, 128), (500, 14336, PER_TOKEN, 128), (303, 14336, PER_TOKEN, 128)]
 
 
 @pytest.mark.parametrize("T,I,mode,G", TMA_SILU, ids=[f"{t}x{i}-m{m}-g{g}" for t, i, m, g in TMA_SILU])
