@@ -17,7 +17,11 @@
  *   a per-token scale, kv in bf16).  Section "RMSNorm + Padding
  *   (fuse_act_padding)": residual add + RMSNorm written into a padded bf16
  *   row.  Section "QK Norm + RoPE (enable_qk_norm_rope_fusion)": per-head
- *   RMSNorm of Q and K, then the rotary embedding, in place on qkv.
+ *   RMSNorm of Q and K, then the rotary embedding, in place on qkv.  The
+ *   "Quick Reference" table also names FP4 outputs of both fusions and the
+ *   "Support Matrix" NVFP4 and DeepGEMM-style per-group FP8 on sm100: the
+ *   NVFP4 entry points and the per-group scale options (UE8M0,
+ *   column-major) below.
  *
  * Numerics (the pages give no formulas; these are the readings the library
  * implements):
