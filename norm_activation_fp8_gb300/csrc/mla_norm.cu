@@ -240,6 +240,117 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArg
   }
 }
 
+// ------------------------------------------------------ warp-pair kernel
+//
+// Two warps per token for the middle range of T, where one warp per token
+// leaves SM warp slots empty and its ~600-instruction chain per token is
+// the latency: lane L = half * 32 + lane of the pair holds chunks L, L+64,
+// ... of the q row (kq per lane) then of the kv row.  Each warp reduces its
+// half in double-float; the halves meet in shared memory behind a 64-thread
+// named barrier and are combined in the same order by both warps, so both
+// compute identical scales.
+
+constexpr int kMlaPairChunks = 4;  // chunks per lane over both rows of a token
+
+template <bool QFP8>
+__global__ void __launch_bounds__(256, 4) mla_dual_norm_pair_kernel(const MlaArgs a, const int kq) {
+  __shared__ uint4 ws[kMlaPairChunks * 64];  // both weights: q chunks, then kv
+  __shared__ float4 part[4][2][2];            // [pair][half][side]: sum hi, lo, amax
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int pair = warp >> 1, half = warp & 1, L = half * 32 + lane;
+  const int64_t row = (int64_t)blockIdx.x * 4 + pair;
+  const bool live = row < a.T;  // the same for both warps of a pair
+  const uint16_t *src_q = a.src[0] + (live ? row * a.stride[0] : 0);
+  const uint16_t *src_kv = a.src[1] + (live ? row * a.stride[1] : 0);
+
+  uint4 xv[kMlaPairChunks];
+#pragma unroll
+  for (int j = 0; j < kMlaPairChunks; ++j) {
+    const bool q = j < kq;
+    const int c = (q ? j : j - kq) * 64 + L;
+    xv[j] = live && c < (q ? a.nch[0] : a.nch[1])
+                ? ld_stream_ro((q ? src_q : src_kv) + c * kElemsPerChunk)
+                : make_uint4(0, 0, 0, 0);
+  }
+  for (int i = threadIdx.x; i < a.nch[0] + a.nch[1]; i += blockDim.x)
+    ws[i] = i < a.nch[0] ? ld_keep(a.w[0] + i * kElemsPerChunk)
+                         : ld_keep(a.w[1] + (i - a.nch[0]) * kElemsPerChunk);
+  __syncthreads();
+  if (!live) return;  // both warps of the pair leave together
+  RowAcc acc_q, acc_kv;
+  float am = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMlaPairChunks; ++j) {
+    const bool q = j < kq;
+    const int c = (q ? j : j - kq) * 64 + L;
+    const uint4 wv = c < (q ? a.nch[0] : a.nch[1]) ? ws[q ? c : a.nch[0] + c] : make_uint4(0, 0, 0, 0);
+    float2 t[4];
+    float cmax;
+    if (q) {
+      pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_q);
+      am = fmaxf(am, cmax);
+    } else {
+      pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_kv);
+    }
+  }
+  float hq = acc_q.ss.x, lq = acc_q.lo.x + acc_q.lo.y;
+  two_sum_acc(hq, lq, acc_q.ss.y);
+  lanes_sum2(hq, lq, 32);
+  float hk = acc_kv.ss.x, lk = acc_kv.lo.x + acc_kv.lo.y;
+  two_sum_acc(hk, lk, acc_kv.ss.y);
+  lanes_sum2(hk, lk, 32);
+  if (QFP8) am = warp_max(am);
+  if (lane == 0) {
+    part[pair][half][0] = make_float4(hq, lq, am, 0.f);
+    part[pair][half][1] = make_float4(hk, lk, 0.f, 0.f);
+  }
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
+  float yq, dyq, ykv, dykv;
+  {
+    const float4 p0 = part[pair][0][0], p1 = part[pair][1][0];
+    float h = p0.x, l = p0.y;
+    two_sum_acc(h, l, p1.x);
+    l += p1.y;
+    rsqrt_df(h, l, a.n[0], a.inv_n[0], a.eps[0], yq, dyq);
+    am = fmaxf(p0.z, p1.z);
+  }
+  {
+    const float4 p0 = part[pair][0][1], p1 = part[pair][1][1];
+    float h = p0.x, l = p0.y;
+    two_sum_acc(h, l, p1.x);
+    l += p1.y;
+    rsqrt_df(h, l, a.n[1], a.inv_n[1], a.eps[1], ykv, dykv);
+  }
+  DynScale d;
+  if (QFP8) {
+    d = make_dyn_scale(am, yq, dyq);
+    if (L == 0) a.q_scale[row] = d.s;
+  }
+#pragma unroll
+  for (int j = 0; j < kMlaPairChunks; ++j) {
+    const bool q = j < kq;
+    const int c = (q ? j : j - kq) * 64 + L;
+    const int nch = q ? a.nch[0] : a.nch[1];
+    if (c >= nch) continue;
+    float2 t[4];
+    chunk_t(xv[j], ws[q ? c : a.nch[0] + c], t);
+    const int64_t off = (row * nch + c) * kElemsPerChunk;
+    if (QFP8 && q) {
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 qv = dyn_values(t[e], d);
+        v[2 * e] = qv.x;
+        v[2 * e + 1] = qv.y;
+      }
+      st_stream(a.q8 + off, quant8(v));
+    } else {
+      st_stream((q ? a.out[0] : a.out[1]) + off,
+                bf16x8_product_rn(t, q ? yq : ykv, q ? dyq : dykv));
+    }
+  }
+}
+
 template <int VPT, bool BIG>
 cudaError_t launch_vpt(const MlaArgs &a, bool q_fp8, const MlaPlan &p, cudaStream_t s) {
   if (q_fp8)
@@ -255,6 +366,14 @@ cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaSt
   a.thr[0] = p.thr[0];
   a.thr[1] = p.thr[1];
   a.rpc = p.rpc;
+  if (p.vpt < 0) {  // one warp pair per token
+    const int kq = (a.nch[0] + 63) / 64;
+    if (q_fp8)
+      mla_dual_norm_pair_kernel<true><<<(unsigned)p.grid, p.block, 0, s>>>(a, kq);
+    else
+      mla_dual_norm_pair_kernel<false><<<(unsigned)p.grid, p.block, 0, s>>>(a, kq);
+    return cudaGetLastError();
+  }
   if (p.vpt == 0) {  // one warp per token
     const int kq = (a.nch[0] + 31) / 32;
     if (q_fp8)
