@@ -143,6 +143,24 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def replay_spread(torch, graph, stream, steps, replays=10):
+    """Median, p10 and p90 of ms per step over `replays` further replays of
+    a graph of `steps` steps, each bracketed by CUDA events (context for the
+    single timed replay)."""
+    per = []
+    for _ in range(replays):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record()
+            graph.replay()
+            b.record()
+        torch.cuda.synchronize()
+        per.append(a.elapsed_time(b) / steps)
+    q = np.percentile(per, [10, 50, 90])
+    return {"p10": round(float(q[0]), 6), "median": round(float(q[1]), 6),
+            "p90": round(float(q[2]), 6), "replays": replays}
+
+
 def whole_job(dist, bytes_per_step, tokens_per_step, steps, ms_local):
     """Weak scaling over replicas: every rank runs the same step on its own
     copy of the data, the job's time is the slowest rank's and its work the
@@ -459,6 +477,7 @@ def run_gpu(args, dist):
             s1.record()
         torch.cuda.synchronize()
         per_kernel[w.name] = s0.elapsed_time(s1) / args.steps
+    spread = replay_spread(torch, graph, stream, args.steps)
     clk = clocks.stop()
 
 
@@ -498,6 +517,7 @@ def run_gpu(args, dist):
             "per_kernel_ms": {k: round(v, 6) for k, v in per_kernel.items()},
             "per_kernel_timing": "each op's K launches (same buffer rotation) in its own graph, "
                                  "replayed right after the timed region",
+            "ms_per_step_spread": spread,
             "parallelism": f"replicas x{dist.world} (rows sharded, no collective)",
             "gpu": props.name, "sms": props.multi_processor_count,
             "torch": torch.__version__,
@@ -819,17 +839,21 @@ def time_op_point(torch, vg, w, host, dev, stream, steps, warmup, l2):
         s1.record()
     torch.cuda.synchronize()
     us = s0.elapsed_time(s1) * 1e3 / k_launch
+    spread = replay_spread(torch, g, stream, k_launch, replays=5)
     del sets, g
     torch.cuda.empty_cache()
-    return us
+    return us, {k: (v * 1e3 if k != "replays" else v) for k, v in spread.items()}
 
 
-def point_record(w, us, peak, peak_kind):
+def point_record(w, us, peak, peak_kind, spread=None):
     nbytes = w.algorithmic_bytes()
     gbs = nbytes / (us * 1e-6) / 1e9
-    return {"point": w.name, "op": w.op, "T": w.T, "n": w.n, "mode": mode_name(w),
-            "bytes": nbytes, "us": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-            "peak": peak, "peak_source": peak_kind, "tokens_per_s": round(w.T / (us * 1e-6), 1)}
+    r = {"point": w.name, "op": w.op, "T": w.T, "n": w.n, "mode": mode_name(w),
+         "bytes": nbytes, "us": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+         "peak": peak, "peak_source": peak_kind, "tokens_per_s": round(w.T / (us * 1e-6), 1)}
+    if spread:
+        r["us_spread"] = {k: (round(v, 3) if k != "replays" else v) for k, v in spread.items()}
+    return r
 
 
 def run_sweep(args):
@@ -854,8 +878,8 @@ def run_sweep(args):
         if key not in cache:
             cache.clear()
             cache[key] = w.inputs()
-        us = time_op_point(torch, vg, w, cache[key], dev, stream, args.steps, args.warmup, l2)
-        print(json.dumps(point_record(w, us, peak, peak_kind)), flush=True)
+        us, spread = time_op_point(torch, vg, w, cache[key], dev, stream, args.steps, args.warmup, l2)
+        print(json.dumps(point_record(w, us, peak, peak_kind, spread)), flush=True)
     return 0
 
 
@@ -865,8 +889,8 @@ def run_large_token(torch, vg, dev, stream, args, l2):
     peak, peak_kind = measured_peak()
     out = []
     for w in (gen.CFG2A, gen.CFG2B, gen.CFG3):
-        us = time_op_point(torch, vg, w, w.inputs(), dev, stream, max(8, args.steps // 10),
-                           args.warmup, l2)
+        us, _ = time_op_point(torch, vg, w, w.inputs(), dev, stream, max(8, args.steps // 10),
+                              args.warmup, l2)
         r = point_record(w, us, peak, peak_kind)
         out.append({k: r[k] for k in ("point", "us", "GB/s", "frac")})
     return out
