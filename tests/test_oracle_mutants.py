@@ -73,6 +73,10 @@ MUTANTS = {
                               "                q4[col / 2] = (uint8_t)(e << 4);\n            else\n                q4[col / 2] = (uint8_t)(q4[col / 2] | e);"),
     "nvfp4_global_scale_ignored": ("double vj = s > 0.0 ? yb[j] * (double)gs / s : 0.0;",
                                    "double vj = s > 0.0 ? yb[j] / s : 0.0;"),
+    "nvfp4_amax_not_abs": ("            if (fabs(yb[j]) > amax)\n                amax = fabs(yb[j]);",
+                           "            if (yb[j] > amax)\n                amax = yb[j];"),
+    "nvfp4_zero_block_divided": ("double vj = s > 0.0 ? yb[j] * (double)gs / s : 0.0;",
+                                 "double vj = yb[j] * (double)gs / s;"),
     "rope_sign": ("rot[a] = y[a] * c - y[b] * sn;", "rot[a] = y[a] * c + y[b] * sn;"),
     "rope_cos_sin_swapped": ("double c = (double)cs[i], sn = (double)cs[D / 2 + i];",
                              "double sn = (double)cs[i], c = (double)cs[D / 2 + i];"),
