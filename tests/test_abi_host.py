@@ -252,3 +252,15 @@ def test_nvfp4_validation(lib):
     for k in ("q4", "gu"):
         assert nf_silu(lib, **{k: A + 8}) == ALIGN, k
     assert nf_silu(lib, gs=A + 2) == ALIGN
+
+
+def test_header_is_plain_c():
+    """The boundary header compiles as C99 and as C++ on its own (no CUDA or
+    torch types in the signatures)."""
+    import shutil
+    h = os.path.join(ROOT, "include", "vg_fused.h")
+    for cc, lang, std in (("gcc", "c", "-std=c99"), ("g++", "c++", "-std=c++11")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not available")
+        subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-fsyntax-only", "-x", lang, h],
+                       check=True, capture_output=True)
