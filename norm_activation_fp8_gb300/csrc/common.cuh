@@ -49,6 +49,34 @@ __device__ __forceinline__ uint2 quant8(const float (&v)[8]) {
   return o;
 }
 
+
+// Programmatic dependent launch: the grid may be scheduled while the
+// previous kernel in the stream finishes; its kernel waits
+// (griddepcontrol.wait) for that kernel's completion before reading memory,
+// so stream order is kept.
+template <class... P, class... A>
+inline cudaError_t launch_pdl(void (*kern)(P...), dim3 g, dim3 b, size_t smem, cudaStream_t s,
+                              A &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = g;
+  cfg.blockDim = b;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<A &&>(args)...);
+}
+
+// The two halves of it inside a kernel: wait for the previous grid, and let
+// the next one be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // -------------------------------------------------------------- memory ops
 
 // Read-only data streamed once: non-coherent path, no L1 allocation.
