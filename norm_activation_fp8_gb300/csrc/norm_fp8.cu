@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(512) norm_fp8_kernel(const NormArgs a) {
   constexpr bool DYN = MODE != kStatic;
   extern __shared__ __align__(128) unsigned char dsm[];
   const RowSmem sm = carve_row_smem(dsm, blockDim.x, VPT);
-  if constexpr (MODE == kStatic) pdl_wait();
+  pdl_wait();
 
   const int tid = threadIdx.x;
   const int slot = tid / a.ntr;       // row slot inside the CTA
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(512) norm_fp8_kernel(const NormArgs a) {
       wv[k] = make_uint4(0, 0, 0, 0);
     }
   }
-  if constexpr (MODE == kStatic) pdl_launch_dependents();
+  pdl_launch_dependents();
 
   float2 t[VPT][4];
   float cmax[VPT];
@@ -409,16 +409,10 @@ template <int VPT, int MODE, int GCH>
 cudaError_t launch_res(const NormArgs &a, const RowPlan &p, cudaStream_t s) {
   const int slots = scale_slots(MODE, a.ngroups) * p.rpc;
   const size_t smem = row_smem_bytes(p.block(), VPT, slots);
-  if constexpr (MODE == kStatic) {  // row CTAs: the next grid may be scheduled early
-    const dim3 g((unsigned)p.grid), b((unsigned)p.block());
-    return a.res != nullptr ? launch_pdl(norm_fp8_kernel<VPT, MODE, GCH, true>, g, b, smem, s, a)
-                            : launch_pdl(norm_fp8_kernel<VPT, MODE, GCH, false>, g, b, smem, s, a);
-  }
-  if (a.res != nullptr)
-    norm_fp8_kernel<VPT, MODE, GCH, true><<<(unsigned)p.grid, p.block(), smem, s>>>(a);
-  else
-    norm_fp8_kernel<VPT, MODE, GCH, false><<<(unsigned)p.grid, p.block(), smem, s>>>(a);
-  return cudaGetLastError();
+  // row CTAs: the next grid may be scheduled while this one drains
+  const dim3 g((unsigned)p.grid), b((unsigned)p.block());
+  return a.res != nullptr ? launch_pdl(norm_fp8_kernel<VPT, MODE, GCH, true>, g, b, smem, s, a)
+                          : launch_pdl(norm_fp8_kernel<VPT, MODE, GCH, false>, g, b, smem, s, a);
 }
 
 template <int VPT, int MODE, int GCH, bool RES>

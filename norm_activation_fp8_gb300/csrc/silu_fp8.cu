@@ -210,11 +210,10 @@ template <int VPT, int MODE, int GCH, bool BIG, bool OPT = false>
 __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken ? 2 : 3))
     silu_fp8_kernel(const SiluArgs a) {
   __shared__ float red[32];
-  // Row-segment modes are launched with programmatic dependent launch (the
-  // next grid is scheduled while this one drains; measured 2-15 % faster for
-  // back-to-back launches); the per-token modes are not (slower with it).
-  constexpr bool kPdl = MODE == kStatic || MODE == kPerGroup || MODE == kNvfp4;
-  if constexpr (kPdl) pdl_wait();
+  // Launched with programmatic dependent launch: the next grid is scheduled
+  // while this one drains (measured 2-15 % faster back to back; the
+  // persistent TMA kernels keep plain launches, slower with it).
+  pdl_wait();
 
   const int tid = threadIdx.x;
   const int slot = tid / a.ntr;
@@ -238,7 +237,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
     }
   }
 
-  if constexpr (kPdl) pdl_launch_dependents();
+  pdl_launch_dependents();
   if constexpr (MODE == kNvfp4) {
     // 16-column blocks = chunk pairs (2b, 2b + 1), held by lanes lr, lr ^ 1.
     // x = gs * amax / 6 in fp32 is within ~2^-19 of the exact value (the
@@ -485,11 +484,8 @@ cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStrea
       else
         return cudaErrorInvalidConfiguration;
     case kPerToken:
-      if (p.block() > 512)
-        silu_fp8_kernel<VPT, kPerToken, 1, true><<<g, b, 0, s>>>(a);
-      else
-        silu_fp8_kernel<VPT, kPerToken, 1, false><<<g, b, 0, s>>>(a);
-      break;
+      return p.block() > 512 ? launch_pdl(silu_fp8_kernel<VPT, kPerToken, 1, true>, g, b, 0, s, a)
+                             : launch_pdl(silu_fp8_kernel<VPT, kPerToken, 1, false>, g, b, 0, s, a);
     default:
       if (a.ue8m0 || a.s_gs != 1) {
         return a.gch == 8 ? launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 8, false, true>, g, b, 0, s, a)
