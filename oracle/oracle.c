@@ -66,6 +66,12 @@
  *  - e4m3 conversion rounds to nearest, ties to even mantissa, saturates
  *    finite overflow (and infinity) to +-448, keeps the sign of zero, and
  *    maps NaN to 0x7F.
+ *  - NaN and infinite inputs: every formula above is evaluated in IEEE
+ *    arithmetic as written, and the amax of a row or group is the largest
+ *    |y| among its non-NaN elements (a NaN never wins the comparison; 0 when
+ *    there is none).  So a NaN in r makes inv and every y NaN; an infinity
+ *    in r makes sum(r^2) infinite and inv = 0, so y = +-0 at finite r and
+ *    inf * 0 = NaN at the infinite one; silu(-inf) = -inf / inf is NaN.
  *
  * Build: plain C11, -ffp-contract=off so that no multiply-add is fused and
  * the results are the same on every host architecture.

@@ -678,6 +678,160 @@ def check_qk_norm_rope_brute_force(orc):
                     (neox, t, h)
 
 
+# ------------------------------------------------------- NaN and infinity
+#
+# The reading for non-finite inputs: every formula is evaluated in IEEE
+# arithmetic as written, and the amax of a row or group is the largest |y|
+# among its non-NaN elements (a NaN never wins the comparison; 0 when there
+# is none), floored at A_MIN as usual.  Consequences fixed here without the
+# oracle's own arithmetic:
+#   a NaN anywhere in r makes sum(r^2), inv and every y NaN: every code 0x7F,
+#     every dynamic scale fp32(A_MIN / 448);
+#   an infinity in r (and no NaN) makes sum(r^2) = inf and inv = 0: y = +-0
+#     (the sign of r w) at finite r and NaN at the infinite one, so the codes
+#     are 0x00 / 0x80 and 0x7F there, and every dynamic scale is the floor;
+#   eps = 0 with an all-zero row: inv = 1/0 = inf and y = 0 * inf = NaN;
+#   a NaN in the weight turns only its own column into NaN;
+#   SiLU: silu(g) u with a NaN operand, or silu(-inf) = -inf / inf, is NaN
+#     (code 0x7F, left out of the amax); an infinite a saturates to +-448
+#     under a static scale and makes its row's or group's dynamic scale
+#     +inf, so its own code is 0x7F (inf / inf) and its finite neighbours
+#     code as +-0.
+
+_NAN16, _PINF16, _NINF16 = 0x7FC0, 0x7F80, 0xFF80
+
+
+def _is_nan16(b):
+    b = np.asarray(b, np.uint16)
+    return ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+
+
+def check_nonfinite_norm(orc):
+    rng = np.random.default_rng(31)
+    T, H, G = 6, 256, 128
+    x = _rand_bf16(rng, (T, H))
+    res = _rand_bf16(rng, (T, H))
+    w = _weight(rng, H)
+    x[0, 5] = _NAN16                        # NaN in x
+    x[1, 7] = _PINF16                       # +inf in x
+    res[2, 200] = _NINF16                   # -inf in the residual
+    x[3, 9], res[3, 9] = _PINF16, _NINF16   # inf + (-inf) = NaN
+    floor = np.float32(orc.amax_floor() / 448.0)
+    xt = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).float()
+    rt = torch.from_numpy(res.view(np.int16)).view(torch.bfloat16).float()
+    lib = (xt + rt).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    wf = exact.bf16_bits_to_f64(w)
+    control = {m: orc.fused_add_rms_norm_fp8(x[5:6], res[5:6], w, 1e-5, m, G, scale=0.05)
+               for m in (STATIC, PER_TOKEN, PER_GROUP)}
+    for mode in (STATIC, PER_TOKEN, PER_GROUP, PER_GROUP | 0x100):
+        out = orc.fused_add_rms_norm_fp8(x, res, w, 1e-5, mode, G, scale=0.05)
+        ro = out["residual_out"]
+        nan = _is_nan16(ro)
+        assert np.array_equal(np.argwhere(nan), [[0, 5], [3, 9]])
+        assert np.array_equal(ro[~nan], lib[~nan])
+        assert ro[1, 7] == _PINF16 and ro[2, 200] == _NINF16
+        q = out["q"]
+        # the floored scale: fp32(A_MIN / 448), or the power of two above it
+        fl = np.float32(exact.pow2_at_least(F(float(orc.amax_floor())) / 448)) if mode & 0x100 \
+            else floor
+        for t in (0, 3):  # NaN rows
+            assert np.all(q[t] == 0x7F), (mode, t)
+            if mode != STATIC:
+                assert np.all(out["scale"][t] == fl), (mode, t)
+        if mode & 0x100:
+            continue  # an infinite amax has no power-of-two scale; NaN rows only
+        for t, j in ((1, 7), (2, 200)):  # infinite rows
+            assert q[t, j] == 0x7F
+            r = exact.bf16_bits_to_f64(ro[t])
+            sign = np.signbit(r * wf).astype(np.uint8) << 7
+            keep = np.arange(H) != j
+            assert np.array_equal(q[t, keep], sign[keep]), (mode, t)
+            if mode != STATIC:
+                assert np.all(out["scale"][t] == floor), (mode, t)
+        if mode in control:  # a finite row next to them is unaffected
+            assert np.array_equal(q[5], control[mode]["q"][0])
+            if mode != STATIC:
+                assert np.array_equal(out["scale"][5], control[mode]["scale"][0])
+    # a NaN weight column: 0x7F in that column only; elsewhere as with w = 0 there
+    wn, w0 = w.copy(), w.copy()
+    wn[3], w0[3] = _NAN16, 0
+    for mode in (STATIC, PER_TOKEN, PER_GROUP):
+        a = orc.fused_add_rms_norm_fp8(x[4:6], res[4:6], wn, 1e-5, mode, G, scale=0.05)
+        b = orc.fused_add_rms_norm_fp8(x[4:6], res[4:6], w0, 1e-5, mode, G, scale=0.05)
+        assert np.all(a["q"][:, 3] == 0x7F)
+        keep = np.arange(H) != 3
+        assert np.array_equal(a["q"][:, keep], b["q"][:, keep]), mode
+        if mode != STATIC:
+            assert np.array_equal(a["scale"], b["scale"]), mode
+    # eps = 0 with an all-zero row: 0 * (1/0) is NaN everywhere
+    z = np.zeros((1, H), np.uint16)
+    for mode in (STATIC, PER_TOKEN, PER_GROUP):
+        out = orc.fused_add_rms_norm_fp8(z, None, w, 0.0, mode, G, scale=0.05)
+        assert np.all(out["q"] == 0x7F), mode
+        if mode != STATIC:
+            assert np.all(out["scale"] == floor), mode
+
+
+def check_nonfinite_silu(orc):
+    rng = np.random.default_rng(32)
+    T, I, G = 6, 256, 128
+    gu = _rand_bf16(rng, (T, 2 * I))
+    marks = {0: (4, _NAN16, None),              # NaN gate
+             1: (10, _bits([1.0])[0], _PINF16),  # silu(1) * inf = +inf
+             2: (20, _PINF16, _bits([-1.5])[0]), # silu(inf) * -1.5 = -inf
+             3: (30, _NINF16, None),             # silu(-inf) = -inf / inf = NaN
+             4: (40, None, _NAN16)}              # NaN up
+    zeroed = gu.copy()
+    for t, (j, g, u) in marks.items():
+        if g is not None:
+            gu[t, j] = g
+        if u is not None:
+            gu[t, I + j] = u
+        zeroed[t, j] = zeroed[t, I + j] = 0     # a_j = 0 in the reference row
+    nan_rows, inf_rows = (0, 3, 4), (1, 2)
+    for mode in (STATIC, PER_TOKEN, PER_GROUP, PER_GROUP | 0x100):
+        out = orc.silu_mul_fp8(gu, mode, G, scale=0.1)
+        ref = orc.silu_mul_fp8(zeroed, mode, G, scale=0.1)
+        q, rq = out["q"], ref["q"]
+        for t in range(T):
+            j = marks[t][0] if t in marks else None
+            keep = np.arange(I) != j if j is not None else np.ones(I, bool)
+            if t in inf_rows and mode & 0x100:
+                continue  # an infinite amax has no power-of-two scale
+            if mode == STATIC:
+                assert np.array_equal(q[t, keep], rq[t, keep]), (mode, t)
+                if t in nan_rows:
+                    assert q[t, j] == 0x7F
+                elif t in inf_rows:
+                    assert q[t, j] == (0x7E if t == 1 else 0xFE)
+                continue
+            srow = out["scale"][t] if mode == PER_TOKEN else out["scale"][t]
+            rrow = ref["scale"][t]
+            if t in nan_rows or t == 5:
+                assert np.array_equal(srow, rrow), (mode, t)
+                assert np.array_equal(q[t, keep], rq[t, keep]), (mode, t)
+                if j is not None:
+                    assert q[t, j] == 0x7F
+                continue
+            # an infinite activation: its row (per-token) or group gets scale inf
+            assert q[t, j] == 0x7F
+            width = I if mode == PER_TOKEN else G
+            g0 = j // width
+            cols = np.arange(g0 * width, (g0 + 1) * width)
+            cols = cols[cols != j]
+            sign = (np.signbit(ref["v"][t, cols]).astype(np.uint8) << 7)
+            assert np.array_equal(q[t, cols], sign), (mode, t)
+            if mode == PER_TOKEN:
+                assert np.isposinf(srow)
+            else:
+                assert np.isposinf(srow[g0])
+                other = np.arange(I // G) != g0
+                assert np.array_equal(srow[other], rrow[other])
+                rest = np.ones(I, bool)
+                rest[g0 * G:(g0 + 1) * G] = False
+                assert np.array_equal(q[t, rest], rq[t, rest])
+
+
 ALL_CHECKS = [
     check_e4m3_spec_points, check_e4m3_all_codes, check_e4m3_encoder_brute_force,
     check_e4m3_special_values, check_bf16_all_patterns, check_bf16_encoder_brute_force,
@@ -688,4 +842,5 @@ ALL_CHECKS = [
     check_rms_norm_bf16_invariants, check_rms_norm_bf16_brute_force, check_norm_pad,
     check_qk_norm_rope_rotations, check_qk_norm_rope_pairings, check_qk_norm_rope_brute_force,
     check_group_scale_options, check_e2m1_codec, check_nvfp4_rows,
+    check_nonfinite_norm, check_nonfinite_silu,
 ]

@@ -25,6 +25,9 @@ MUTANTS = {
     "static_scale_multiplied": ("double vj = y[j] / s;", "double vj = y[j] * s;"),
     "amax_not_abs": ("if (fabs(yg[j]) > amax)\n                amax = fabs(yg[j]);",
                      "if (yg[j] > amax)\n                amax = yg[j];"),
+    "amax_propagates_nan": ("if (fabs(yg[j]) > amax)\n                amax = fabs(yg[j]);",
+                            "if (!(fabs(yg[j]) <= amax))\n                amax = fabs(yg[j]);"),
+    "silu_exp_form": ("a[j] = g / (1.0 + exp(-g)) * u;", "a[j] = g * exp(g) / (1.0 + exp(g)) * u;"),
     "fp8_max_480": ("#define ORC_E4M3_MAX 448.0", "#define ORC_E4M3_MAX 480.0"),
     "scale_layout_transposed": ("scale[t * ngroups + g] = s32;", "scale[g * 1 + t * 1] = s32;"),
     "ties_away_from_zero": ("return nearbyint(m) * quantum;", "return round(m) * quantum;"),

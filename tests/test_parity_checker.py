@@ -152,3 +152,21 @@ def test_e2m1_checker():
     g[near] = (c[near] & 8) | 3
     with pytest.raises(parity.ParityError, match="flips"):
         parity.compare_e2m1(_pack(g), _pack(o), v4)
+
+
+def test_bf16_nan_payloads_match_but_not_numbers():
+    a = np.array([0x7FC0, 0x3F80, 0xFF80], np.uint16)
+    parity.compare_bf16_exact(np.array([0x7FFF, 0x3F80, 0xFF80], np.uint16), a, "r")
+    with pytest.raises(parity.ParityError):
+        parity.compare_bf16_exact(np.array([0x7F80, 0x3F80, 0xFF80], np.uint16), a, "r")
+    with pytest.raises(parity.ParityError):
+        parity.compare_bf16_exact(np.array([0x7FC0, 0x3F81, 0xFF80], np.uint16), a, "r")
+
+
+def test_non_finite_scales_must_match_exactly():
+    o = np.array([np.inf, 1.0, np.nan], np.float32)
+    parity.compare_scales(np.array([np.inf, 1.0 + 5e-7, np.nan], np.float32), o)
+    for g in ([3e38, 1.0, np.nan], [np.inf, np.inf, np.nan], [np.inf, 1.0, 1.0],
+              [-np.inf, 1.0, np.nan]):
+        with pytest.raises(parity.ParityError):
+            parity.compare_scales(np.array(g, np.float32), o)
