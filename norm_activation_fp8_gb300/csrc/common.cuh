@@ -199,6 +199,10 @@ __device__ __forceinline__ void rsqrt_df(float s_hi, float s_lo, float n, float 
   const float c = y0 * rho * fmaf(0.375f, rho, 0.5f);
   y = y0 + c;               // renormalise: |c| << y0, so Fast2Sum is exact
   dy = (y0 - y) + c;
+  // An infinite sum of squares (an infinite element) gives 1/sqrt(inf) = 0,
+  // which the refinement above would turn into inf * 0 = NaN.  A NaN sum
+  // stays NaN.
+  if (s_hi == __int_as_float(0x7F800000)) y = dy = 0.f;
 }
 
 // --------------------------------------------------------- packed fp32 x2

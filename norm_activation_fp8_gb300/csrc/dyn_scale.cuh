@@ -50,12 +50,17 @@ __device__ __forceinline__ DynScale make_dyn_scale(float amax, float y, float dy
     d.s = s;
     d.f = D > 0.f ? kAwayOneUlp : (D < 0.f ? kTowardOneUlp : 1.0f);
     d.a = amax;
-  } else {  // amax floored: v = t * inv / s, no exact ties to resolve
+    d.ra = __frcp_rn(amax);
+  } else {
+    // amax floored, or X not a number (a NaN in the row, or inv = 0 from an
+    // infinite sum of squares): v = t * inv / s, no exact ties to resolve.
+    // inv = 0 takes a = 1 and 1/a = 0, so that v = t * 0 is the IEEE +-0, or
+    // NaN for an infinite t; a NaN inv makes every v NaN.
     d.s = kFloorScale;
     d.f = 1.0f;
-    d.a = amax > 0.f ? 448.0f * kFloorScale / y : 1.0f;
+    d.a = y == 0.f ? 1.0f : 448.0f * kFloorScale / y;
+    d.ra = y == 0.f ? 0.f : __frcp_rn(d.a);
   }
-  d.ra = __frcp_rn(d.a);
   return d;
 }
 
@@ -90,7 +95,7 @@ __device__ __forceinline__ float exp2i(int k) { return __uint_as_float((uint32_t
 __device__ __forceinline__ DynScale make_pow2_scale(float amax, float y, float dy) {
   float xh = amax * y;
   float xl = fmaf(amax, y, -xh) + amax * dy;
-  if (xh < kAmaxFloor) {  // floored (the equal case rounds to the floor too)
+  if (!(xh >= kAmaxFloor)) {  // floored (the equal case rounds to the floor too; NaN too)
     xh = kAmaxFloor;
     xl = 0.f;
   }
