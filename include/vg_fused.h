@@ -42,6 +42,17 @@
  *     library allocates nothing, keeps no per-call state, never
  *     synchronises, and launches only on `stream` (NULL = legacy default
  *     stream).  Calls are asynchronous and may be captured in a CUDA graph.
+ *   - Stream order: every output is visible to whatever runs after the call
+ *     in stream order.  Most kernels are launched with programmatic
+ *     dependent launch (the non-persistent ones): such a kernel may start
+ *     while the previous kernel in the stream is still draining, waits for
+ *     it (griddepcontrol.wait) before it reads or writes any memory, and
+ *     signals griddepcontrol.launch_dependents once its loads are issued --
+ *     before q, scale and residual_out are written.  A consumer launched
+ *     after it with programmatic dependent launch too must therefore wait
+ *     on the grid dependency (cudaGridDependencySynchronize() or
+ *     griddepcontrol.wait) before it reads these outputs; an ordinary
+ *     launch, a copy or an event needs nothing extra.
  *   - bf16 tensors are passed as uint16_t bit patterns, fp8 outputs as
  *     uint8_t E4M3 codes.  All tensors are dense and row-major, except the
  *     MLA dual norm's two inputs, which are read through a row stride.
