@@ -4,9 +4,11 @@
 One step = one pass of the whole path over one batch: residual add + RMSNorm
 -> FP8 (vg_fused_add_rms_norm_fp8) followed by SiLU-and-mul -> FP8
 (vg_silu_mul_fp8), the two fused ops that bracket an MLP block's gate-up
-GEMM.  The default workload is the Llama-3-8B decode shape: T=256 tokens,
-hidden 4096 with per-token dynamic scales, intermediate 14336 (the sweep's
-hidden/intermediate pairing) with per-token dynamic scales.
+GEMM.  The default workload is the 70B-shaped prefill: T = 16384 tokens,
+hidden 8192 (Student-t(3) x with 0.1 % outliers) with per-group-128 dynamic
+scales, then intermediate 28672 (Llama-3-70B's) with per-group-128 dynamic
+scales.  The Llama-3-8B decode step (T = 256, hidden 4096 / intermediate
+14336, per-token scales) is timed after it and reported under `decode_step`.
 
 Timing (device, CUDA events on the launching stream):
   * inputs are resident in HBM; R buffer sets (each its own copy of every
@@ -16,15 +18,15 @@ Timing (device, CUDA events on the launching stream):
     hidden); the timed region is one replay bracketed by a barrier and a
     torch.cuda.synchronize() on both sides; max over ranks;
   * the roofline's per-kernel duration: each op's K launches, over the same
-    rotation of buffer sets, captured in a graph of their own and replayed
-    right after the timed region (event nodes inside a graph would add
-    microseconds per kernel);
+    rotation of buffer sets, captured in a graph of their own, replayed once
+    untimed and then timed over several replays (median, p10, p90);
   * clocks are sampled by nvidia-smi over a window of untimed replays of the
     same graph just before the timed one, through the per-kernel replays.
 e2e repeats the step through the C ABI from pinned HOST buffers: every step
 copies its inputs host->device and reads every output back device->host,
 pipelined over three streams as a serving loop would overlap them.
---impl reference times the fp64 CPU oracle on the host cores instead.
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded row sample of the same workload.
 
 Prints ONE JSON line (rank 0).
 """
@@ -58,6 +60,7 @@ CFG3_ACT = gen.Workload("silu_per_group128_16384x28672", "silu", 16384, 28672, g
 STEPS = {
     "llama3_8b_decode": (gen.CFG1, gen.CFG1_ACT),
     "llama3_70b_prefill": (gen.CFG3, CFG3_ACT),
+    CFG3_ACT.name: (CFG3_ACT,),
 }
 # every named single-op workload and every sweep point is also a (one-op) step
 STEPS.update({name: (w,) for name, w in gen.NAMED.items()})
@@ -67,7 +70,8 @@ STEPS.update({w.name: (w,) for w in gen.pad_workloads()})
 STEPS.update({w.name: (w,) for w in gen.qk_workloads()})
 STEPS.update({w.name: (w,) for w in gen.nvfp4_workloads()})
 STEPS.update({w.name: (w,) for w in gen.group_option_workloads()})
-DEFAULT_STEP = "llama3_8b_decode"
+DEFAULT_STEP = "llama3_70b_prefill"
+DECODE_STEP = "llama3_8b_decode"
 
 
 def parse_args(argv=None):
@@ -80,6 +84,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-large-token", action="store_true",
                    help="skip timing the large-token single-op configs after the step")
+    p.add_argument("--no-decode", action="store_true",
+                   help="skip timing the decode step after the default (prefill) step")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="bound on the oracle's CPU-baseline sample")
@@ -243,25 +249,38 @@ def measured_peak():
 
 
 _CSRC = "norm_activation_fp8_gb300/csrc/"
-KERNEL_SOURCES = {
-    "norm": [_CSRC + f for f in ("norm_fp8.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
-                                 "tma.cuh", "vg_fused.cu")],
-    "pad": [_CSRC + f for f in ("norm_fp8.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
-                                "tma.cuh", "vg_fused.cu")],
-    "silu": [_CSRC + f for f in ("silu_fp8.cu", "common.cuh", "tma.cuh", "vg_fused.cu")],
-    "norm4": [_CSRC + f for f in ("norm_fp8.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
-                                  "nvfp4.cuh", "tma.cuh", "vg_fused.cu")],
-    "silu4": [_CSRC + f for f in ("silu_fp8.cu", "common.cuh", "nvfp4.cuh", "tma.cuh",
-                                  "vg_fused.cu")],
-    "mla": [_CSRC + f for f in ("mla_norm.cu", "row_norm.cuh", "common.cuh", "dyn_scale.cuh",
-                                "vg_fused.cu")],
-    "qk": [_CSRC + f for f in ("qk_norm_rope.cu", "row_norm.cuh", "common.cuh", "vg_fused.cu")],
-}
+# The translation unit of each op's kernels; the launch plans of every op
+# live in vg_fused.cu.
+KERNEL_UNITS = {"norm": "norm_fp8.cu", "pad": "norm_fp8.cu", "norm4": "norm_fp8.cu",
+                "silu": "silu_fp8.cu", "silu4": "silu_fp8.cu", "mla": "mla_norm.cu",
+                "qk": "qk_norm_rope.cu"}
+
+
+def kernel_sources(op: str):
+    """The files an op's kernel and launch plan are built from: its
+    translation unit and vg_fused.cu, with every header they include,
+    transitively (quoted includes, resolved in csrc/ and include/)."""
+    dirs = [os.path.join(ROOT, _CSRC), os.path.join(ROOT, "include")]
+    todo = [os.path.join(ROOT, _CSRC, KERNEL_UNITS[op]), os.path.join(ROOT, _CSRC, "vg_fused.cu")]
+    seen = []
+    while todo:
+        path = todo.pop(0)
+        if path in seen:
+            continue
+        seen.append(path)
+        with open(path) as f:
+            for name in re.findall(r'^\s*#\s*include\s+"([^"]+)"', f.read(), re.M):
+                for d in dirs:
+                    cand = os.path.join(d, name)
+                    if os.path.exists(cand):
+                        todo.append(cand)
+                        break
+    return [os.path.relpath(p, ROOT) for p in seen]
 
 
 def kernel_source_hash(op: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES[op]:
+    for rel in kernel_sources(op):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -403,6 +422,81 @@ def launch(vg, op):
         vg.vg_silu_mul_fp8(op["q"], op["scale"], op["gate_up"], w.mode | w.flags, w.group_size)
 
 
+def op_spread(torch, graph, stream, launches, replays=7):
+    """Duration per launch of a graph of `launches` launches of one op: one
+    untimed replay (the graph's first replay uploads it), then `replays`
+    timed replays; the median is the kernel's duration, p10 / p90 its spread."""
+    with torch.cuda.stream(stream):
+        graph.replay()
+    torch.cuda.synchronize()
+    return replay_spread(torch, graph, stream, launches, replays=replays)
+
+
+def time_step(torch, vg, step, host, dev, stream, args, dist, l2, clocks=None):
+    """Times K steps of `step` as one CUDA graph replay over rotating buffer
+    sets (inputs > 3x L2), then each op alone in a graph of its own.  With
+    `clocks`, nvidia-smi samples a window of untimed replays before the timed
+    one and the per-op replays after it."""
+    nbytes = step_bytes(step)
+    weights = device_weights(torch, step, host, dev)
+    resident = nbytes  # every set holds one copy of every input and output
+    n_sets = max(2, math.ceil(3 * l2 / max(1, resident)))
+    n_sets = min(n_sets, max(2, int(20e9 // max(1, resident))))
+    sets = [DeviceSet(torch, step, host, weights, dev) for _ in range(n_sets)]
+
+    # warm-up: W eager steps
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            for op in sets[k % n_sets].ops:
+                launch(vg, op)
+    torch.cuda.synchronize()
+
+    # The K timed steps captured once into one graph (hides launch cost).
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for k in range(args.steps):
+            for op in sets[(args.warmup + k) % n_sets].ops:
+                launch(vg, op)
+    # Per-op graphs: the same K launches of one op, for its duration.
+    op_graphs = []
+    for i in range(len(step)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(args.steps):
+                launch(vg, sets[(args.warmup + k) % n_sets].ops[i])
+        op_graphs.append(g)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):  # upload the graph: its first replay is not timed
+        graph.replay()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+        t_end = time.time() + args.clock_window
+        with torch.cuda.stream(stream):
+            while time.time() < t_end:
+                graph.replay()
+                stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    with torch.cuda.stream(stream):
+        start.record()
+        graph.replay()
+        end.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms_local = start.elapsed_time(end)
+    per_kernel = {w.name: op_spread(torch, g, stream, args.steps) for w, g in zip(step, op_graphs)}
+    spread = replay_spread(torch, graph, stream, args.steps)
+    clk = clocks.stop() if clocks is not None else None
+    del graph, op_graphs, sets
+    torch.cuda.empty_cache()
+    return dict(ms_local=ms_local, per_kernel=per_kernel, spread=spread, n_sets=n_sets,
+                resident=resident, clocks=clk)
+
+
 def run_gpu(args, dist):
     import torch
     import norm_activation_fp8_gb300 as vg
@@ -415,90 +509,40 @@ def run_gpu(args, dist):
     step = select_step(args)
     nbytes = step_bytes(step)
     host = [w.inputs() for w in step]
-    weights = device_weights(torch, step, host, dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 0) or 132 * 2 ** 20)
-    resident = nbytes  # every set holds one copy of every input and output
-    n_sets = max(2, math.ceil(3 * l2 / max(1, resident)))
-    n_sets = min(n_sets, max(2, int(20e9 // max(1, resident))))
-    sets = [DeviceSet(torch, step, host, weights, dev) for _ in range(n_sets)]
     stream = torch.cuda.Stream(device=dev)
 
-    # warm-up: W eager steps
-    with torch.cuda.stream(stream):
-        for k in range(args.warmup):
-            for op in sets[k % n_sets].ops:
-                launch(vg, op)
-    torch.cuda.synchronize()
+    t = time_step(torch, vg, step, host, dev, stream, args, dist, l2,
+                  clocks=ClockSampler(dist.local))
+    ms, value, tokens_s = whole_job(dist, nbytes, step_tokens(step), args.steps, t["ms_local"])
+    per_kernel_ms = {k: v["median"] for k, v in t["per_kernel"].items()}
 
-    # The K timed steps captured once into one graph (hides launch cost).
-    nk = len(step)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for k in range(args.steps):
-            for op in sets[(args.warmup + k) % n_sets].ops:
-                launch(vg, op)
-    # Per-kernel graphs: the same K launches of one op, for its duration.
-    op_graphs = []
-    for i in range(nk):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for k in range(args.steps):
-                launch(vg, sets[(args.warmup + k) % n_sets].ops[i])
-        op_graphs.append(g)
-    torch.cuda.synchronize()
-
-    clocks = ClockSampler(dist.local)
-    clocks.start()
-    t_end = time.time() + args.clock_window
-    with torch.cuda.stream(stream):
-        while time.time() < t_end:
-            graph.replay()
-            stream.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    dist.barrier()
-    with torch.cuda.stream(stream):
-        start.record()
-        graph.replay()
-        end.record()
-    torch.cuda.synchronize()
-    dist.barrier()
-    ms_local = start.elapsed_time(end)
-    ms, value, tokens_s = whole_job(dist, nbytes, step_tokens(step), args.steps, ms_local)
-
-    per_kernel = {}
-    for w, g in zip(step, op_graphs):
-        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            s0.record()
-            g.replay()
-            s1.record()
-        torch.cuda.synchronize()
-        per_kernel[w.name] = s0.elapsed_time(s1) / args.steps
-    spread = replay_spread(torch, graph, stream, args.steps)
-    clk = clocks.stop()
-
-
-    dom = max(step, key=lambda w: per_kernel[w.name])
-    dom_ms = per_kernel[dom.name]
+    dom = max(step, key=lambda w: per_kernel_ms[w.name])
+    dom_ms = per_kernel_ms[dom.name]
     peak, peak_kind = measured_peak()
     achieved = dom.algorithmic_bytes() / (dom_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                 "kernel": dom.name, "kernel_ms": round(dom_ms, 6),
+                "kernel_ms_spread": t["per_kernel"][dom.name],
+                "algorithmic_bytes_per_launch": dom.algorithmic_bytes(),
                 "traffic": profiled_traffic(dom.op, dom.name)}
 
+    weights = device_weights(torch, step, host, dev)
     e2e = None if args.no_e2e else run_e2e(torch, vg, step, host, weights, dev, stream, args,
                                           dist)
+    del weights
+    torch.cuda.empty_cache()
     cpu = None
     if not args.no_cpu_baseline and dist.rank == 0 and dist.world == 1:
         cpu = run_cpu_baseline(step, host, args.cpu_seconds)
+    del host
+    decode = None
+    if args.workload == DEFAULT_STEP and args.tokens is None and not args.no_decode:
+        decode = run_decode_step(torch, vg, dev, stream, args, dist, l2)
     large = None
     if not args.no_large_token and dist.rank == 0 and args.tokens is None:
-        del sets
-        torch.cuda.empty_cache()
         large = run_large_token(torch, vg, dev, stream, args, l2)
 
     line = {
@@ -511,13 +555,15 @@ def run_gpu(args, dist):
             "workload": args.workload if args.tokens is None else f"{args.workload}@T{args.tokens}",
             "ops": [describe(w) for w in step],
             "bytes_per_step": nbytes,
-            "l2": f"inputs > L2: {n_sets} rotating buffer sets x {resident / 2**20:.1f} MiB "
-                  f"(>= 3x L2 of {l2 / 2**20:.0f} MiB)",
+            "l2": f"inputs > L2: {t['n_sets']} rotating buffer sets x "
+                  f"{t['resident'] / 2**20:.1f} MiB (>= 3x L2 of {l2 / 2**20:.0f} MiB)",
             "timing": "K steps in one CUDA graph replay, CUDA events on the launching stream",
-            "per_kernel_ms": {k: round(v, 6) for k, v in per_kernel.items()},
-            "per_kernel_timing": "each op's K launches (same buffer rotation) in its own graph, "
-                                 "replayed right after the timed region",
-            "ms_per_step_spread": spread,
+            "per_kernel_ms": per_kernel_ms,
+            "per_kernel_ms_spread": t["per_kernel"],
+            "per_kernel_timing": "each op's K launches (same buffer rotation) in its own graph: "
+                                 "one untimed replay, then the median of 7 timed replays",
+            "per_kernel_sum_ms": round(sum(per_kernel_ms.values()), 6),
+            "ms_per_step_spread": t["spread"],
             "parallelism": f"replicas x{dist.world} (rows sharded, no collective)",
             "gpu": props.name, "sms": props.multi_processor_count,
             "torch": torch.__version__,
@@ -526,10 +572,32 @@ def run_gpu(args, dist):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": len(step) * args.steps,
-        "clocks": clk,
+        "clocks": t["clocks"],
+        "decode_step": decode,
         "large_token": large,
     }
     return line
+
+
+def run_decode_step(torch, vg, dev, stream, args, dist, l2):
+    """The Llama-3-8B decode step (norm per-token 256 x 4096, SiLU per-token
+    256 x 14336), timed like the main step, reported beside it."""
+    step = STEPS[DECODE_STEP]
+    host = [w.inputs() for w in step]
+    t = time_step(torch, vg, step, host, dev, stream, args, dist, l2)
+    ms = t["ms_local"] / args.steps
+    nbytes = step_bytes(step)
+    peak, _ = measured_peak()
+    per = {k: round(v["median"] * 1e3, 3) for k, v in t["per_kernel"].items()}
+    return {"workload": DECODE_STEP, "ops": [describe(w) for w in step], "bytes_per_step": nbytes,
+            "us_per_step": round(ms * 1e3, 3), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+            "tokens_per_s": round(step_tokens(step) / (ms * 1e-3), 1),
+            "us_per_step_spread": {k: (round(v * 1e3, 3) if k != "replays" else v)
+                                   for k, v in t["spread"].items()},
+            "per_kernel_us": per,
+            "per_kernel_frac": {w.name: round(w.algorithmic_bytes() / (per[w.name] * 1e-6) / 1e9
+                                              / peak, 4) for w in step},
+            "l2": f"{t['n_sets']} rotating buffer sets (>= 3x L2)"}
 
 
 def select_step(args):
@@ -752,7 +820,23 @@ def oracle_step_runner(step, host, threads):
     return one, pool
 
 
-def _time_oracle(step, host, threads, seconds):
+def sample_step(step, host, rows):
+    """The first `rows` rows of every op of a step (the generator's rows are
+    independent blocks, so this is a prefix of the same workload)."""
+    import dataclasses
+    s_step, s_host = [], []
+    for w, h in zip(step, host):
+        r = min(w.T, rows)
+        s_step.append(dataclasses.replace(w, T=r))
+        s_host.append({k: (v[:r] if k in ROW_KEYS else v) for k, v in h.items()})
+    return tuple(s_step), s_host
+
+
+# host arrays indexed by token row (the rest are per-op constants)
+ROW_KEYS = ("x", "residual", "gate_up", "q_c", "kv_c", "qkv", "positions")
+
+
+def _time_oracle(step, host, threads, seconds, max_iters=1000):
     one, pool = oracle_step_runner(step, host, threads)
     one()  # builds/loads the oracle library, warms caches
     n, t0 = 0, time.perf_counter()
@@ -760,36 +844,51 @@ def _time_oracle(step, host, threads, seconds):
         one()
         n += 1
         el = time.perf_counter() - t0
-        if el >= seconds or n >= 1000:
+        if el >= seconds or n >= max_iters:
             break
     pool.shutdown()
     return n, el
 
 
+CPU_SAMPLE_ROWS = 4096       # rows per op in one sample step on all host cores
+CPU_SAMPLE_ROWS_ONE = 256    # rows per op in one sample step on one thread
+
+
 def run_cpu_baseline(step, host, seconds):
     """The oracle on all host cores (rows split over threads), then on one
-    thread for a third of the time."""
+    thread for a third of the time, each over a bounded row sample of the
+    step repeated until the time is up."""
     threads = os.cpu_count() or 1
-    n, el = _time_oracle(step, host, threads, seconds)
-    n1, el1 = _time_oracle(step, host, 1, seconds / 3)
-    return {"value": round(step_bytes(step) * n / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+    s_step, s_host = sample_step(step, host, CPU_SAMPLE_ROWS)
+    n, el = _time_oracle(s_step, s_host, threads, seconds)
+    o_step, o_host = sample_step(step, host, CPU_SAMPLE_ROWS_ONE)
+    n1, el1 = _time_oracle(o_step, o_host, 1, seconds / 3)
+    rows = "+".join(str(w.T) for w in s_step)
+    rows1 = "+".join(str(w.T) for w in o_step)
+    return {"value": round(step_bytes(s_step) * n / el / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{n} whole steps of this workload ({el:.1f} s of CPU work), rows split "
-                      f"over {threads} threads",
-            "tokens_per_s": round(step_tokens(step) * n / el, 2),
-            "single_thread": {"value": round(step_bytes(step) * n1 / el1 / 1e9, 4), "unit": "GB/s",
-                              "sample": f"{n1} whole steps on one thread ({el1:.1f} s)"}}
+            "sample": f"{n} repetitions of the first {rows} rows of the step's ops "
+                      f"({step_bytes(s_step) / 1e6:.1f} MB each, {el:.1f} s of CPU work), rows "
+                      f"split over {threads} threads",
+            "tokens_per_s": round(step_tokens(s_step) * n / el, 2),
+            "single_thread": {"value": round(step_bytes(o_step) * n1 / el1 / 1e9, 4), "unit": "GB/s",
+                              "sample": f"{n1} repetitions of the first {rows1} rows on one thread "
+                                        f"({el1:.1f} s)"}}
 
 
 def run_reference(args, dist):
-    """The fp64 CPU oracle as the reference arm, on this workload."""
+    """The fp64 CPU oracle as the reference arm, on this workload: each step
+    is a bounded row sample (the first CPU_SAMPLE_ROWS rows of every op)."""
     if dist.rank != 0:
         return None
-    step = select_step(args)
+    import dataclasses
+    full = select_step(args)
+    # the generator's rows are independent blocks: inputs drawn for the
+    # first R rows are the first R rows of the full workload's inputs
+    step = tuple(dataclasses.replace(w, T=min(w.T, CPU_SAMPLE_ROWS)) for w in full)
     host = [w.inputs() for w in step]
     threads = os.cpu_count() or 1
     one, pool = oracle_step_runner(step, host, threads)
-    # each step is one whole step of the workload; bounded by the sample rule
     for _ in range(args.warmup):
         one()
     t0 = time.perf_counter()
@@ -798,16 +897,20 @@ def run_reference(args, dist):
     el = time.perf_counter() - t0
     pool.shutdown()
     value = step_bytes(step) * args.steps / el / 1e9
+    rows = "+".join(str(w.T) for w in step)
     cpu = {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-           "sample": f"{args.steps} whole steps of this workload, rows split over {threads} threads"}
+           "sample": f"{args.steps} steps, each the first {rows} rows of the workload's ops "
+                     f"({step_bytes(step) / 1e6:.1f} MB), rows split over {threads} threads"}
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "tokens_per_s": round(step_tokens(step) * args.steps / el, 2),
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el * 1e3 / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "ops": [describe(w) for w in step],
-                   "bytes_per_step": step_bytes(step)},
+        "config": {"workload": args.workload, "ops": [describe(w) for w in full],
+                   "bytes_per_step": step_bytes(full),
+                   "sample_ops": [describe(w) for w in step],
+                   "sample_bytes_per_step": step_bytes(step)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -815,9 +918,10 @@ def run_reference(args, dist):
     }
 
 
-def time_op_point(torch, vg, w, host, dev, stream, steps, warmup, l2):
-    """Mean duration (us) of one op's launches: K launches over rotating
-    buffer sets (together > 3x L2) in one CUDA graph, CUDA events."""
+def time_op_point(torch, vg, w, host, dev, stream, steps, warmup, l2, replays=5):
+    """Duration (us) of one op's launch: K launches over rotating buffer
+    sets (together > 3x L2) in one CUDA graph, one untimed replay, then the
+    median of `replays` timed replays (CUDA events)."""
     nbytes = w.algorithmic_bytes()
     n_sets = max(2, min(64, math.ceil(3 * l2 / nbytes)))
     weights = device_weights(torch, (w,), [host], dev)
@@ -831,18 +935,11 @@ def time_op_point(torch, vg, w, host, dev, stream, steps, warmup, l2):
         for k in range(k_launch):
             launch(vg, sets[k % n_sets].ops[0])
     torch.cuda.synchronize()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g.replay()
-        s0.record()
-        g.replay()
-        s1.record()
-    torch.cuda.synchronize()
-    us = s0.elapsed_time(s1) * 1e3 / k_launch
-    spread = replay_spread(torch, g, stream, k_launch, replays=5)
-    del sets, g
+    spread = op_spread(torch, g, stream, k_launch, replays=replays)
+    del sets, g, weights
     torch.cuda.empty_cache()
-    return us, {k: (v * 1e3 if k != "replays" else v) for k, v in spread.items()}
+    spread = {k: (v * 1e3 if k != "replays" else v) for k, v in spread.items()}
+    return spread["median"], spread
 
 
 def point_record(w, us, peak, peak_kind, spread=None):
@@ -883,16 +980,34 @@ def run_sweep(args):
     return 0
 
 
+def large_token_workloads():
+    """The configs the >= 80 % roofline gate covers: SiLU 2048 x 14336
+    (static and per-group 128), the 70B-shaped prefill norm, and every sweep
+    point with T >= 4096 (both ops, all three scale modes, both shapes)."""
+    return [gen.CFG2A, gen.CFG2B, gen.CFG3] + [w for w in gen.sweep() if w.T >= 4096]
+
+
 def run_large_token(torch, vg, dev, stream, args, l2):
-    """The large-token single-op configs (the >= 80 % roofline gate), timed
-    after the step in the same run, for context next to the step line."""
+    """Every large-token point timed after the step in the same run.  Inputs
+    are drawn once per (op, row length, distribution) at the largest T and
+    sliced: the generator's rows are independent blocks, so the first T rows
+    are exactly the inputs of the T-row point."""
     peak, peak_kind = measured_peak()
+    points = large_token_workloads()
+    groups = {}
+    for w in points:
+        groups.setdefault((w.op, w.n, w.x_dist), []).append(w)
     out = []
-    for w in (gen.CFG2A, gen.CFG2B, gen.CFG3):
-        us, _ = time_op_point(torch, vg, w, w.inputs(), dev, stream, max(8, args.steps // 10),
-                              args.warmup, l2)
-        r = point_record(w, us, peak, peak_kind)
-        out.append({k: r[k] for k in ("point", "us", "GB/s", "frac")})
+    for key, ws in groups.items():
+        big = max(ws, key=lambda w: w.T)
+        full = big.inputs()
+        for w in ws:
+            host = {k: (v[:w.T] if k in ROW_KEYS else v) for k, v in full.items()}
+            us, spread = time_op_point(torch, vg, w, host, dev, stream, max(8, args.steps // 2),
+                                       args.warmup, l2)
+            r = point_record(w, us, peak, peak_kind, spread)
+            out.append({k: r[k] for k in ("point", "us", "GB/s", "frac", "us_spread")})
+        del full
     return out
 
 
