@@ -1003,7 +1003,7 @@ def run_large_token(torch, vg, dev, stream, args, l2):
         full = big.inputs()
         for w in ws:
             host = {k: (v[:w.T] if k in ROW_KEYS else v) for k, v in full.items()}
-            us, spread = time_op_point(torch, vg, w, host, dev, stream, max(8, args.steps // 2),
+            us, spread = time_op_point(torch, vg, w, host, dev, stream, max(20, args.steps),
                                        args.warmup, l2)
             r = point_record(w, us, peak, peak_kind, spread)
             out.append({k: r[k] for k in ("point", "us", "GB/s", "frac", "us_spread")})

@@ -87,6 +87,7 @@ struct TmaPlan {
   int block;
   int stages;
   int64_t grid;
+  size_t smem;  // dynamic shared memory to request (>= the layout's need)
 };
 constexpr size_t kTmaMaxSmem = 227 * 1024;  // opt-in limit per CTA (static + dynamic)
 
@@ -115,6 +116,7 @@ struct SiluTmaPlan {
   int block;
   int nseg;  // column segments of a row, one stage each (1 or 2)
   int64_t grid;
+  size_t smem;  // dynamic shared memory to request (>= the stages' need)
 };
 size_t silu_tma_token_smem_bytes(int I, int nseg);
 cudaError_t launch_silu_fp8_tma_token(SiluArgs a, const SiluTmaPlan &plan, cudaStream_t stream);

@@ -145,18 +145,41 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const M
 // recomputes t = x * w from the registers.  Warps run independent tokens, so
 // one token's reduction latency hides behind the loads of others.
 
-__device__ __forceinline__ void chunk_t(const uint4 &xv, const uint4 &wv, float2 (&t)[4]) {
+// t = x * w with the weight as fp32 pairs.
+__device__ __forceinline__ void chunk_t(const uint4 &xv, const float2 (&wf)[4], float2 (&t)[4]) {
   const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-  const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) t[i] = f2_mul(bf16x2_to_f2(xw[i]), bf16x2_to_f2(ww[i]));
+  for (int i = 0; i < 4; ++i) t[i] = f2_mul(bf16x2_to_f2(xw[i]), wf[i]);
+}
+
+// Both weights of the warp and warp-pair kernels sit in shared memory as
+// fp32, converted once per CTA (two float4 a chunk), so that neither pass
+// unpacks them again: these kernels are bound by the integer pipe, which
+// does the unpacking.
+__device__ __forceinline__ void stage_weights_f32(float4 *ws, const MlaArgs &a) {
+  for (int i = threadIdx.x; i < a.nch[0] + a.nch[1]; i += blockDim.x) {
+    const uint4 wb = i < a.nch[0] ? ld_keep(a.w[0] + i * kElemsPerChunk)
+                                  : ld_keep(a.w[1] + (i - a.nch[0]) * kElemsPerChunk);
+    ws[2 * i] = make_float4(bf16_lo(wb.x), bf16_hi(wb.x), bf16_lo(wb.y), bf16_hi(wb.y));
+    ws[2 * i + 1] = make_float4(bf16_lo(wb.z), bf16_hi(wb.z), bf16_lo(wb.w), bf16_hi(wb.w));
+  }
+}
+
+// Chunk i of the staged weights (zeros past the row).
+__device__ __forceinline__ void weights_f32(const float4 *ws, int i, bool in_row, float2 (&wf)[4]) {
+  const float4 w0 = in_row ? ws[2 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 w1 = in_row ? ws[2 * i + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  wf[0] = make_float2(w0.x, w0.y);
+  wf[1] = make_float2(w0.z, w0.w);
+  wf[2] = make_float2(w1.x, w1.y);
+  wf[3] = make_float2(w1.z, w1.w);
 }
 
 constexpr int kMlaWarpChunks = 8;  // chunks per lane over both rows of a token
 
 template <bool QFP8>
 __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArgs a, const int kq) {
-  __shared__ uint4 ws[kMlaWarpChunks * 32];  // both weights: q chunks, then kv
+  __shared__ float4 ws[kMlaWarpChunks * 32 * 2];  // both weights as fp32: q chunks, then kv
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const bool live = row < a.T;  // warp-uniform
@@ -176,9 +199,7 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArg
                 ? ld_stream_ro((q ? src_q : src_kv) + c * kElemsPerChunk)
                 : make_uint4(0, 0, 0, 0);
   }
-  for (int i = threadIdx.x; i < a.nch[0] + a.nch[1]; i += blockDim.x)
-    ws[i] = i < a.nch[0] ? ld_keep(a.w[0] + i * kElemsPerChunk)
-                         : ld_keep(a.w[1] + (i - a.nch[0]) * kElemsPerChunk);
+  stage_weights_f32(ws, a);
   __syncthreads();
   if (!live) return;  // whole warps leave together
   RowAcc acc_q, acc_kv;
@@ -187,7 +208,8 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArg
   for (int j = 0; j < kMlaWarpChunks; ++j) {
     const bool q = j < kq;
     const int c = (q ? j : j - kq) * 32 + lane;
-    const uint4 wv = c < (q ? a.nch[0] : a.nch[1]) ? ws[q ? c : a.nch[0] + c] : make_uint4(0, 0, 0, 0);
+    float2 wv[4];
+    weights_f32(ws, q ? c : a.nch[0] + c, c < (q ? a.nch[0] : a.nch[1]), wv);
     float2 t[4];
     float cmax;
     if (q) {
@@ -221,8 +243,9 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArg
     const int c = (q ? j : j - kq) * 32 + lane;
     const int nch = q ? a.nch[0] : a.nch[1];
     if (c >= nch) continue;
-    float2 t[4];
-    chunk_t(xv[j], ws[q ? c : a.nch[0] + c], t);
+    float2 wv[4], t[4];
+    weights_f32(ws, q ? c : a.nch[0] + c, true, wv);
+    chunk_t(xv[j], wv, t);
     const int64_t off = (row * nch + c) * kElemsPerChunk;
     if (QFP8 && q) {
       float v[8];
@@ -254,7 +277,7 @@ constexpr int kMlaPairChunks = 4;  // chunks per lane over both rows of a token
 
 template <bool QFP8>
 __global__ void __launch_bounds__(256, 4) mla_dual_norm_pair_kernel(const MlaArgs a, const int kq) {
-  __shared__ uint4 ws[kMlaPairChunks * 64];  // both weights: q chunks, then kv
+  __shared__ float4 ws[kMlaPairChunks * 64 * 2];  // both weights as fp32: q chunks, then kv
   __shared__ float4 part[4][2][2];            // [pair][half][side]: sum hi, lo, amax
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int pair = warp >> 1, half = warp & 1, L = half * 32 + lane;
@@ -272,9 +295,7 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_pair_kernel(const MlaArg
                 ? ld_stream_ro((q ? src_q : src_kv) + c * kElemsPerChunk)
                 : make_uint4(0, 0, 0, 0);
   }
-  for (int i = threadIdx.x; i < a.nch[0] + a.nch[1]; i += blockDim.x)
-    ws[i] = i < a.nch[0] ? ld_keep(a.w[0] + i * kElemsPerChunk)
-                         : ld_keep(a.w[1] + (i - a.nch[0]) * kElemsPerChunk);
+  stage_weights_f32(ws, a);
   __syncthreads();
   if (!live) return;  // both warps of the pair leave together
   RowAcc acc_q, acc_kv;
@@ -283,7 +304,8 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_pair_kernel(const MlaArg
   for (int j = 0; j < kMlaPairChunks; ++j) {
     const bool q = j < kq;
     const int c = (q ? j : j - kq) * 64 + L;
-    const uint4 wv = c < (q ? a.nch[0] : a.nch[1]) ? ws[q ? c : a.nch[0] + c] : make_uint4(0, 0, 0, 0);
+    float2 wv[4];
+    weights_f32(ws, q ? c : a.nch[0] + c, c < (q ? a.nch[0] : a.nch[1]), wv);
     float2 t[4];
     float cmax;
     if (q) {
@@ -332,8 +354,9 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_pair_kernel(const MlaArg
     const int c = (q ? j : j - kq) * 64 + L;
     const int nch = q ? a.nch[0] : a.nch[1];
     if (c >= nch) continue;
-    float2 t[4];
-    chunk_t(xv[j], ws[q ? c : a.nch[0] + c], t);
+    float2 wv[4], t[4];
+    weights_f32(ws, q ? c : a.nch[0] + c, true, wv);
+    chunk_t(xv[j], wv, t);
     const int64_t off = (row * nch + c) * kElemsPerChunk;
     if (QFP8 && q) {
       float v[8];

@@ -349,12 +349,19 @@ __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, con
     fence_mbar_init();
   }
   __syncthreads();
+  // Launched with programmatic dependent launch: the barriers above are set
+  // up while the previous grid drains; nothing in global memory is touched
+  // before it has finished.  The next grid may then be scheduled: its CTAs
+  // take the slots of CTAs of this one as they exit (the plan's shared
+  // memory keeps exactly its CTAs on an SM).
+  pdl_wait();
   if (lr == 0) {
     mbar_arrive_expect_tx(wbar, row_bytes);
     tma_load_bulk(wbuf, a.w, row_bytes, wbar);
     for (int s = 0; s < stages; ++s)
       if (first + s * stride < a.T) issue(s, first + s * stride);
   }
+  pdl_launch_dependents();
   bool failed = __syncthreads_or(!mbar_wait_bounded(wbar, 0));
 
   int64_t i = 0;
@@ -431,8 +438,8 @@ cudaError_t launch_tma_res(const NormArgs &a, const TmaPlan &p, cudaStream_t s) 
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit, std::memory_order_release);
   }
-  kern<<<(unsigned)p.grid, p.block, L.total, s>>>(a, p.stages);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)p.grid), dim3((unsigned)p.block),
+                    p.smem > L.total ? p.smem : L.total, s, a, p.stages);
 }
 
 template <int VPT, int MODE, int GCH>

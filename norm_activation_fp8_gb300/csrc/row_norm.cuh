@@ -17,13 +17,13 @@ struct RowAcc {
 };
 
 // Pass 1 over one chunk: r = bf16(x + residual) (returned packed, for
-// residual_out), t = r * w, the chunk's amax |t|, and sum r^2.
+// residual_out), t = r * w, the chunk's amax |t|, and sum r^2.  The weight
+// comes as four fp32 pairs.
 template <bool DYN, bool RES>
-__device__ __forceinline__ uint4 pass1_chunk(const uint4 &xv, const uint4 &rv, const uint4 &wv,
+__device__ __forceinline__ uint4 pass1_chunk(const uint4 &xv, const uint4 &rv, const float2 (&wf)[4],
                                              float2 (&t)[4], float &cmax, RowAcc &acc) {
   const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
   const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
-  const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
   const float2 neg1 = make_float2(-1.f, -1.f);
   uint32_t ow[4];
   float m = 0.f;
@@ -46,11 +46,20 @@ __device__ __forceinline__ uint4 pass1_chunk(const uint4 &xv, const uint4 &rv, c
     } else {
       acc.ss = f2_fma(r, r, acc.ss);
     }
-    t[i] = f2_mul(r, bf16x2_to_f2(ww[i]));
+    t[i] = f2_mul(r, wf[i]);
     m = fmaxf(m, fmaxf(fabsf(t[i].x), fabsf(t[i].y)));
   }
   cmax = m;
   return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
+// The same with the weight as a packed bf16 chunk.
+template <bool DYN, bool RES>
+__device__ __forceinline__ uint4 pass1_chunk(const uint4 &xv, const uint4 &rv, const uint4 &wv,
+                                             float2 (&t)[4], float &cmax, RowAcc &acc) {
+  const float2 wf[4] = {bf16x2_to_f2(wv.x), bf16x2_to_f2(wv.y), bf16x2_to_f2(wv.z),
+                        bf16x2_to_f2(wv.w)};
+  return pass1_chunk<DYN, RES>(xv, rv, wf, t, cmax, acc);
 }
 
 // bf16(t * (y + dy)) for two elements, rounded as the exact product would
@@ -77,9 +86,16 @@ __device__ __forceinline__ uint32_t bf16x2_product_rn(float2 t, float y, float d
 }
 
 // bf16 of t * (y + dy) for a chunk of 8.  p = fp32(t * y) lies within
-// ~1.5 fp32 ulps of the exact product, so its bf16 rounding is the exact
-// product's unless p sits within a few fp32 ulps of a bf16 midpoint (low
-// half 0x8000); only such chunks (about 1 in 1000) take the double-float path.
+// 2^-23 |p| (normal p) or 2^-149 (subnormal p) of the exact product E.  The
+// bracket b <= E <= a (or a <= E <= b for negative p) with
+//   a = fp32(p (1 + 2^-22) + 2^-149),   b = fp32(p (1 - 2^-22) - 2^-149)
+// holds after the roundings of a and b, and rounding is monotonic: wherever
+// bf16(a) and bf16(b) have the same magnitude, every value between them --
+// E included -- rounds to that magnitude, and bf16(p) carries E's sign (the
+// sign of t; a zero p keeps its sign).  Only chunks with an element whose
+// bracket straddles a bf16 rounding boundary (about 1 in 1000) take the
+// double-float path.  Three packed conversions and one logic op a pair,
+// instead of a bit test per element: this keeps the integer pipe free.
 static __device__ __noinline__ uint4 bf16x8_product_rn_slow(float2 t0, float2 t1, float2 t2, float2 t3,
                                                      float y, float dy) {
   return make_uint4(bf16x2_product_rn(t0, y, dy), bf16x2_product_rn(t1, y, dy),
@@ -88,18 +104,22 @@ static __device__ __noinline__ uint4 bf16x8_product_rn_slow(float2 t0, float2 t1
 
 __device__ __forceinline__ uint4 bf16x8_product_rn(const float2 (&t)[4], float y, float dy) {
   const float2 yy = make_float2(y, y);
-  float2 p[4];
-  bool near = false;
+  const float2 ku = make_float2(1.0f + 0x1p-22f, 1.0f + 0x1p-22f);
+  const float2 kd = make_float2(1.0f - 0x1p-22f, 1.0f - 0x1p-22f);
+  const float2 eu = make_float2(0x1p-149f, 0x1p-149f);
+  const float2 ed = make_float2(-0x1p-149f, -0x1p-149f);
+  uint32_t o[4], diff = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    p[i] = f2_mul(t[i], yy);
-    near |= ((__float_as_uint(p[i].x) & 0xFFFFu) - 0x7FF8u) <= 0x10u;
-    near |= ((__float_as_uint(p[i].y) & 0xFFFFu) - 0x7FF8u) <= 0x10u;
+    const float2 p = f2_mul(t[i], yy);
+    const float2 a = f2_fma(p, ku, eu);
+    const float2 b = f2_fma(p, kd, ed);
+    diff |= pack_bf16x2_rn(a.x, a.y) ^ pack_bf16x2_rn(b.x, b.y);
+    o[i] = pack_bf16x2_rn(p.x, p.y);
   }
-  if (near)  // rare: out of line, so it costs the common path no registers
+  if (diff & 0x7FFF7FFFu)  // rare: out of line, so it costs the common path no registers
     return bf16x8_product_rn_slow(t[0], t[1], t[2], t[3], y, dy);
-  return make_uint4(pack_bf16x2_rn(p[0].x, p[0].y), pack_bf16x2_rn(p[1].x, p[1].y),
-                    pack_bf16x2_rn(p[2].x, p[2].y), pack_bf16x2_rn(p[3].x, p[3].y));
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 }  // namespace vg

@@ -391,8 +391,13 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
     fence_mbar_init();
   }
   __syncthreads();
+  // Programmatic dependent launch, as the persistent norm kernel: nothing in
+  // global memory before the previous grid has finished; the next grid's
+  // CTAs take the slots of this one's as they exit.
+  pdl_wait();
   if (tid == 0 && first < a.T)
     for (int sg = 0; sg < NSEG; ++sg) issue(sg, first);
+  pdl_launch_dependents();
 
   bool failed = false;
   int fail_sg = 0;      // the segment whose wait gave up
@@ -469,8 +474,9 @@ cudaError_t launch_tma_token(const SiluArgs &a, const SiluTmaPlan &p, cudaStream
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit, std::memory_order_release);
   }
-  kern<<<(unsigned)p.grid, p.block, silu_tma_token_smem_bytes(a.I, NSEG), s>>>(a);
-  return cudaGetLastError();
+  const size_t need = silu_tma_token_smem_bytes(a.I, NSEG);
+  return launch_pdl(kern, dim3((unsigned)p.grid), dim3((unsigned)p.block),
+                    p.smem > need ? p.smem : need, s, a);
 }
 
 template <int VPT>

@@ -19,6 +19,8 @@ constexpr int kMaxDevices = 64;
 // 0 = not checked yet, 1 = supported (cc 10.3), 2 = unsupported.
 std::atomic<int> g_device_state[kMaxDevices];
 std::atomic<int> g_device_sms[kMaxDevices];
+std::atomic<int> g_device_smem[kMaxDevices];      // shared memory per SM
+std::atomic<int> g_device_smem_rsv[kMaxDevices];  // reserved by the system per CTA
 
 // Checks (once per device) that the current device is a GB300 and returns
 // its SM count in *sms.
@@ -28,17 +30,41 @@ vg_status check_device(int *sms) {
   if (dev < 0 || dev >= kMaxDevices) return VG_ERR_UNSUPPORTED_DEVICE;
   int st = g_device_state[dev].load(std::memory_order_acquire);
   if (st == 0) {
-    int major = 0, minor = 0, n = 0;
+    int major = 0, minor = 0, n = 0, smem = 0, rsv = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
       return VG_ERR_CUDA;
     g_device_sms[dev].store(n, std::memory_order_relaxed);
+    g_device_smem[dev].store(smem, std::memory_order_relaxed);
+    g_device_smem_rsv[dev].store(rsv, std::memory_order_relaxed);
     st = (major == 10 && minor == 3) ? 1 : 2;
     g_device_state[dev].store(st, std::memory_order_release);
   }
   *sms = g_device_sms[dev].load(std::memory_order_relaxed);
   return st == 1 ? VG_OK : VG_ERR_UNSUPPORTED_DEVICE;
+}
+
+// Dynamic shared memory for a persistent kernel that must keep exactly
+// `ctas` CTAs on an SM: at least `need`, and enough that ctas + 1 of them do
+// not fit.  The persistent kernels are launched with programmatic dependent
+// launch; without the cap, CTAs of the next launch would take a spare slot
+// beside the running ones as soon as it is scheduled, and the later CTAs
+// would then pile onto the SMs that free up first, so that some SMs hold
+// more CTAs (and rows) than others.  With it, each next CTA takes the slot
+// of one that has finished.  Returns `need` if the cap does not fit.
+size_t cap_residency_smem(int ctas, size_t need) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return need;
+  const size_t per_sm = (size_t)g_device_smem[dev].load(std::memory_order_relaxed);
+  const size_t rsv = (size_t)g_device_smem_rsv[dev].load(std::memory_order_relaxed);
+  if (per_sm == 0) return need;
+  const size_t cap = per_sm / (size_t)(ctas + 1) + 128 - rsv;  // ctas + 1 exceed the SM
+  const size_t want = need > cap ? need : (cap + 127) / 128 * 128;
+  if (want > kTmaMaxSmem || (size_t)ctas * (want + rsv) > per_sm) return need;
+  return want;
 }
 
 // Each launch reports its own error through cudaGetLastError(); clear any
@@ -148,6 +174,7 @@ bool plan_silu_tma_token(int64_t T, int nch, int mode, int sms, SiluTmaPlan *out
   if (smem > kTmaMaxSmem - 1024 || p.block > 1024) return false;
   const int ctas = (p.block <= 512 && 2 * smem <= 220 * 1024) ? 2 : 1;
   p.grid = T < (int64_t)sms * ctas ? T : (int64_t)sms * ctas;
+  p.smem = cap_residency_smem(ctas, smem);
   *out = p;
   return true;
 }
@@ -177,6 +204,7 @@ bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, T
   if (p.block >= 128 && T < 10LL * sms * ctas) ++ctas;
   while (ctas > 1 && (bytes * ctas > 220 * 1024 || ctas * p.block > 1024)) --ctas;
   p.grid = T < (int64_t)sms * ctas ? T : (int64_t)sms * ctas;
+  p.smem = cap_residency_smem(ctas, bytes);
   *out = p;
   return true;
 }
