@@ -139,7 +139,6 @@ struct MlaArgs {
   float inv_n[2];          // 1 / row length
 };
 
-// vpt == -1: the warp-pair-per-token kernel (block/64 tokens per CTA);
 // vpt == 0: the warp-per-token kernel (block/32 tokens per CTA);
 // otherwise the warp-group kernel (rpc tokens per CTA).
 struct MlaPlan {

@@ -57,6 +57,10 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const M
   const uint16_t *w = a.w[side];
   const bool fp8_row = QFP8 && side == 0;
 
+  // Launched with programmatic dependent launch: nothing in global memory
+  // before the previous grid has finished; the next grid may be scheduled
+  // once this one's loads are out.
+  pdl_wait();
   uint4 xv[VPT], wv[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
@@ -69,6 +73,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const M
       wv[k] = make_uint4(0, 0, 0, 0);
     }
   }
+  pdl_launch_dependents();
   float2 t[VPT][4];
   float cmax[VPT];
   RowAcc acc;
@@ -152,10 +157,9 @@ __device__ __forceinline__ void chunk_t(const uint4 &xv, const float2 (&wf)[4], 
   for (int i = 0; i < 4; ++i) t[i] = f2_mul(bf16x2_to_f2(xw[i]), wf[i]);
 }
 
-// Both weights of the warp and warp-pair kernels sit in shared memory as
-// fp32, converted once per CTA (two float4 a chunk), so that neither pass
-// unpacks them again: these kernels are bound by the integer pipe, which
-// does the unpacking.
+// Both weights of the warp kernel sit in shared memory as fp32, converted
+// once per CTA (two float4 a chunk), so that neither pass unpacks them
+// again: the kernel is bound by the integer pipe, which does the unpacking.
 __device__ __forceinline__ void stage_weights_f32(float4 *ws, const MlaArgs &a) {
   for (int i = threadIdx.x; i < a.nch[0] + a.nch[1]; i += blockDim.x) {
     const uint4 wb = i < a.nch[0] ? ld_keep(a.w[0] + i * kElemsPerChunk)
@@ -177,8 +181,14 @@ __device__ __forceinline__ void weights_f32(const float4 *ws, int i, bool in_row
 
 constexpr int kMlaWarpChunks = 8;  // chunks per lane over both rows of a token
 
-template <bool QFP8>
-__global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArgs a, const int kq) {
+// KQ > 0: the rows are exactly KQ * 32 (q) and (8 - KQ) * 32 (kv) chunks
+// wide, known at compile time, so no chunk needs a bounds check or a
+// run-time choice of row (DeepSeek's 1536 + 512 is KQ = 6).  KQ = 0: any
+// widths that fit, with `kq` q chunks per lane at run time.
+template <bool QFP8, int KQ>
+__global__ void __launch_bounds__(256, QFP8 && KQ > 0 ? 3 : 4)
+    mla_dual_norm_warp_kernel(const MlaArgs a, const int kq_rt) {
+  const int kq = KQ > 0 ? KQ : kq_rt;
   __shared__ float4 ws[kMlaWarpChunks * 32 * 2];  // both weights as fp32: q chunks, then kv
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -190,16 +200,18 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArg
 
   // the token's loads go out first, then the CTA stages the weights, so the
   // two round trips overlap
+  pdl_wait();  // programmatic dependent launch, as the kernel above
   uint4 xv[kMlaWarpChunks];
 #pragma unroll
   for (int j = 0; j < kMlaWarpChunks; ++j) {
     const bool q = j < kq;
     const int c = (q ? j : j - kq) * 32 + lane;
-    xv[j] = live && c < (q ? a.nch[0] : a.nch[1])
+    xv[j] = live && (KQ > 0 || c < (q ? a.nch[0] : a.nch[1]))
                 ? ld_stream_ro((q ? src_q : src_kv) + c * kElemsPerChunk)
                 : make_uint4(0, 0, 0, 0);
   }
   stage_weights_f32(ws, a);
+  pdl_launch_dependents();
   __syncthreads();
   if (!live) return;  // whole warps leave together
   RowAcc acc_q, acc_kv;
@@ -209,7 +221,7 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArg
     const bool q = j < kq;
     const int c = (q ? j : j - kq) * 32 + lane;
     float2 wv[4];
-    weights_f32(ws, q ? c : a.nch[0] + c, c < (q ? a.nch[0] : a.nch[1]), wv);
+    weights_f32(ws, q ? c : a.nch[0] + c, KQ > 0 || c < (q ? a.nch[0] : a.nch[1]), wv);
     float2 t[4];
     float cmax;
     if (q) {
@@ -219,18 +231,30 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArg
       pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_kv);
     }
   }
+  // Both sums of squares in one butterfly: after one exchange across the
+  // half-warps, lanes 0-15 hold partial q sums and lanes 16-31 partial kv
+  // sums; each half reduces its row (the same double-float steps in every
+  // lane of a half, so all its lanes agree) and computes that row's inv.
+  // Lane 0 then holds q's, lane 16 kv's.
   float yq, dyq, ykv, dykv;
   {
-    float hi = acc_q.ss.x, lo = acc_q.lo.x + acc_q.lo.y;
-    two_sum_acc(hi, lo, acc_q.ss.y);
-    lanes_sum2(hi, lo, 32);
-    rsqrt_df(hi, lo, a.n[0], a.inv_n[0], a.eps[0], yq, dyq);
-  }
-  {
-    float hi = acc_kv.ss.x, lo = acc_kv.lo.x + acc_kv.lo.y;
-    two_sum_acc(hi, lo, acc_kv.ss.y);
-    lanes_sum2(hi, lo, 32);
-    rsqrt_df(hi, lo, a.n[1], a.inv_n[1], a.eps[1], ykv, dykv);
+    float hq = acc_q.ss.x, lq = acc_q.lo.x + acc_q.lo.y;
+    two_sum_acc(hq, lq, acc_q.ss.y);
+    float hk = acc_kv.ss.x, lk = acc_kv.lo.x + acc_kv.lo.y;
+    two_sum_acc(hk, lk, acc_kv.ss.y);
+    const int side = lane >> 4;  // 0: q, 1: kv
+    float h = side ? hk : hq, l = side ? lk : lq;
+    const float oh = __shfl_xor_sync(0xFFFFFFFFu, side ? hq : hk, 16);
+    const float ol = __shfl_xor_sync(0xFFFFFFFFu, side ? lq : lk, 16);
+    two_sum_acc(h, l, oh);
+    l += ol;
+    lanes_sum2(h, l, 16);
+    float y, dy;
+    rsqrt_df(h, l, a.n[side], a.inv_n[side], a.eps[side], y, dy);
+    yq = __shfl_sync(0xFFFFFFFFu, y, 0);
+    dyq = __shfl_sync(0xFFFFFFFFu, dy, 0);
+    ykv = __shfl_sync(0xFFFFFFFFu, y, 16);
+    dykv = __shfl_sync(0xFFFFFFFFu, dy, 16);
   }
   DynScale d;
   if (QFP8) {
@@ -242,118 +266,7 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_warp_kernel(const MlaArg
     const bool q = j < kq;
     const int c = (q ? j : j - kq) * 32 + lane;
     const int nch = q ? a.nch[0] : a.nch[1];
-    if (c >= nch) continue;
-    float2 wv[4], t[4];
-    weights_f32(ws, q ? c : a.nch[0] + c, true, wv);
-    chunk_t(xv[j], wv, t);
-    const int64_t off = (row * nch + c) * kElemsPerChunk;
-    if (QFP8 && q) {
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 qv = dyn_values(t[e], d);
-        v[2 * e] = qv.x;
-        v[2 * e + 1] = qv.y;
-      }
-      st_stream(a.q8 + off, quant8(v));
-    } else {
-      st_stream((q ? a.out[0] : a.out[1]) + off,
-                bf16x8_product_rn(t, q ? yq : ykv, q ? dyq : dykv));
-    }
-  }
-}
-
-// ------------------------------------------------------ warp-pair kernel
-//
-// Two warps per token for the middle range of T, where one warp per token
-// leaves SM warp slots empty and its ~600-instruction chain per token is
-// the latency: lane L = half * 32 + lane of the pair holds chunks L, L+64,
-// ... of the q row (kq per lane) then of the kv row.  Each warp reduces its
-// half in double-float; the halves meet in shared memory behind a 64-thread
-// named barrier and are combined in the same order by both warps, so both
-// compute identical scales.
-
-constexpr int kMlaPairChunks = 4;  // chunks per lane over both rows of a token
-
-template <bool QFP8>
-__global__ void __launch_bounds__(256, 4) mla_dual_norm_pair_kernel(const MlaArgs a, const int kq) {
-  __shared__ float4 ws[kMlaPairChunks * 64 * 2];  // both weights as fp32: q chunks, then kv
-  __shared__ float4 part[4][2][2];            // [pair][half][side]: sum hi, lo, amax
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int pair = warp >> 1, half = warp & 1, L = half * 32 + lane;
-  const int64_t row = (int64_t)blockIdx.x * 4 + pair;
-  const bool live = row < a.T;  // the same for both warps of a pair
-  const uint16_t *src_q = a.src[0] + (live ? row * a.stride[0] : 0);
-  const uint16_t *src_kv = a.src[1] + (live ? row * a.stride[1] : 0);
-
-  uint4 xv[kMlaPairChunks];
-#pragma unroll
-  for (int j = 0; j < kMlaPairChunks; ++j) {
-    const bool q = j < kq;
-    const int c = (q ? j : j - kq) * 64 + L;
-    xv[j] = live && c < (q ? a.nch[0] : a.nch[1])
-                ? ld_stream_ro((q ? src_q : src_kv) + c * kElemsPerChunk)
-                : make_uint4(0, 0, 0, 0);
-  }
-  stage_weights_f32(ws, a);
-  __syncthreads();
-  if (!live) return;  // both warps of the pair leave together
-  RowAcc acc_q, acc_kv;
-  float am = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMlaPairChunks; ++j) {
-    const bool q = j < kq;
-    const int c = (q ? j : j - kq) * 64 + L;
-    float2 wv[4];
-    weights_f32(ws, q ? c : a.nch[0] + c, c < (q ? a.nch[0] : a.nch[1]), wv);
-    float2 t[4];
-    float cmax;
-    if (q) {
-      pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_q);
-      am = fmaxf(am, cmax);
-    } else {
-      pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_kv);
-    }
-  }
-  float hq = acc_q.ss.x, lq = acc_q.lo.x + acc_q.lo.y;
-  two_sum_acc(hq, lq, acc_q.ss.y);
-  lanes_sum2(hq, lq, 32);
-  float hk = acc_kv.ss.x, lk = acc_kv.lo.x + acc_kv.lo.y;
-  two_sum_acc(hk, lk, acc_kv.ss.y);
-  lanes_sum2(hk, lk, 32);
-  if (QFP8) am = warp_max(am);
-  if (lane == 0) {
-    part[pair][half][0] = make_float4(hq, lq, am, 0.f);
-    part[pair][half][1] = make_float4(hk, lk, 0.f, 0.f);
-  }
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + pair) : "memory");
-  float yq, dyq, ykv, dykv;
-  {
-    const float4 p0 = part[pair][0][0], p1 = part[pair][1][0];
-    float h = p0.x, l = p0.y;
-    two_sum_acc(h, l, p1.x);
-    l += p1.y;
-    rsqrt_df(h, l, a.n[0], a.inv_n[0], a.eps[0], yq, dyq);
-    am = fmaxf(p0.z, p1.z);
-  }
-  {
-    const float4 p0 = part[pair][0][1], p1 = part[pair][1][1];
-    float h = p0.x, l = p0.y;
-    two_sum_acc(h, l, p1.x);
-    l += p1.y;
-    rsqrt_df(h, l, a.n[1], a.inv_n[1], a.eps[1], ykv, dykv);
-  }
-  DynScale d;
-  if (QFP8) {
-    d = make_dyn_scale(am, yq, dyq);
-    if (L == 0) a.q_scale[row] = d.s;
-  }
-#pragma unroll
-  for (int j = 0; j < kMlaPairChunks; ++j) {
-    const bool q = j < kq;
-    const int c = (q ? j : j - kq) * 64 + L;
-    const int nch = q ? a.nch[0] : a.nch[1];
-    if (c >= nch) continue;
+    if (KQ == 0 && c >= nch) continue;
     float2 wv[4], t[4];
     weights_f32(ws, q ? c : a.nch[0] + c, true, wv);
     chunk_t(xv[j], wv, t);
@@ -376,11 +289,10 @@ __global__ void __launch_bounds__(256, 4) mla_dual_norm_pair_kernel(const MlaArg
 
 template <int VPT, bool BIG>
 cudaError_t launch_vpt(const MlaArgs &a, bool q_fp8, const MlaPlan &p, cudaStream_t s) {
+  const dim3 g((unsigned)p.grid), b((unsigned)p.block);
   if (q_fp8)
-    mla_dual_norm_kernel<VPT, true, BIG><<<(unsigned)p.grid, p.block, 0, s>>>(a);
-  else
-    mla_dual_norm_kernel<VPT, false, BIG><<<(unsigned)p.grid, p.block, 0, s>>>(a);
-  return cudaGetLastError();
+    return launch_pdl(mla_dual_norm_kernel<VPT, true, BIG>, g, b, 0, s, a);
+  return launch_pdl(mla_dual_norm_kernel<VPT, false, BIG>, g, b, 0, s, a);
 }
 
 }  // namespace
@@ -389,21 +301,14 @@ cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaSt
   a.thr[0] = p.thr[0];
   a.thr[1] = p.thr[1];
   a.rpc = p.rpc;
-  if (p.vpt < 0) {  // one warp pair per token
-    const int kq = (a.nch[0] + 63) / 64;
-    if (q_fp8)
-      mla_dual_norm_pair_kernel<true><<<(unsigned)p.grid, p.block, 0, s>>>(a, kq);
-    else
-      mla_dual_norm_pair_kernel<false><<<(unsigned)p.grid, p.block, 0, s>>>(a, kq);
-    return cudaGetLastError();
-  }
+  const dim3 g((unsigned)p.grid), b((unsigned)p.block);
   if (p.vpt == 0) {  // one warp per token
     const int kq = (a.nch[0] + 31) / 32;
-    if (q_fp8)
-      mla_dual_norm_warp_kernel<true><<<(unsigned)p.grid, p.block, 0, s>>>(a, kq);
-    else
-      mla_dual_norm_warp_kernel<false><<<(unsigned)p.grid, p.block, 0, s>>>(a, kq);
-    return cudaGetLastError();
+    if (a.nch[0] == 6 * 32 && a.nch[1] == 2 * 32)  // DeepSeek's latent widths
+      return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, 6>, g, b, 0, s, a, kq)
+                   : launch_pdl(mla_dual_norm_warp_kernel<false, 6>, g, b, 0, s, a, kq);
+    return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, 0>, g, b, 0, s, a, kq)
+                 : launch_pdl(mla_dual_norm_warp_kernel<false, 0>, g, b, 0, s, a, kq);
   }
   switch (p.vpt) {
     case 1: return launch_vpt<1, false>(a, q_fp8, p, s);

@@ -213,24 +213,13 @@ bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, T
 // warp (DeepSeek's 1536 + 512 exactly): one warp per token, eight tokens per
 // CTA -- the fewest instructions per element, but about 6 us of latency per
 // token, so it pays from about 13 tokens per SM (measured: from T ~ 2048 on
-// 152 SMs).  Between 13 and 40 tokens per SM, rows that fit four chunks per
-// lane of a warp pair run a warp pair per token (shorter chain, twice the
-// warps; measured 2-8 % faster at T = 2048-4096, slower from T = 8192).
-// Otherwise a token's rows spread over a warp group: one token
+// 152 SMs).  Otherwise a token's rows spread over a warp group: one token
 // per CTA and one chunk per thread for few tokens (the shortest chain); two
 // chunks per thread and tokens packed into CTAs of up to 512 threads for
 // more.  A token's group stays within 512 threads up to four chunks per
 // thread (eight allow 1024).
 MlaPlan plan_mla(int64_t T, int nq, int nkv, int sms) {
   MlaPlan p;
-  if ((nq + 63) / 64 + (nkv + 63) / 64 <= 4 && T >= 13LL * sms && T < 40LL * sms) {
-    p.vpt = -1;
-    p.thr[0] = p.thr[1] = 0;
-    p.rpc = 4;
-    p.block = 256;
-    p.grid = (T + 3) / 4;
-    return p;
-  }
   if ((nq + 31) / 32 + (nkv + 31) / 32 <= 8 && T >= 13LL * sms) {
     p.vpt = 0;
     p.thr[0] = p.thr[1] = 0;
@@ -368,8 +357,9 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
   if (vg::plan_norm_tma(num_tokens, (int)hidden, residual != nullptr, mode, a.ngroups, sms, &tp))
     return vg::launch_norm_fp8_tma(a, mode, tp, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                      : VG_ERR_CUDA;
-  // Dynamic scales do more work per row: more chunks per thread amortise it.
-  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, mode == VG_SCALE_STATIC ? 2 : 4, sms);
+  // Two chunks a thread in both scale modes (measured on GB300 for dynamic
+  // scales at 2-4 rows per SM: 6-7 % faster than four chunks a thread).
+  const vg::RowPlan plan = vg::plan_rows(num_tokens, a.nch, 2, sms);
   return vg::launch_norm_fp8(a, mode, plan, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                    : VG_ERR_CUDA;
 }
