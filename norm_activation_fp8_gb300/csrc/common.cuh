@@ -31,6 +31,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
   return d;
 }
 
+// bf16(a + b) for two bf16 pairs: the exact sum rounded once to nearest
+// even (IEEE addition in the bf16 format, subnormals kept), one instruction.
+__device__ __forceinline__ uint32_t add_bf16x2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // ------------------------------------------------------------------ fp8
 
 // Two fp32 -> two E4M3 codes, RNE with saturation to +-448 (NaN -> 0x7F),

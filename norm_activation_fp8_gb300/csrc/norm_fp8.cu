@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(512) norm_fp8_kernel(const NormArgs a) {
   RowAcc acc;
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
-    const uint4 ow = pass1_chunk<DYN, RES>(xv[k], rv[k], wv[k], t[k], cmax[k], acc);
+    const uint4 ow = pass1_chunk<DYN, RES, true>(xv[k], rv[k], wv[k], t[k], cmax[k], acc);
     const int c = lr + k * a.ntr;
     if (RES && live && c < a.nch) st_stream(a.res_out + base + c * kElemsPerChunk, ow);
   }

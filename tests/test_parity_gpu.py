@@ -322,3 +322,26 @@ def test_device_status_clean_after_runs():
     run_norm(d["x"], d["residual"], d["weight"], 1e-5, PER_GROUP, 128)
     assert vg.vg_device_status(reset=True) == 0
     assert vg.vg_device_status() == 0
+
+
+@pytest.mark.parametrize("pairing", ["shuffled", "negated_neighbour", "subnormal"])
+def test_residual_add_every_bf16_pattern(pairing):
+    """residual_out = bf16(x + residual) for every one of the 65536 bf16 bit
+    patterns as x (NaNs, infinities, subnormals, both zeros), against the
+    oracle: bit-exact, NaNs by class.  The partner residuals make the sums
+    cancel to zero or to subnormals, overflow, and round at every
+    exponent."""
+    rng = np.random.default_rng({"shuffled": 1, "negated_neighbour": 2, "subnormal": 3}[pairing])
+    x = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    if pairing == "shuffled":
+        res = rng.permutation(x)
+    elif pairing == "negated_neighbour":  # -(x + one ulp either way): cancellation
+        res = ((x ^ 0x8000).astype(np.int32) + rng.integers(-1, 2, x.size)).astype(np.uint16)
+    else:  # subnormal and tiny partners
+        res = (rng.integers(0, 0x0100, x.size) | (rng.integers(0, 2, x.size) << 15)).astype(np.uint16)
+    T, H = 64, 1024
+    x, res = x.reshape(T, H), res.reshape(T, H)
+    w = _bits(np.ones(H))
+    g = parity.gpu_norm(x, res, w, 1e-5, STATIC, scale=0.05)
+    o = parity.oracle_norm(x, res, w, 1e-5, STATIC, scale=0.05)
+    parity.compare_bf16_exact(g["residual_out"], o["residual_out"], "residual_out")
