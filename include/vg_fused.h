@@ -43,12 +43,14 @@
  *     synchronises, and launches only on `stream` (NULL = legacy default
  *     stream).  Calls are asynchronous and may be captured in a CUDA graph.
  *   - Stream order: every output is visible to whatever runs after the call
- *     in stream order.  Most kernels are launched with programmatic
- *     dependent launch (the non-persistent ones): such a kernel may start
- *     while the previous kernel in the stream is still draining, waits for
- *     it (griddepcontrol.wait) before it reads or writes any memory, and
- *     signals griddepcontrol.launch_dependents once its loads are issued --
- *     before q, scale and residual_out are written.  A consumer launched
+ *     in stream order.  Every kernel is launched with programmatic
+ *     dependent launch: it may start while the previous kernel in the
+ *     stream is still draining, waits for it (griddepcontrol.wait) before
+ *     it reads or writes any memory -- it only asks its first input rows
+ *     into L2 before the wait, which cannot return stale data, since L2
+ *     also takes every write of the previous kernel -- and signals
+ *     griddepcontrol.launch_dependents once its loads are issued, before
+ *     q, scale and residual_out are written.  A consumer launched
  *     after it with programmatic dependent launch too must therefore wait
  *     on the grid dependency (cudaGridDependencySynchronize() or
  *     griddepcontrol.wait) before it reads these outputs; an ordinary

@@ -85,6 +85,22 @@ __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Asks for [p, p + bytes) to be brought into L2: bulk prefetches of at most
+// 16 KB each, with no destination and nothing to wait for.  p must be
+// 16-byte aligned and bytes a multiple of 16.  A CTA issues this for its
+// first rows before pdl_wait(), so that their DRAM round trip overlaps the
+// previous grid's drain.  It cannot make the CTA read stale data: the
+// prefetch only fills L2, the device's point of coherence, which also takes
+// every write of the previous grid, and the CTA's own loads come after the
+// wait.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  const char *c = static_cast<const char *>(p);
+  for (uint32_t off = 0; off < bytes; off += 16384u) {
+    const uint32_t n = bytes - off < 16384u ? bytes - off : 16384u;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(n) : "memory");
+  }
+}
+
 // -------------------------------------------------------------- memory ops
 
 // Read-only data streamed once: non-coherent path, no L1 allocation.

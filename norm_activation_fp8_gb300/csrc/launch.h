@@ -59,6 +59,8 @@ struct NormArgs {
   int32_t s_gs;
   int32_t ue8m0;
   uint8_t *sf8;    // kNvfp4: E4M3 block scale codes [T, H/16]; q holds [T, H/2]
+  int32_t pf_ctas; // CTAs below this index prefetch their first rows into L2
+  int32_t fastq;   // dynamic FP8 codes in the two-multiply form where allowed
 };
 
 struct SiluArgs {
@@ -76,6 +78,7 @@ struct SiluArgs {
   int32_t s_gs;
   int32_t ue8m0;   // power-of-two per-group scales
   uint8_t *sf8;    // kNvfp4: E4M3 block scale codes [T, I/16]; q holds [T, I/2]
+  int32_t pf_ctas; // CTAs below this index prefetch their first rows into L2
 };
 
 cudaError_t launch_norm_fp8(NormArgs a, int mode, const RowPlan &plan, cudaStream_t stream);
@@ -137,18 +140,20 @@ struct MlaArgs {
   float eps[2];
   float n[2];              // row lengths
   float inv_n[2];          // 1 / row length
+  int32_t pf_ctas;         // CTAs below this index prefetch their rows into L2
 };
 
 // vpt == 0: the warp-per-token kernel (block/32 tokens per CTA);
 // otherwise the warp-group kernel (rpc tokens per CTA).
 struct MlaPlan {
+  bool stage = false;  // warp kernel: the token's chunks staged in shared memory
   int vpt;
   int thr[2];
   int rpc;
   int block;
   int64_t grid;
 };
-MlaPlan plan_mla(int64_t T, int nq, int nkv, int sms);
+MlaPlan plan_mla(int64_t T, int nq, int nkv, bool q_fp8, int sms);
 cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaStream_t s);
 
 // QK norm + RoPE, in place on qkv [T, row] with row = (hq + 2 hkv) * D.
@@ -164,6 +169,7 @@ struct QkArgs {
   int32_t nh;            // heads normalised: hq + hkv
   int32_t hq;
   float eps;
+  int32_t pf_ctas;       // tokens below this index prefetch their heads into L2
 };
 // Device status bit of the rope kernel: a position outside [0, max_pos).
 constexpr uint32_t kErrBadPosition = 2u;

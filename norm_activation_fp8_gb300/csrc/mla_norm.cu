@@ -26,19 +26,21 @@
 // hi + lo and only hi is rounded, after hi has been moved one fp32 ulp toward
 // lo when it sits exactly on a bf16 midpoint.  The fp8 q row uses the exact
 // dynamic-scale arithmetic of dyn_scale.cuh.
+#include <type_traits>
+
 #include "common.cuh"
 #include "dyn_scale.cuh"
 #include "launch.h"
 #include "row_norm.cuh"
+#include "tma.cuh"
 
 namespace vg {
 
 namespace {
 
-// CTAs of up to 512 threads leave room for the fp8 q row's state at up to
-// eight chunks per thread; a token wider than 512 threads (BIG) takes 1024.
-template <int VPT, bool QFP8, bool BIG>
-__global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const MlaArgs a) {
+// The body of the warp-group kernel (wrappers below).
+template <int VPT, bool QFP8>
+__device__ __forceinline__ void mla_dual_norm_rows(const MlaArgs &a) {
   __shared__ float4 red[32];      // per warp: sum hi, sum lo, amax
   __shared__ float2 inv[32][2];   // per token slot and side: y, dy
   __shared__ DynScale dq[32];     // per token slot: the q row's fp8 scale
@@ -58,8 +60,9 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const M
   const bool fp8_row = QFP8 && side == 0;
 
   // Launched with programmatic dependent launch: nothing in global memory
-  // before the previous grid has finished; the next grid may be scheduled
-  // once this one's loads are out.
+  // before the previous grid has finished (the row is only asked into L2);
+  // the next grid may be scheduled once this one's loads are out.
+  if (lr == 0 && live && (int)blockIdx.x < a.pf_ctas) prefetch_l2(src, 16u * (uint32_t)nch);
   pdl_wait();
   uint4 xv[VPT], wv[VPT];
 #pragma unroll
@@ -115,17 +118,22 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const M
   if (fp8_row) {
     const DynScale d = dq[slot];
     uint8_t *out = a.q8 + (live ? row * (int64_t)nch * kElemsPerChunk : 0);
+    if (two_multiply_ok(d)) {  // all but degenerate rows
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      const int c = lr + k * ntr;
-      float v[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 q = dyn_values(t[k][i], d);
-        v[2 * i] = q.x;
-        v[2 * i + 1] = q.y;
+      for (int k = 0; k < VPT; ++k) {
+        const int c = lr + k * ntr;
+        float v[8];
+        dyn_values8_fast(t[k], d.rf, v);
+        if (live && c < nch) st_stream(out + c * kElemsPerChunk, quant8(v));
       }
-      if (live && c < nch) st_stream(out + c * kElemsPerChunk, quant8(v));
+    } else {
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const int c = lr + k * ntr;
+        float v[8];
+        dyn_values8_exact(t[k], d, v);
+        if (live && c < nch) st_stream(out + c * kElemsPerChunk, quant8(v));
+      }
     }
   } else {
     const float2 yd = inv[slot][side];
@@ -137,6 +145,18 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512) mla_dual_norm_kernel(const M
       if (live && c < nch) st_stream(out + c * kElemsPerChunk, o);
     }
   }
+}
+
+// CTAs of up to 512 threads leave room for the fp8 q row's state at up to
+// eight chunks per thread; a token wider than 512 threads takes a CTA of
+// 1024 (one per SM, so up to 64 registers a thread).
+template <int VPT, bool QFP8>
+__global__ void __launch_bounds__(512) mla_dual_norm_kernel(const MlaArgs a) {
+  mla_dual_norm_rows<VPT, QFP8>(a);
+}
+template <int VPT, bool QFP8>
+__global__ void __launch_bounds__(1024, 1) mla_dual_norm_kernel_big(const MlaArgs a) {
+  mla_dual_norm_rows<VPT, QFP8>(a);
 }
 
 // ----------------------------------------------------------- warp kernel
@@ -181,15 +201,30 @@ __device__ __forceinline__ void weights_f32(const float4 *ws, int i, bool in_row
 
 constexpr int kMlaWarpChunks = 8;  // chunks per lane over both rows of a token
 
+// 16-byte asynchronous copy global -> shared (no register staging); a
+// source size of 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(void *dst_smem, const void *src, bool full) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst_smem)), "l"(src),
+               "r"(full ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // KQ > 0: the rows are exactly KQ * 32 (q) and (8 - KQ) * 32 (kv) chunks
 // wide, known at compile time, so no chunk needs a bounds check or a
 // run-time choice of row (DeepSeek's 1536 + 512 is KQ = 6).  KQ = 0: any
 // widths that fit, with `kq` q chunks per lane at run time.
-template <bool QFP8, int KQ>
-__global__ void __launch_bounds__(256, QFP8 && KQ > 0 ? 3 : 4)
+// STAGE: the token's chunks go to shared memory by asynchronous copies and
+// both passes read them there, instead of 32 registers a lane holding them
+// from the loads to the stores, so that more warps fit on an SM.
+template <bool QFP8, int KQ, bool STAGE = false>
+__global__ void __launch_bounds__(256, STAGE ? (QFP8 ? 4 : 5) : (QFP8 && KQ > 0 ? 3 : 4))
     mla_dual_norm_warp_kernel(const MlaArgs a, const int kq_rt) {
   const int kq = KQ > 0 ? KQ : kq_rt;
   __shared__ float4 ws[kMlaWarpChunks * 32 * 2];  // both weights as fp32: q chunks, then kv
+  __shared__ uint4 xs[STAGE ? 8 : 1][kMlaWarpChunks][32];  // STAGE: per warp, per chunk, per lane
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const bool live = row < a.T;  // warp-uniform
@@ -200,20 +235,34 @@ __global__ void __launch_bounds__(256, QFP8 && KQ > 0 ? 3 : 4)
 
   // the token's loads go out first, then the CTA stages the weights, so the
   // two round trips overlap
+  if (lane == 0 && live && (int)blockIdx.x < a.pf_ctas) {  // both rows into L2 before the wait
+    prefetch_l2(src_q, 16u * (uint32_t)a.nch[0]);
+    prefetch_l2(src_kv, 16u * (uint32_t)a.nch[1]);
+  }
   pdl_wait();  // programmatic dependent launch, as the kernel above
-  uint4 xv[kMlaWarpChunks];
+  uint4 xv[STAGE ? 1 : kMlaWarpChunks];
+  uint4 (&xw)[kMlaWarpChunks][32] = xs[STAGE ? threadIdx.x >> 5 : 0];
 #pragma unroll
   for (int j = 0; j < kMlaWarpChunks; ++j) {
     const bool q = j < kq;
     const int c = (q ? j : j - kq) * 32 + lane;
-    xv[j] = live && (KQ > 0 || c < (q ? a.nch[0] : a.nch[1]))
-                ? ld_stream_ro((q ? src_q : src_kv) + c * kElemsPerChunk)
-                : make_uint4(0, 0, 0, 0);
+    const bool in = live && (KQ > 0 || c < (q ? a.nch[0] : a.nch[1]));
+    const uint16_t *src = (q ? src_q : src_kv) + (in ? c * kElemsPerChunk : 0);
+    if constexpr (STAGE)
+      cp_async16(&xw[j][lane], src, in);
+    else
+      xv[j] = in ? ld_stream_ro(src) : make_uint4(0, 0, 0, 0);
   }
   stage_weights_f32(ws, a);
   pdl_launch_dependents();
+  if constexpr (STAGE) cp_async_wait_all();  // this lane's own copies
   __syncthreads();
   if (!live) return;  // whole warps leave together
+  // chunk j of this lane: from registers, or from its own slots in shared memory
+  auto chunk = [&](int j) -> uint4 {
+    if constexpr (STAGE) return lds128(&xw[j][lane]);
+    else return xv[j];
+  };
   RowAcc acc_q, acc_kv;
   float am = 0.f;
 #pragma unroll
@@ -224,11 +273,12 @@ __global__ void __launch_bounds__(256, QFP8 && KQ > 0 ? 3 : 4)
     weights_f32(ws, q ? c : a.nch[0] + c, KQ > 0 || c < (q ? a.nch[0] : a.nch[1]), wv);
     float2 t[4];
     float cmax;
+    const uint4 x = chunk(j);
     if (q) {
-      pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_q);
+      pass1_chunk<true, false>(x, x, wv, t, cmax, acc_q);
       am = fmaxf(am, cmax);
     } else {
-      pass1_chunk<true, false>(xv[j], xv[j], wv, t, cmax, acc_kv);
+      pass1_chunk<true, false>(x, x, wv, t, cmax, acc_kv);
     }
   }
   // Both sums of squares in one butterfly: after one exchange across the
@@ -261,38 +311,48 @@ __global__ void __launch_bounds__(256, QFP8 && KQ > 0 ? 3 : 4)
     d = make_dyn_scale(warp_max(am), yq, dyq);
     if (lane == 0) a.q_scale[row] = d.s;
   }
+  // Pass 2, with the q row's FP8 codes in the two-multiply form when the
+  // token's scale has a tie direction (all but degenerate rows; the choice
+  // is made once, so that the common loop has no branch).
+  auto pass2 = [&](auto fast) {
 #pragma unroll
-  for (int j = 0; j < kMlaWarpChunks; ++j) {
-    const bool q = j < kq;
-    const int c = (q ? j : j - kq) * 32 + lane;
-    const int nch = q ? a.nch[0] : a.nch[1];
-    if (KQ == 0 && c >= nch) continue;
-    float2 wv[4], t[4];
-    weights_f32(ws, q ? c : a.nch[0] + c, true, wv);
-    chunk_t(xv[j], wv, t);
-    const int64_t off = (row * nch + c) * kElemsPerChunk;
-    if (QFP8 && q) {
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 qv = dyn_values(t[e], d);
-        v[2 * e] = qv.x;
-        v[2 * e + 1] = qv.y;
+    for (int j = 0; j < kMlaWarpChunks; ++j) {
+      const bool q = j < kq;
+      const int c = (q ? j : j - kq) * 32 + lane;
+      const int nch = q ? a.nch[0] : a.nch[1];
+      if (KQ == 0 && c >= nch) continue;
+      float2 wv[4], t[4];
+      weights_f32(ws, q ? c : a.nch[0] + c, true, wv);
+      chunk_t(chunk(j), wv, t);
+      const int64_t off = (row * nch + c) * kElemsPerChunk;
+      if (QFP8 && q) {
+        float v[8];
+        if (decltype(fast)::value)
+          dyn_values8_fast(t, d.rf, v);
+        else
+          dyn_values8_exact(t, d, v);
+        st_stream(a.q8 + off, quant8(v));
+      } else {
+        st_stream((q ? a.out[0] : a.out[1]) + off,
+                  bf16x8_product_rn(t, q ? yq : ykv, q ? dyq : dykv));
       }
-      st_stream(a.q8 + off, quant8(v));
-    } else {
-      st_stream((q ? a.out[0] : a.out[1]) + off,
-                bf16x8_product_rn(t, q ? yq : ykv, q ? dyq : dykv));
     }
-  }
+  };
+  if (QFP8 && two_multiply_ok(d))
+    pass2(std::true_type{});
+  else
+    pass2(std::false_type{});
 }
 
 template <int VPT, bool BIG>
 cudaError_t launch_vpt(const MlaArgs &a, bool q_fp8, const MlaPlan &p, cudaStream_t s) {
   const dim3 g((unsigned)p.grid), b((unsigned)p.block);
-  if (q_fp8)
-    return launch_pdl(mla_dual_norm_kernel<VPT, true, BIG>, g, b, 0, s, a);
-  return launch_pdl(mla_dual_norm_kernel<VPT, false, BIG>, g, b, 0, s, a);
+  if constexpr (BIG)
+    return q_fp8 ? launch_pdl(mla_dual_norm_kernel_big<VPT, true>, g, b, 0, s, a)
+                 : launch_pdl(mla_dual_norm_kernel_big<VPT, false>, g, b, 0, s, a);
+  else
+    return q_fp8 ? launch_pdl(mla_dual_norm_kernel<VPT, true>, g, b, 0, s, a)
+                 : launch_pdl(mla_dual_norm_kernel<VPT, false>, g, b, 0, s, a);
 }
 
 }  // namespace
@@ -304,9 +364,13 @@ cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaSt
   const dim3 g((unsigned)p.grid), b((unsigned)p.block);
   if (p.vpt == 0) {  // one warp per token
     const int kq = (a.nch[0] + 31) / 32;
-    if (a.nch[0] == 6 * 32 && a.nch[1] == 2 * 32)  // DeepSeek's latent widths
+    if (a.nch[0] == 6 * 32 && a.nch[1] == 2 * 32) {  // DeepSeek's latent widths
+      if (p.stage)
+        return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, 6, true>, g, b, 0, s, a, kq)
+                     : launch_pdl(mla_dual_norm_warp_kernel<false, 6, true>, g, b, 0, s, a, kq);
       return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, 6>, g, b, 0, s, a, kq)
                    : launch_pdl(mla_dual_norm_warp_kernel<false, 6>, g, b, 0, s, a, kq);
+    }
     return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, 0>, g, b, 0, s, a, kq)
                  : launch_pdl(mla_dual_norm_warp_kernel<false, 0>, g, b, 0, s, a, kq);
   }

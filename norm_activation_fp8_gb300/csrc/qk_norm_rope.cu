@@ -63,6 +63,15 @@ __global__ void __launch_bounds__(512) qk_norm_rope_kernel(const QkArgs a) {
   const int l = lane & (G - 1);
   const int64_t t = blockIdx.x;
   const int h = ((int)blockIdx.y * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5)) * (32 / G) + lane / G;
+  // Launched with programmatic dependent launch: nothing in global memory
+  // before the previous grid has finished, except that the CTA's heads are
+  // asked into L2 first; the next grid may be scheduled once the loads are out.
+  if (threadIdx.x == 0 && (int)blockIdx.x < a.pf_ctas) {
+    const int h0 = (int)blockIdx.y * (int)(blockDim.x >> 5) * (32 / G);
+    const int nh = a.nh - h0 < (int)(blockDim.x >> 5) * (32 / G) ? a.nh - h0 : (int)(blockDim.x >> 5) * (32 / G);
+    prefetch_l2(a.qkv + t * a.row + (int64_t)h0 * D, 2u * (uint32_t)(nh * D));
+  }
+  pdl_wait();
   const int64_t pos = a.pos[t];
   const bool live = h < a.nh && pos >= 0 && pos < a.max_pos;  // same for the head's lanes
   if (h < a.nh && !live && l == 0) atomicOr(&g_rope_status, kErrBadPosition);
@@ -74,6 +83,7 @@ __global__ void __launch_bounds__(512) qk_norm_rope_kernel(const QkArgs a) {
   const uint4 xb = live ? ld_stream(head + (l + G) * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
   const uint4 wa = live ? ld_keep(w + l * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
   const uint4 wb = live ? ld_keep(w + (l + G) * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
+  pdl_launch_dependents();
   float2 ta[4], tb[4];
   float cmax;
   RowAcc acc;
@@ -159,11 +169,8 @@ cudaError_t launch_g(const QkArgs &a, bool neox, cudaStream_t s) {
   int warps = (a.nh + heads_per_warp - 1) / heads_per_warp;
   if (warps > 16) warps = 16;
   const dim3 grid((unsigned)a.T, (unsigned)((a.nh + warps * heads_per_warp - 1) / (warps * heads_per_warp)));
-  if (neox)
-    qk_norm_rope_kernel<G, true><<<grid, warps * 32, 0, s>>>(a);
-  else
-    qk_norm_rope_kernel<G, false><<<grid, warps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return neox ? launch_pdl(qk_norm_rope_kernel<G, true>, grid, dim3(warps * 32), 0, s, a)
+              : launch_pdl(qk_norm_rope_kernel<G, false>, grid, dim3(warps * 32), 0, s, a);
 }
 
 }  // namespace

@@ -210,11 +210,6 @@ template <int VPT, int MODE, int GCH, bool BIG, bool OPT = false>
 __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken ? 2 : 3))
     silu_fp8_kernel(const SiluArgs a) {
   __shared__ float red[32];
-  // Launched with programmatic dependent launch: the next grid is scheduled
-  // while this one drains (measured 2-15 % faster back to back; the
-  // persistent TMA kernels keep plain launches, slower with it).
-  pdl_wait();
-
   const int tid = threadIdx.x;
   const int slot = tid / a.ntr;
   const int lr0 = tid - slot * a.ntr;
@@ -223,6 +218,16 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
   const bool live = row < a.T;
   const int64_t in_base = live ? row * 2 * a.I : 0;
   const int64_t out_base = live ? row * a.I : 0;
+  // Launched with programmatic dependent launch: the next grid is scheduled
+  // while this one drains, and its first CTAs ask for their segment of the
+  // row into L2 before they wait for this one to finish.
+  if (lr0 == 0 && live && (int)blockIdx.x < a.pf_ctas && lr < a.nch) {
+    const int c1 = lr + a.ntr * VPT < a.nch ? lr + a.ntr * VPT : a.nch;
+    const uint32_t bytes = 16u * (uint32_t)(c1 - lr);
+    prefetch_l2(a.gate_up + in_base + lr * kElemsPerChunk, bytes);
+    prefetch_l2(a.gate_up + in_base + a.I + lr * kElemsPerChunk, bytes);
+  }
+  pdl_wait();
 
   uint4 gv[VPT], uv[VPT];
 #pragma unroll
@@ -392,8 +397,11 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
   }
   __syncthreads();
   // Programmatic dependent launch, as the persistent norm kernel: nothing in
-  // global memory before the previous grid has finished; the next grid's
-  // CTAs take the slots of this one's as they exit.
+  // global memory before the previous grid has finished (its first row is
+  // only asked into L2); the next grid's CTAs take the slots of this one's
+  // as they exit.
+  if (tid == 0 && first < a.T && a.pf_ctas > 0)
+    prefetch_l2(a.gate_up + first * 2 * a.I, 4u * (uint32_t)a.I);
   pdl_wait();
   if (tid == 0 && first < a.T)
     for (int sg = 0; sg < NSEG; ++sg) issue(sg, first);

@@ -218,9 +218,15 @@ bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, T
 // chunks per thread and tokens packed into CTAs of up to 512 threads for
 // more.  A token's group stays within 512 threads up to four chunks per
 // thread (eight allow 1024).
-MlaPlan plan_mla(int64_t T, int nq, int nkv, int sms) {
+MlaPlan plan_mla(int64_t T, int nq, int nkv, bool q_fp8, int sms) {
   MlaPlan p;
   if ((nq + 31) / 32 + (nkv + 31) / 32 <= 8 && T >= 13LL * sms) {
+    // The token's chunks go through shared memory (DeepSeek's widths): for
+    // bf16 at every T here, for an fp8 q from 40 tokens per SM.  Measured
+    // on GB300: bf16 0.41 -> 0.46 (T = 2048), 0.71 -> 0.81 (8192), 0.89 ->
+    // 0.99 (32768), equal at 4096; fp8 0.58 -> 0.58 (8192), 0.68 -> 0.71
+    // (32768), but 0.47 -> 0.44 at 4096.
+    p.stage = !q_fp8 || T >= 40LL * sms;
     p.vpt = 0;
     p.thr[0] = p.thr[1] = 0;
     p.rpc = 8;
@@ -267,6 +273,7 @@ vg_status mla_dual_norm(uint16_t *q_out, uint8_t *q_fp8, float *q_scale, uint16_
   clear_stale_error();
 
   MlaArgs a{};
+  a.pf_ctas = 2 * sms;
   a.src[0] = q_c;
   a.src[1] = kv_c;
   a.w[0] = q_weight;
@@ -286,7 +293,7 @@ vg_status mla_dual_norm(uint16_t *q_out, uint8_t *q_fp8, float *q_scale, uint16_
   a.n[1] = (float)kv_dim;
   a.inv_n[0] = 1.0f / (float)q_dim;
   a.inv_n[1] = 1.0f / (float)kv_dim;
-  const MlaPlan p = plan_mla(T, a.nch[0], a.nch[1], sms);
+  const MlaPlan p = plan_mla(T, a.nch[0], a.nch[1], fp8, sms);
   return launch_mla_dual_norm(a, fp8, p, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                : VG_ERR_CUDA;
 }
@@ -339,6 +346,7 @@ vg_status vg_fused_add_rms_norm_fp8(uint8_t *q, uint16_t *residual_out, float *s
   vg::clear_stale_error();
 
   vg::NormArgs a{};
+  a.pf_ctas = 2 * sms;
   a.q = q;
   a.res_out = residual_out;
   a.scale = scale;
@@ -385,6 +393,7 @@ vg_status vg_fused_add_rms_norm_nvfp4(uint8_t *q4, uint8_t *block_scale, uint16_
   vg::clear_stale_error();
 
   vg::NormArgs a{};
+  a.pf_ctas = 2 * sms;
   a.q = q4;
   a.sf8 = block_scale;
   a.res_out = residual_out;
@@ -432,6 +441,7 @@ vg_status vg_fused_add_rms_norm_pad(uint16_t *out, uint16_t *residual_out, const
   vg::clear_stale_error();
 
   vg::NormArgs a{};
+  a.pf_ctas = 2 * sms;
   a.res_out = residual_out;
   a.x = x;
   a.res = residual;
@@ -481,6 +491,7 @@ vg_status vg_fused_qk_norm_rope(uint16_t *qkv, const uint16_t *q_weight, const u
   vg::clear_stale_error();
 
   vg::QkArgs a{};
+  a.pf_ctas = 2 * sms;
   a.qkv = qkv;
   a.qw = q_weight;
   a.kw = k_weight;
@@ -511,6 +522,7 @@ vg_status vg_silu_mul_fp8(uint8_t *q, float *scale, const uint16_t *gate_up, int
   vg::clear_stale_error();
 
   vg::SiluArgs a{};
+  a.pf_ctas = 2 * sms;
   a.q = q;
   a.scale = scale;
   a.gate_up = gate_up;
@@ -544,6 +556,7 @@ vg_status vg_silu_mul_nvfp4(uint8_t *q4, uint8_t *block_scale, const uint16_t *g
   vg::clear_stale_error();
 
   vg::SiluArgs a{};
+  a.pf_ctas = 2 * sms;
   a.q = q4;
   a.sf8 = block_scale;
   a.scale = const_cast<float *>(global_scale);  // read only in this mode

@@ -1,0 +1,79 @@
+"""Exact e4m3 ties under dynamic scales, on every launch form.
+
+The dynamic norms code each element from Q = 448 t / amax (t = r * w).  Rows
+of +-1 with a weight built from multiples of 7/64 whose largest magnitude is
+1.75 make Q = 256 t a multiple of 28: Q = 84, 168 and 336 sit exactly on
+e4m3 midpoints.  With eps = 0, inv is exactly 1 and the stored scale
+s = 1.75 / 448 = 2^-8 is exact, so no direction is recorded and those ties
+go to even (the quotient form).  With eps = 1e-5 the scale is rounded, the
+ties follow its rounding direction, and the two-multiply form applies where
+the launch allows it.  The GPU's codes and scales must equal the oracle's
+bit for bit in the register kernel, the persistent kernel with 128-thread
+rows (two-multiply form) and with 256-thread rows (quotient form), and in
+the MLA dual norm's fp8 q row, registers and shared-memory staging
+("Fusion torch.compile passes", sections "RMSNorm + Quantization" and "MLA
+Dual RMSNorm")."""
+import numpy as np
+import pytest
+
+import gen
+import parity
+
+pytestmark = pytest.mark.gpu
+
+PER_TOKEN, PER_GROUP = gen.PER_TOKEN, gen.PER_GROUP
+
+
+def tie_rows(T, n, seed):
+    rng = np.random.default_rng(seed)
+    x = np.where(rng.random((T, n)) < 0.5, -1.0, 1.0).astype(np.float32)
+    return gen.to_bf16_bits(x)
+
+
+def tie_weight(n, group, seed):
+    """Multiples of 7/64 up to 1.75 (exact in bf16), 1.75 at the start of
+    every group of `group` columns so that each group's amax is 1.75."""
+    rng = np.random.default_rng(seed)
+    w = (7.0 / 64.0) * rng.integers(1, 17, n)
+    w *= np.where(rng.random(n) < 0.5, -1.0, 1.0)
+    w[::group] = 1.75
+    return gen.to_bf16_bits(w.astype(np.float32))
+
+
+NORM = [(96, 1024), (1000, 4096), (700, 8192)]  # register, persistent x 128, persistent x 256
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-5], ids=["no-direction", "direction"])
+@pytest.mark.parametrize("mode,G", [(PER_TOKEN, 128), (PER_GROUP, 128), (PER_GROUP, 64)],
+                         ids=["token", "group128", "group64"])
+@pytest.mark.parametrize("T,H", NORM, ids=[f"{t}x{h}" for t, h in NORM])
+def test_norm_exact_ties(T, H, mode, G, eps):
+    x = tie_rows(T, H, seed=T + H)
+    res = np.zeros_like(x)
+    w = tie_weight(H, 64, seed=H)
+    g = parity.gpu_norm(x, res, w, eps, mode, G)
+    o = parity.oracle_norm(x, res, w, eps, mode, G)
+    assert np.array_equal(g["residual_out"], o["residual_out"])
+    assert np.array_equal(g["scale"].view(np.uint32), o["scale"].view(np.uint32))
+    if eps == 0.0:
+        assert np.all(g["scale"] == np.float32(2.0 ** -8))
+    # the ties at 84 and 168: to even (80, 160) without a direction, up to
+    # 88 and 176 with eps = 1e-5, whose stored scale is rounded down
+    mags = o["q"] & 0x7F
+    assert all(np.any(mags == c) for c in ((0x6A, 0x72) if eps == 0.0 else (0x6B, 0x73)))
+    bad = np.flatnonzero(g["q"].ravel() != o["q"].ravel())
+    assert bad.size == 0, (bad[:8], g["q"].ravel()[bad[:8]], o["q"].ravel()[bad[:8]])
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-5], ids=["no-direction", "direction"])
+@pytest.mark.parametrize("T", [64, 2048, 7400], ids=["group-kernel", "warp-registers", "warp-staged"])
+def test_mla_fp8_exact_ties(T, eps):
+    q_dim, kv_dim = gen.MLA_Q_DIM, gen.MLA_KV_DIM
+    d = {"q_c": tie_rows(T, q_dim, seed=T), "kv_c": gen.mla_inputs(T, 8, kv_dim, seed=T)["kv_c"],
+         "q_weight": tie_weight(q_dim, q_dim, seed=1), "kv_weight": tie_weight(kv_dim, kv_dim, seed=2)}
+    g = parity.gpu_mla(d["q_c"], d["q_weight"], d["kv_c"], d["kv_weight"], eps, 1e-6, True)
+    o = parity.oracle_mla(d["q_c"], d["q_weight"], d["kv_c"], d["kv_weight"], eps, 1e-6, True)
+    assert np.array_equal(g["q_scale"].view(np.uint32), o["q_scale"].view(np.uint32))
+    bad = np.flatnonzero(g["q_fp8"].ravel() != o["q_fp8"].ravel())
+    assert bad.size == 0, (bad[:8], g["q_fp8"].ravel()[bad[:8]], o["q_fp8"].ravel()[bad[:8]])
+    parity.check_mla(g, o, True)
