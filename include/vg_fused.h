@@ -299,6 +299,10 @@ vg_status vg_fused_qk_norm_rope(uint16_t *qkv, const uint16_t *q_weight, const u
  */
 #define VG_DEVICE_WAIT_TIMEOUT 1u
 #define VG_DEVICE_BAD_POSITION 2u /* vg_fused_qk_norm_rope: a position out of range */
+/* Debug builds only (compiled with VG_DEBUG_CHECKS, a test copy of the
+ * library): a kernel computed a store or copy address outside the tensor it
+ * belongs to; the access was skipped. */
+#define VG_DEVICE_OUT_OF_BOUNDS 4u
 vg_status vg_device_status(uint32_t *flags, int32_t reset);
 
 /* Static English text for a status code (never NULL). */

@@ -54,6 +54,7 @@ EXPORTED_SYMBOLS = ("vg_fused_add_rms_norm_fp8", "vg_silu_mul_fp8", "vg_fused_ad
                     "vg_status_string", "vg_abi_version")
 DEVICE_WAIT_TIMEOUT = 1
 DEVICE_BAD_POSITION = 2
+DEVICE_OUT_OF_BOUNDS = 4  # debug builds (VG_DEBUG_CHECKS) only
 
 _lock = threading.Lock()
 _lib = None

@@ -92,5 +92,21 @@ def build_wait_test(force: bool = False) -> str:
     return build(force, extra_flags=WAIT_TEST_FLAGS, out=WAIT_TEST_LIB)
 
 
+# Test-only copies with device bounds checks: every store and bulk-copy
+# source is checked against its tensor's extent; an access outside it is
+# skipped and reported as VG_DEVICE_OUT_OF_BOUNDS.  The "shrunk" copy
+# reports every tensor one row short, so that the checks must fire.
+DEBUG_LIB = os.path.join(BUILD, "libvg_fused_debug_checks.so")
+DEBUG_FLAGS = ("-DVG_DEBUG_CHECKS",)
+DEBUG_SHRUNK_LIB = os.path.join(BUILD, "libvg_fused_debug_checks_shrunk.so")
+DEBUG_SHRUNK_FLAGS = ("-DVG_DEBUG_CHECKS", "-DVG_DEBUG_SHRINK_EXTENT")
+
+
+def build_debug(force: bool = False, shrunk: bool = False) -> str:
+    if shrunk:
+        return build(force, extra_flags=DEBUG_SHRUNK_FLAGS, out=DEBUG_SHRUNK_LIB)
+    return build(force, extra_flags=DEBUG_FLAGS, out=DEBUG_LIB)
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

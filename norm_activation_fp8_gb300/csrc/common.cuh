@@ -101,6 +101,36 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
   }
 }
 
+// -------------------------------------------------------- debug checks
+//
+// Debug builds (-DVG_DEBUG_CHECKS, a test-only copy of the library): every
+// global store, and the source of every bulk copy, is first checked against
+// the extent of the tensor it touches.  An access outside it is skipped and
+// sets kErrBounds in the translation unit's status word, so an indexing
+// mistake shows up as a status flag, not as a fault or as overwritten
+// memory.  Product builds compile each check to `true`.
+// VG_DEBUG_SHRINK_EXTENT (tests only) reports every tensor one row short,
+// so that the checks of a row's last accesses fire.
+constexpr uint32_t kErrBounds = 4u;
+#ifdef VG_DEBUG_SHRINK_EXTENT
+#define VG_ROWS(T) ((uint64_t)(T) - 1u)
+#else
+#define VG_ROWS(T) ((uint64_t)(T))
+#endif
+#ifdef VG_DEBUG_CHECKS
+__device__ __forceinline__ bool access_ok(uint32_t *status, const void *p, uint32_t n,
+                                          const void *base, uint64_t bytes) {
+  const uint64_t a = reinterpret_cast<uint64_t>(p), b = reinterpret_cast<uint64_t>(base);
+  if (base != nullptr && a >= b && a + n <= b + bytes) return true;
+  atomicOr(status, kErrBounds);
+  return false;
+}
+#define VG_ACCESS_OK(status, p, n, base, bytes) \
+  ::vg::access_ok(&(status), (const void *)(p), (uint32_t)(n), (const void *)(base), (uint64_t)(bytes))
+#else
+#define VG_ACCESS_OK(status, p, n, base, bytes) true
+#endif
+
 // -------------------------------------------------------------- memory ops
 
 // Read-only data streamed once: non-coherent path, no L1 allocation.

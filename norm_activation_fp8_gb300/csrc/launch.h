@@ -23,6 +23,7 @@ struct RowPlan {
   int rpc;
   int64_t grid;
   int segs = 1;  // column segments per row (row-state-free SiLU modes only)
+  bool dense = false;  // SiLU per-group: the four-CTAs-per-SM instance
   int block() const { return ntr * rpc; }
 };
 
@@ -155,6 +156,7 @@ struct MlaPlan {
 };
 MlaPlan plan_mla(int64_t T, int nq, int nkv, bool q_fp8, int sms);
 cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaStream_t s);
+uint32_t read_mla_status(bool reset);
 
 // QK norm + RoPE, in place on qkv [T, row] with row = (hq + 2 hkv) * D.
 struct QkArgs {

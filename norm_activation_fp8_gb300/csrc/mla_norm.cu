@@ -36,7 +36,18 @@
 
 namespace vg {
 
+// Status word of this translation unit's kernels (kErrBounds, debug builds).
+__device__ uint32_t g_mla_status;
+
 namespace {
+
+// Extents in bytes of the outputs (debug checks).
+__device__ __forceinline__ uint64_t out_extent(const MlaArgs &a, int side) {
+  return VG_ROWS(a.T) * 16ull * (uint64_t)a.nch[side];
+}
+__device__ __forceinline__ uint64_t q8_extent(const MlaArgs &a) {
+  return VG_ROWS(a.T) * 8ull * (uint64_t)a.nch[0];
+}
 
 // The body of the warp-group kernel (wrappers below).
 template <int VPT, bool QFP8>
@@ -108,7 +119,8 @@ __device__ __forceinline__ void mla_dual_norm_rows(const MlaArgs &a) {
     if (fp8_row) {
       const DynScale d = make_dyn_scale(amr, y, dy);
       dq[slot] = d;
-      if (live) a.q_scale[row] = d.s;
+      if (live && VG_ACCESS_OK(g_mla_status, a.q_scale + row, 4, a.q_scale, 4 * VG_ROWS(a.T)))
+        a.q_scale[row] = d.s;
     } else {
       inv[slot][side] = make_float2(y, dy);
     }
@@ -124,7 +136,8 @@ __device__ __forceinline__ void mla_dual_norm_rows(const MlaArgs &a) {
         const int c = lr + k * ntr;
         float v[8];
         dyn_values8_fast(t[k], d.rf, v);
-        if (live && c < nch) st_stream(out + c * kElemsPerChunk, quant8(v));
+        if (live && c < nch && VG_ACCESS_OK(g_mla_status, out + c * kElemsPerChunk, 8, a.q8, q8_extent(a)))
+          st_stream(out + c * kElemsPerChunk, quant8(v));
       }
     } else {
 #pragma unroll
@@ -132,7 +145,8 @@ __device__ __forceinline__ void mla_dual_norm_rows(const MlaArgs &a) {
         const int c = lr + k * ntr;
         float v[8];
         dyn_values8_exact(t[k], d, v);
-        if (live && c < nch) st_stream(out + c * kElemsPerChunk, quant8(v));
+        if (live && c < nch && VG_ACCESS_OK(g_mla_status, out + c * kElemsPerChunk, 8, a.q8, q8_extent(a)))
+          st_stream(out + c * kElemsPerChunk, quant8(v));
       }
     }
   } else {
@@ -142,7 +156,9 @@ __device__ __forceinline__ void mla_dual_norm_rows(const MlaArgs &a) {
     for (int k = 0; k < VPT; ++k) {
       const int c = lr + k * ntr;
       const uint4 o = bf16x8_product_rn(t[k], yd.x, yd.y);
-      if (live && c < nch) st_stream(out + c * kElemsPerChunk, o);
+      if (live && c < nch &&
+          VG_ACCESS_OK(g_mla_status, out + c * kElemsPerChunk, 16, a.out[side], out_extent(a, side)))
+        st_stream(out + c * kElemsPerChunk, o);
     }
   }
 }
@@ -177,29 +193,32 @@ __device__ __forceinline__ void chunk_t(const uint4 &xv, const float2 (&wf)[4], 
   for (int i = 0; i < 4; ++i) t[i] = f2_mul(bf16x2_to_f2(xw[i]), wf[i]);
 }
 
+constexpr int kMlaWarpChunks = 8;  // chunks per lane over both rows of a token
+constexpr int kMlaWeightChunks = kMlaWarpChunks * 32;  // both weights, at most
+
 // Both weights of the warp kernel sit in shared memory as fp32, converted
-// once per CTA (two float4 a chunk), so that neither pass unpacks them
-// again: the kernel is bound by the integer pipe, which does the unpacking.
+// once per CTA, so that neither pass unpacks them again: the kernel is bound
+// by the integer pipe, which does the unpacking.  Two planes (elements 0-3
+// of every chunk, then elements 4-7), so that the lanes of a warp, which read
+// consecutive chunks, read consecutive 16-byte words without bank conflicts.
 __device__ __forceinline__ void stage_weights_f32(float4 *ws, const MlaArgs &a) {
   for (int i = threadIdx.x; i < a.nch[0] + a.nch[1]; i += blockDim.x) {
     const uint4 wb = i < a.nch[0] ? ld_keep(a.w[0] + i * kElemsPerChunk)
                                   : ld_keep(a.w[1] + (i - a.nch[0]) * kElemsPerChunk);
-    ws[2 * i] = make_float4(bf16_lo(wb.x), bf16_hi(wb.x), bf16_lo(wb.y), bf16_hi(wb.y));
-    ws[2 * i + 1] = make_float4(bf16_lo(wb.z), bf16_hi(wb.z), bf16_lo(wb.w), bf16_hi(wb.w));
+    ws[i] = make_float4(bf16_lo(wb.x), bf16_hi(wb.x), bf16_lo(wb.y), bf16_hi(wb.y));
+    ws[kMlaWeightChunks + i] = make_float4(bf16_lo(wb.z), bf16_hi(wb.z), bf16_lo(wb.w), bf16_hi(wb.w));
   }
 }
 
 // Chunk i of the staged weights (zeros past the row).
 __device__ __forceinline__ void weights_f32(const float4 *ws, int i, bool in_row, float2 (&wf)[4]) {
-  const float4 w0 = in_row ? ws[2 * i] : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4 w1 = in_row ? ws[2 * i + 1] : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 w0 = in_row ? ws[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float4 w1 = in_row ? ws[kMlaWeightChunks + i] : make_float4(0.f, 0.f, 0.f, 0.f);
   wf[0] = make_float2(w0.x, w0.y);
   wf[1] = make_float2(w0.z, w0.w);
   wf[2] = make_float2(w1.x, w1.y);
   wf[3] = make_float2(w1.z, w1.w);
 }
-
-constexpr int kMlaWarpChunks = 8;  // chunks per lane over both rows of a token
 
 // 16-byte asynchronous copy global -> shared (no register staging); a
 // source size of 0 fills the 16 bytes with zeros.
@@ -220,10 +239,10 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // both passes read them there, instead of 32 registers a lane holding them
 // from the loads to the stores, so that more warps fit on an SM.
 template <bool QFP8, int KQ, bool STAGE = false>
-__global__ void __launch_bounds__(256, STAGE ? (QFP8 ? 4 : 5) : (QFP8 && KQ > 0 ? 3 : 4))
+__global__ void __launch_bounds__(256, STAGE ? 5 : (QFP8 && KQ > 0 ? 3 : 4))
     mla_dual_norm_warp_kernel(const MlaArgs a, const int kq_rt) {
   const int kq = KQ > 0 ? KQ : kq_rt;
-  __shared__ float4 ws[kMlaWarpChunks * 32 * 2];  // both weights as fp32: q chunks, then kv
+  __shared__ float4 ws[kMlaWeightChunks * 2];  // both weights as fp32: q chunks, then kv; two planes
   __shared__ uint4 xs[STAGE ? 8 : 1][kMlaWarpChunks][32];  // STAGE: per warp, per chunk, per lane
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -309,7 +328,8 @@ __global__ void __launch_bounds__(256, STAGE ? (QFP8 ? 4 : 5) : (QFP8 && KQ > 0 
   DynScale d;
   if (QFP8) {
     d = make_dyn_scale(warp_max(am), yq, dyq);
-    if (lane == 0) a.q_scale[row] = d.s;
+    if (lane == 0 && VG_ACCESS_OK(g_mla_status, a.q_scale + row, 4, a.q_scale, 4 * VG_ROWS(a.T)))
+      a.q_scale[row] = d.s;
   }
   // Pass 2, with the q row's FP8 codes in the two-multiply form when the
   // token's scale has a tie direction (all but degenerate rows; the choice
@@ -331,10 +351,11 @@ __global__ void __launch_bounds__(256, STAGE ? (QFP8 ? 4 : 5) : (QFP8 && KQ > 0 
           dyn_values8_fast(t, d.rf, v);
         else
           dyn_values8_exact(t, d, v);
-        st_stream(a.q8 + off, quant8(v));
+        if (VG_ACCESS_OK(g_mla_status, a.q8 + off, 8, a.q8, q8_extent(a))) st_stream(a.q8 + off, quant8(v));
       } else {
-        st_stream((q ? a.out[0] : a.out[1]) + off,
-                  bf16x8_product_rn(t, q ? yq : ykv, q ? dyq : dykv));
+        uint16_t *op = (q ? a.out[0] : a.out[1]) + off;
+        if (VG_ACCESS_OK(g_mla_status, op, 16, q ? a.out[0] : a.out[1], out_extent(a, q ? 0 : 1)))
+          st_stream(op, bf16x8_product_rn(t, q ? yq : ykv, q ? dyq : dykv));
       }
     }
   };
@@ -356,6 +377,16 @@ cudaError_t launch_vpt(const MlaArgs &a, bool q_fp8, const MlaPlan &p, cudaStrea
 }
 
 }  // namespace
+
+uint32_t read_mla_status(bool reset) {
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_mla_status, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  if (reset) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_mla_status, &zero, sizeof(zero)) != cudaSuccess) return 0xFFFFFFFFu;
+  }
+  return v;
+}
 
 cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaStream_t s) {
   a.thr[0] = p.thr[0];

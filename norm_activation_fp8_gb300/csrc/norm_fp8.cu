@@ -49,8 +49,22 @@
 
 namespace vg {
 
-// Status word of this translation unit's kernels (kErrWaitTimeout).
+// Status word of this translation unit's kernels (kErrWaitTimeout, and
+// kErrBounds in debug builds).
 __device__ uint32_t g_norm_status;
+
+// Extents in bytes of the tensors a launch touches (debug checks).
+__device__ __forceinline__ uint64_t q_extent(const NormArgs &a, int mode) {
+  return VG_ROWS(a.T) * (uint64_t)(mode == kNvfp4 ? a.H / 2 : a.H);
+}
+__device__ __forceinline__ uint64_t row_extent(const NormArgs &a) {  // x, residual, residual_out
+  return VG_ROWS(a.T) * 2ull * (uint64_t)a.H;
+}
+__device__ __forceinline__ uint64_t scale_extent(const NormArgs &a, int mode) {
+  const uint64_t rows = VG_ROWS(a.T);
+  if (mode == kPerToken) return 4 * rows;
+  return rows == 0 ? 0 : 4 * ((rows - 1) * (uint64_t)a.s_ts + (uint64_t)(a.ngroups - 1) * a.s_gs + 1);
+}
 
 namespace {
 
@@ -94,7 +108,9 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
         v[2 * i] = q.x;
         v[2 * i + 1] = q.y;
       }
-      if (live && c < a.nch) st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
+      if (live && c < a.nch &&
+          VG_ACCESS_OK(g_norm_status, a.q + base + c * kElemsPerChunk, 8, a.q, q_extent(a, MODE)))
+        st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
     }
     return;
   }
@@ -153,7 +169,9 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
           return e4m3_code_df(qs, ql - (qs - qh));
         });
         const float sv = e4m3_value(code);
-        if (live) a.sf8[row * nslots + g] = (uint8_t)code;
+        if (live && VG_ACCESS_OK(g_norm_status, a.sf8 + row * nslots + g, 1, a.sf8,
+                                 VG_ROWS(a.T) * (uint64_t)nslots))
+          a.sf8[row * nslots + g] = (uint8_t)code;
         reinterpret_cast<float2 *>(sm.dyn)[slot * nslots + g] =
             make_float2(sv, sv > 0.f ? ygs * __frcp_rn(sv) : 0.f);
       }
@@ -166,12 +184,9 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
       const DynScale d = MODE == kPerGroupX && a.ue8m0 ? make_pow2_scale(amr, y, dy)
                                                        : make_dyn_scale(amr, y, dy);
       sm.dyn[slot * nslots + lr] = d;
-      if (live) {
-        if (MODE == kPerGroupX)
-          a.scale[row * a.s_ts + (int64_t)lr * a.s_gs] = d.s;
-        else
-          a.scale[row * nslots + lr] = d.s;
-      }
+      float *sp = MODE == kPerGroupX ? a.scale + row * a.s_ts + (int64_t)lr * a.s_gs
+                                     : a.scale + row * nslots + lr;
+      if (live && VG_ACCESS_OK(g_norm_status, sp, 4, a.scale, scale_extent(a, MODE))) *sp = d.s;
     }
   }
   __syncthreads();
@@ -190,7 +205,8 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
         v[2 * i + 1] = q.y;
       }
       const uint32_t codes = quant_e2m1x8(v) & (d.x > 0.f ? 0xFFFFFFFFu : 0u);  // +0 codes
-      if (live && c < a.nch) st_stream(out + c * 4, codes);
+      if (live && c < a.nch && VG_ACCESS_OK(g_norm_status, out + c * 4, 4, a.q, q_extent(a, MODE)))
+        st_stream(out + c * 4, codes);
     }
     return;
   }
@@ -201,11 +217,16 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
     for (int k = 0; k < VPT; ++k) {
       const int c = lr + k * a.ntr;
       const uint4 o = bf16x8_product_rn(t[k], d.s, d.a);
-      if (live && c < a.nch) st_stream(out + c * kElemsPerChunk, o);
+      if (live && c < a.nch &&
+          VG_ACCESS_OK(g_norm_status, out + c * kElemsPerChunk, 16, a.out16,
+                       VG_ROWS(a.T) * 16ull * (uint64_t)a.nch_pad))
+        st_stream(out + c * kElemsPerChunk, o);
     }
     // the padded tail is zero
     for (int c = a.nch + lr; live && c < a.nch_pad; c += a.ntr)
-      st_stream(out + c * kElemsPerChunk, make_uint4(0, 0, 0, 0));
+      if (VG_ACCESS_OK(g_norm_status, out + c * kElemsPerChunk, 16, a.out16,
+                       VG_ROWS(a.T) * 16ull * (uint64_t)a.nch_pad))
+        st_stream(out + c * kElemsPerChunk, make_uint4(0, 0, 0, 0));
     return;
   }
   // padding chunks (c >= nch) read slot 0 and store nothing
@@ -216,7 +237,8 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int c = lr + k * a.ntr;
-      const float2 m2 = make_float2(scale_of(c).ra, scale_of(c).ra);
+      const DynScale d = scale_of(c);
+      const float2 m2 = make_float2(d.ra, d.ra);
       float v[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -224,7 +246,9 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
         v[2 * i] = q.x;
         v[2 * i + 1] = q.y;
       }
-      if (live && c < a.nch) st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
+      if (live && c < a.nch &&
+          VG_ACCESS_OK(g_norm_status, a.q + base + c * kElemsPerChunk, 8, a.q, q_extent(a, MODE)))
+        st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
     }
     return;
   }
@@ -249,15 +273,20 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
       const int c = lr + k * a.ntr;
       float v[8];
       dyn_values8_fast(t[k], rf[k], v);
-      if (live && c < a.nch) st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
+      if (live && c < a.nch &&
+          VG_ACCESS_OK(g_norm_status, a.q + base + c * kElemsPerChunk, 8, a.q, q_extent(a, MODE)))
+        st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
     }
   } else {
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       const int c = lr + k * a.ntr;
+      const DynScale d = scale_of(c);
       float v[8];
-      dyn_values8_exact(t[k], scale_of(c), v);
-      if (live && c < a.nch) st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
+      dyn_values8_exact(t[k], d, v);
+      if (live && c < a.nch &&
+          VG_ACCESS_OK(g_norm_status, a.q + base + c * kElemsPerChunk, 8, a.q, q_extent(a, MODE)))
+        st_stream(a.q + base + c * kElemsPerChunk, quant8(v));
     }
   }
 }
@@ -331,7 +360,9 @@ __global__ void __launch_bounds__(512) norm_fp8_kernel(const NormArgs a) {
   for (int k = 0; k < VPT; ++k) {
     const uint4 ow = pass1_chunk<DYN, RES, true>(xv[k], rv[k], wv[k], t[k], cmax[k], acc);
     const int c = lr + k * a.ntr;
-    if (RES && live && c < a.nch) st_stream(a.res_out + base + c * kElemsPerChunk, ow);
+    if (RES && live && c < a.nch &&
+        VG_ACCESS_OK(g_norm_status, a.res_out + base + c * kElemsPerChunk, 16, a.res_out, row_extent(a)))
+      st_stream(a.res_out + base + c * kElemsPerChunk, ow);
   }
   finish_rows<VPT, MODE, GCH>(a, t, cmax, acc, sm, 0, slot, lr, row, live, base);
 }
@@ -369,6 +400,13 @@ __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, con
 
   auto issue = [&](int s, int64_t row) {
     unsigned char *st = dsm + (size_t)s * L.stage_bytes;
+    // (debug builds: a copy whose source is out of range is replaced by a
+    // plain arrival, so that the stage's wait still completes)
+    if (!VG_ACCESS_OK(g_norm_status, a.x + row * a.H, row_bytes, a.x, row_extent(a)) ||
+        (RES && !VG_ACCESS_OK(g_norm_status, a.res + row * a.H, row_bytes, a.res, row_extent(a)))) {
+      mbar_arrive(&full[s]);
+      return;
+    }
     mbar_arrive_expect_tx(&full[s], RES ? 2 * row_bytes : row_bytes);
     tma_load_bulk(st, a.x + row * a.H, row_bytes, &full[s]);
     if (RES) tma_load_bulk(st + row_bytes, a.res + row * a.H, row_bytes, &full[s]);
@@ -425,7 +463,9 @@ __global__ void __launch_bounds__(512) norm_fp8_tma_kernel(const NormArgs a, con
         wv = lds128(wbuf + c * 16);
       }
       const uint4 ow = pass1_chunk<DYN, RES>(xv, rv, wv, t[k], cmax[k], acc);
-      if (RES && ok && c < a.nch) st_stream(a.res_out + base + c * kElemsPerChunk, ow);
+      if (RES && ok && c < a.nch &&
+          VG_ACCESS_OK(g_norm_status, a.res_out + base + c * kElemsPerChunk, 16, a.res_out, row_extent(a)))
+        st_stream(a.res_out + base + c * kElemsPerChunk, ow);
     }
     // Every thread has read stage s once this barrier is passed, so its
     // refill goes out now; a timed-out wait anywhere in the CTA ends the

@@ -39,10 +39,21 @@
 
 namespace vg {
 
-// Status word of this translation unit's kernels (kErrWaitTimeout).
+// Status word of this translation unit's kernels (kErrWaitTimeout, and
+// kErrBounds in debug builds).
 __device__ uint32_t g_silu_status;
 
 namespace {
+
+// Extents in bytes of the tensors a launch touches (debug checks).
+__device__ __forceinline__ uint64_t q_extent(const SiluArgs &a, bool fp4) {
+  return VG_ROWS(a.T) * (uint64_t)(fp4 ? a.I / 2 : a.I);
+}
+__device__ __forceinline__ uint64_t scale_extent(const SiluArgs &a, int mode) {
+  const uint64_t rows = VG_ROWS(a.T);
+  if (mode == kPerToken) return 4 * rows;
+  return rows == 0 ? 0 : 4 * ((rows - 1) * (uint64_t)a.s_ts + (uint64_t)(a.ngroups - 1) * a.s_gs + 1);
+}
 
 __device__ __forceinline__ float fast_rcp(float x) {
   float r;
@@ -148,7 +159,8 @@ __device__ __forceinline__ double candidates_amax_f64(uint4 gv, uint4 uv, const 
 template <int GCH>
 __device__ __noinline__ void pow2_group_settle(const uint16_t *gate_up, uint8_t *q, float *scale,
                                                int32_t I, int32_t s_ts, int32_t s_gs, int64_t row,
-                                               int c, bool near) {
+                                               int c, bool near, uint64_t q_bytes,
+                                               uint64_t s_bytes) {
   uint4 gv = make_uint4(0, 0, 0, 0), uv = gv;
   if (near) {
     gv = ld_stream_ro(gate_up + row * 2 * I + c * kElemsPerChunk);
@@ -161,9 +173,11 @@ __device__ __noinline__ void pow2_group_settle(const uint16_t *gate_up, uint8_t 
   for (int o = GCH >> 1; o > 0; o >>= 1) m = fmax(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if (!near) return;
   const int e = pow2_exponent(m);
-  if ((c & (GCH - 1)) == 0) scale[row * s_ts + (int64_t)(c / GCH) * s_gs] = exp2i(e);
+  float *sp = scale + row * s_ts + (int64_t)(c / GCH) * s_gs;
+  if ((c & (GCH - 1)) == 0 && VG_ACCESS_OK(g_silu_status, sp, 4, scale, s_bytes)) *sp = exp2i(e);
   scale8(v, exp2i(-e));
-  st_stream(q + row * (int64_t)I + c * kElemsPerChunk, quant8(v));
+  uint8_t *qp = q + row * (int64_t)I + c * kElemsPerChunk;
+  if (VG_ACCESS_OK(g_silu_status, qp, 8, q, q_bytes)) st_stream(qp, quant8(v));
 }
 
 // Rewrites one NVFP4 block whose fp32 value gs * amax / 6 lay near an E4M3
@@ -174,7 +188,8 @@ __device__ __noinline__ void pow2_group_settle(const uint16_t *gate_up, uint8_t 
 // is below am (1 - 2^-15) (am the fp32 block amax; both carry under 2^-19 of
 // error) cannot be it.
 __device__ __noinline__ void nvfp4_silu_settle(const uint16_t *gate_up, uint8_t *q4, uint8_t *sf,
-                                               int32_t I, int64_t row, int c, float gs, bool near) {
+                                               int32_t I, int64_t row, int c, float gs, bool near,
+                                               uint64_t q_bytes, uint64_t sf_bytes) {
   uint4 gv = make_uint4(0, 0, 0, 0), uv = gv;
   if (near) {
     gv = ld_stream_ro(gate_up + row * 2 * I + c * kElemsPerChunk);
@@ -191,8 +206,11 @@ __device__ __noinline__ void nvfp4_silu_settle(const uint16_t *gate_up, uint8_t 
   const uint32_t code = e4m3_code_df(xh, (float)(x - (double)xh));
   const float sv = e4m3_value(code);
   scale8(v, sv > 0.f ? gs * fast_rcp(sv) : 0.f);
-  if ((c & 1) == 0) sf[row * (int64_t)(I / kNvfp4Block) + c / 2] = (uint8_t)code;
-  st_stream(q4 + row * (int64_t)(I / 2) + c * 4, quant_e2m1x8(v) & (sv > 0.f ? 0xFFFFFFFFu : 0u));
+  uint8_t *fp = sf + row * (int64_t)(I / kNvfp4Block) + c / 2;
+  if ((c & 1) == 0 && VG_ACCESS_OK(g_silu_status, fp, 1, sf, sf_bytes)) *fp = (uint8_t)code;
+  uint8_t *qp = q4 + row * (int64_t)(I / 2) + c * 4;
+  if (VG_ACCESS_OK(g_silu_status, qp, 4, q4, q_bytes))
+    st_stream(qp, quant_e2m1x8(v) & (sv > 0.f ? 0xFFFFFFFFu : 0u));
 }
 
 // A row is covered by ntr * VPT chunks per CTA.  Static and per-group modes
@@ -206,8 +224,13 @@ __device__ __noinline__ void nvfp4_silu_settle(const uint16_t *gate_up, uint8_t 
 // CTA.
 // OPT: per-group with scale options (UE8M0 and/or column-major), an
 // instance of its own so that plain per-group code stays as it is.
-template <int VPT, int MODE, int GCH, bool BIG, bool OPT = false>
-__global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken ? 2 : 3))
+// DENSE: plain per-group rows of at most two chunks a thread in 32
+// registers, four CTAs per SM: more row segments in flight per SM (measured
+// on GB300 from two rows per SM: 2048 x 14336 0.94 -> 1.00, 32768 x 28672
+// 0.93 -> 0.99; below that, with a single partial wave, three CTAs' longer
+// register budget is faster).
+template <int VPT, int MODE, int GCH, bool BIG, bool OPT = false, bool DENSE = false>
+__global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken ? 2 : (DENSE ? 4 : 3)))
     silu_fp8_kernel(const SiluArgs a) {
   __shared__ float red[32];
   const int tid = threadIdx.x;
@@ -267,14 +290,17 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
       scale8(v, sv > 0.f ? gs * fast_rcp(sv) : 0.f);
       const uint32_t codes = quant_e2m1x8(v) & (sv > 0.f ? 0xFFFFFFFFu : 0u);  // +0 codes
       if (live && c < a.nch) {
-        if ((c & 1) == 0) a.sf8[row * (int64_t)(a.I / kNvfp4Block) + c / 2] = (uint8_t)code;
-        st_stream(out + c * 4, codes);
+        uint8_t *fp = a.sf8 + row * (int64_t)(a.I / kNvfp4Block) + c / 2;
+        if ((c & 1) == 0 && VG_ACCESS_OK(g_silu_status, fp, 1, a.sf8, VG_ROWS(a.T) * (uint64_t)(a.I / kNvfp4Block)))
+          *fp = (uint8_t)code;
+        if (VG_ACCESS_OK(g_silu_status, out + c * 4, 4, a.q, q_extent(a, true))) st_stream(out + c * 4, codes);
       }
     }
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
       if (__any_sync(0xFFFFFFFFu, (near_k >> k) & 1u))
-        nvfp4_silu_settle(a.gate_up, a.q, a.sf8, a.I, row, lr + k * a.ntr, gs, (near_k >> k) & 1u);
+        nvfp4_silu_settle(a.gate_up, a.q, a.sf8, a.I, row, lr + k * a.ntr, gs, (near_k >> k) & 1u,
+                          q_extent(a, true), VG_ROWS(a.T) * (uint64_t)(a.I / kNvfp4Block));
     return;
   }
   if constexpr (OPT) {
@@ -300,16 +326,20 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
         s = silu_scale(am);
         m = fast_rcp(s);
       }
-      if (live && c < a.nch && (c & (GCH - 1)) == 0)
-        a.scale[row * a.s_ts + (int64_t)(c / GCH) * a.s_gs] = s;
+      float *sp = a.scale + row * a.s_ts + (int64_t)(c / GCH) * a.s_gs;
+      if (live && c < a.nch && (c & (GCH - 1)) == 0 &&
+          VG_ACCESS_OK(g_silu_status, sp, 4, a.scale, scale_extent(a, MODE)))
+        *sp = s;
       scale8(v, m);
-      if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
+      if (live && c < a.nch &&
+          VG_ACCESS_OK(g_silu_status, a.q + out_base + c * kElemsPerChunk, 8, a.q, q_extent(a, false)))
+        st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
     }
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
       if (__any_sync(0xFFFFFFFFu, (near_k >> k) & 1u))
         pow2_group_settle<GCH>(a.gate_up, a.q, a.scale, a.I, a.s_ts, a.s_gs, row, lr + k * a.ntr,
-                               (near_k >> k) & 1u);
+                               (near_k >> k) & 1u, q_extent(a, false), scale_extent(a, MODE));
     return;
   }
   if (MODE != kPerToken) {
@@ -322,11 +352,15 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
       float m = inv_static;
       if (MODE == kPerGroup) {
         const float s = silu_scale(lanes_max(amax8(v), GCH));
-        if (live && c < a.nch && (c & (GCH - 1)) == 0) a.scale[row * a.ngroups + c / GCH] = s;
+        if (live && c < a.nch && (c & (GCH - 1)) == 0 &&
+            VG_ACCESS_OK(g_silu_status, a.scale + row * a.ngroups + c / GCH, 4, a.scale, scale_extent(a, MODE)))
+          a.scale[row * a.ngroups + c / GCH] = s;
         m = fast_rcp(s);
       }
       scale8(v, m);
-      if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
+      if (live && c < a.nch &&
+          VG_ACCESS_OK(g_silu_status, a.q + out_base + c * kElemsPerChunk, 8, a.q, q_extent(a, false)))
+        st_stream(a.q + out_base + c * kElemsPerChunk, quant8(v));
     }
     return;
   }
@@ -348,13 +382,16 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken
     for (int i = 0; i < nw; ++i) am = fmaxf(am, red[slot * nw + i]);
   }
   const float s = silu_scale(am);
-  if (live && lr == 0) a.scale[row] = s;
+  if (live && lr == 0 && VG_ACCESS_OK(g_silu_status, a.scale + row, 4, a.scale, scale_extent(a, MODE)))
+    a.scale[row] = s;
   const float m = fast_rcp(s);
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int c = lr + k * a.ntr;
     scale8(act[k], m);
-    if (live && c < a.nch) st_stream(a.q + out_base + c * kElemsPerChunk, quant8(act[k]));
+    if (live && c < a.nch &&
+        VG_ACCESS_OK(g_silu_status, a.q + out_base + c * kElemsPerChunk, 8, a.q, q_extent(a, false)))
+      st_stream(a.q + out_base + c * kElemsPerChunk, quant8(act[k]));
   }
 }
 
@@ -385,6 +422,14 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
   auto issue = [&](int sg, int64_t row) {
     unsigned char *st = dsm + (size_t)sg * 2 * seg_bytes;
     const uint16_t *src = a.gate_up + row * 2 * a.I + (int64_t)sg * seg_ch * kElemsPerChunk;
+    // (debug builds: a copy whose source is out of range is replaced by a
+    // plain arrival, so that the stage's wait still completes)
+    const uint64_t in_bytes = VG_ROWS(a.T) * 4ull * (uint64_t)a.I;
+    if (!VG_ACCESS_OK(g_silu_status, src, seg_bytes, a.gate_up, in_bytes) ||
+        !VG_ACCESS_OK(g_silu_status, src + a.I, seg_bytes, a.gate_up, in_bytes)) {
+      mbar_arrive(&full[sg]);
+      return;
+    }
     mbar_arrive_expect_tx(&full[sg], 2 * seg_bytes);
     tma_load_bulk(st, src, seg_bytes, &full[sg]);
     tma_load_bulk(st + seg_bytes, src + a.I, seg_bytes, &full[sg]);
@@ -446,7 +491,8 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
     am = 0.f;
     for (int w = 0; w < (a.ntr >> 5); ++w) am = fmaxf(am, r[w]);
     const float s = silu_scale(am);
-    if (tid == 0) a.scale[row] = s;
+    if (tid == 0 && VG_ACCESS_OK(g_silu_status, a.scale + row, 4, a.scale, scale_extent(a, kPerToken)))
+      a.scale[row] = s;
     const float m = fast_rcp(s);
     const int64_t out_base = row * a.I;
 #pragma unroll
@@ -455,7 +501,9 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
       for (int k = 0; k < KS; ++k) {
         const int c = tid + k * a.ntr;
         scale8(act[sg * KS + k], m);
-        if (c < seg_ch)
+        if (c < seg_ch &&
+            VG_ACCESS_OK(g_silu_status, a.q + out_base + ((int64_t)sg * seg_ch + c) * kElemsPerChunk, 8, a.q,
+                         q_extent(a, false)))
           st_stream(a.q + out_base + ((int64_t)sg * seg_ch + c) * kElemsPerChunk,
                     quant8(act[sg * KS + k]));
       }
@@ -505,6 +553,11 @@ cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStrea
         return a.gch == 8 ? launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 8, false, true>, g, b, 0, s, a)
                           : launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 16, false, true>, g, b, 0, s, a);
       }
+      if constexpr (VPT <= 2)
+        if (p.dense)
+          return a.gch == 8
+                     ? launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 8, false, false, true>, g, b, 0, s, a)
+                     : launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 16, false, false, true>, g, b, 0, s, a);
       return a.gch == 8 ? launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 8, false>, g, b, 0, s, a)
                         : launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 16, false>, g, b, 0, s, a);
   }

@@ -133,7 +133,6 @@ RowPlan plan_rows(int64_t T, int nch, int min_vpt, int sms) {
 // four chunks a thread, up to 1024 threads (fewer chunks when that still
 // fits 448 threads).
 RowPlan plan_silu(int64_t T, int nch, int mode, int sms) {
-  (void)sms;
   RowPlan p;
   p.rpc = 1;
   p.segs = 1;
@@ -149,6 +148,7 @@ RowPlan plan_silu(int64_t T, int nch, int mode, int sms) {
   } else {
     p.vpt = mode == VG_SCALE_STATIC ? 4 : 2;
     p.segs = (nch + 448 * p.vpt - 1) / (448 * p.vpt);
+    p.dense = mode == VG_SCALE_PER_GROUP && T >= 2LL * sms;
   }
   const int per = (nch + p.segs * p.vpt - 1) / (p.segs * p.vpt);
   p.ntr = (per + 31) / 32 * 32;
@@ -577,9 +577,10 @@ vg_status vg_silu_mul_nvfp4(uint8_t *q4, uint8_t *block_scale, const uint16_t *g
 vg_status vg_device_status(uint32_t *flags, int32_t reset) {
   if (!flags) return VG_ERR_NULL_PTR;
   const uint32_t v = vg::read_norm_status(reset != 0), w = vg::read_silu_status(reset != 0),
-                 r = vg::read_rope_status(reset != 0);
-  if (v == 0xFFFFFFFFu || w == 0xFFFFFFFFu || r == 0xFFFFFFFFu) return VG_ERR_CUDA;
-  *flags = v | w | r;
+                 r = vg::read_rope_status(reset != 0), m = vg::read_mla_status(reset != 0);
+  if (v == 0xFFFFFFFFu || w == 0xFFFFFFFFu || r == 0xFFFFFFFFu || m == 0xFFFFFFFFu)
+    return VG_ERR_CUDA;
+  *flags = v | w | r | m;
   return VG_OK;
 }
 
