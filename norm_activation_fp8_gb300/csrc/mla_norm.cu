@@ -42,10 +42,10 @@ __device__ uint32_t g_mla_status;
 namespace {
 
 // Extents in bytes of the outputs (debug checks).
-__device__ __forceinline__ uint64_t out_extent(const MlaArgs &a, int side) {
+[[maybe_unused]] __device__ __forceinline__ uint64_t out_extent(const MlaArgs &a, int side) {
   return VG_ROWS(a.T) * 16ull * (uint64_t)a.nch[side];
 }
-__device__ __forceinline__ uint64_t q8_extent(const MlaArgs &a) {
+[[maybe_unused]] __device__ __forceinline__ uint64_t q8_extent(const MlaArgs &a) {
   return VG_ROWS(a.T) * 8ull * (uint64_t)a.nch[0];
 }
 

@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(512) qk_norm_rope_kernel(const QkArgs a) {
                               pack_bf16x2_rn(p[4], p[5]), pack_bf16x2_rn(p[6], p[7]));
   const uint4 ob = make_uint4(pack_bf16x2_rn(p[8], p[9]), pack_bf16x2_rn(p[10], p[11]),
                               pack_bf16x2_rn(p[12], p[13]), pack_bf16x2_rn(p[14], p[15]));
-  const uint64_t bytes = VG_ROWS(a.T) * 2ull * (uint64_t)a.row;
+  [[maybe_unused]] const uint64_t bytes = VG_ROWS(a.T) * 2ull * (uint64_t)a.row;
   if (live && VG_ACCESS_OK(g_rope_status, head + l * kElemsPerChunk, 16, a.qkv, bytes))
     st_stream(head + l * kElemsPerChunk, oa);
   if (live && VG_ACCESS_OK(g_rope_status, head + (l + G) * kElemsPerChunk, 16, a.qkv, bytes))

@@ -224,10 +224,12 @@ __device__ __noinline__ void nvfp4_silu_settle(const uint16_t *gate_up, uint8_t 
 // CTA.
 // OPT: per-group with scale options (UE8M0 and/or column-major), an
 // instance of its own so that plain per-group code stays as it is.
-// DENSE: plain per-group rows of at most two chunks a thread in 32
-// registers, four CTAs per SM: more row segments in flight per SM (measured
-// on GB300 from two rows per SM: 2048 x 14336 0.94 -> 1.00, 32768 x 28672
-// 0.93 -> 0.99; below that, with a single partial wave, three CTAs' longer
+// DENSE: row-segment rows (per-group, scale options, NVFP4) of at most two
+// chunks a thread in 32 registers, four CTAs per SM: more row segments in
+// flight per SM (measured on GB300 from two rows per SM: per-group
+// 2048 x 14336 0.94 -> 1.00, 32768 x 28672 0.93 -> 0.99; NVFP4
+// 32768 x 28672 0.88 -> 0.93; UE8M0 column-major 32768 x 14336 0.92 ->
+// 0.96; below two rows per SM, a single partial wave, three CTAs' larger
 // register budget is faster).
 template <int VPT, int MODE, int GCH, bool BIG, bool OPT = false, bool DENSE = false>
 __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken ? 2 : (DENSE ? 4 : 3)))
@@ -424,7 +426,7 @@ __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : 2)
     const uint16_t *src = a.gate_up + row * 2 * a.I + (int64_t)sg * seg_ch * kElemsPerChunk;
     // (debug builds: a copy whose source is out of range is replaced by a
     // plain arrival, so that the stage's wait still completes)
-    const uint64_t in_bytes = VG_ROWS(a.T) * 4ull * (uint64_t)a.I;
+    [[maybe_unused]] const uint64_t in_bytes = VG_ROWS(a.T) * 4ull * (uint64_t)a.I;
     if (!VG_ACCESS_OK(g_silu_status, src, seg_bytes, a.gate_up, in_bytes) ||
         !VG_ACCESS_OK(g_silu_status, src + a.I, seg_bytes, a.gate_up, in_bytes)) {
       mbar_arrive(&full[sg]);
@@ -542,7 +544,8 @@ cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStrea
     case kStatic: return launch_pdl(silu_fp8_kernel<VPT, kStatic, 1, false>, g, b, 0, s, a);
     case kNvfp4:  // the per-group plan: at most two chunks a thread
       if constexpr (VPT <= 2)
-        return launch_pdl(silu_fp8_kernel<VPT, kNvfp4, 2, false>, g, b, 0, s, a);
+        return p.dense ? launch_pdl(silu_fp8_kernel<VPT, kNvfp4, 2, false, false, true>, g, b, 0, s, a)
+                       : launch_pdl(silu_fp8_kernel<VPT, kNvfp4, 2, false>, g, b, 0, s, a);
       else
         return cudaErrorInvalidConfiguration;
     case kPerToken:
@@ -550,6 +553,10 @@ cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStrea
                              : launch_pdl(silu_fp8_kernel<VPT, kPerToken, 1, false>, g, b, 0, s, a);
     default:
       if (a.ue8m0 || a.s_gs != 1) {
+        if constexpr (VPT <= 2)
+          if (p.dense)
+            return a.gch == 8 ? launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 8, false, true, true>, g, b, 0, s, a)
+                              : launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 16, false, true, true>, g, b, 0, s, a);
         return a.gch == 8 ? launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 8, false, true>, g, b, 0, s, a)
                           : launch_pdl(silu_fp8_kernel<VPT, kPerGroup, 16, false, true>, g, b, 0, s, a);
       }
