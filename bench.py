@@ -969,8 +969,9 @@ def run_sweep(args):
     peak, peak_kind = measured_peak()
     stream = torch.cuda.Stream(device=dev)
     cache = {}
-    for w in (list(gen.NAMED.values()) + gen.sweep() + gen.mla_workloads() + gen.pad_workloads()
-              + gen.qk_workloads() + gen.nvfp4_workloads() + gen.group_option_workloads()):
+    for w in (list(gen.NAMED.values()) + [CFG3_ACT] + gen.sweep() + gen.mla_workloads()
+              + gen.pad_workloads() + gen.qk_workloads() + gen.nvfp4_workloads()
+              + gen.group_option_workloads()):
         if args.sweep_filter and not any(f in w.name for f in args.sweep_filter.split(",")):
             continue
         key = (w.op, w.T, w.n, w.n2, w.x_dist)
