@@ -255,10 +255,12 @@ __device__ __forceinline__ void finish_rows(const NormArgs &a, const float2 (&t)
   // FP8 codes under the dynamic scales: the two-multiply form when the
   // launch asks for it and every chunk of this thread allows it (all but
   // degenerate rows), decided once so that the common loop is straight-line
-  // code; otherwise the quotient form.
+  // code; otherwise the quotient form.  The scale-option instance keeps the
+  // quotient form only (measured on GB300: UE8M0 column-major 32768 x 8192
+  // 315 -> 303 us without the second form compiled in).
   float rf[VPT];
   bool fast = false;
-  if (a.fastq) {
+  if (MODE != kPerGroupX && a.fastq) {
     fast = true;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
