@@ -703,9 +703,9 @@ def run_e2e(torch, vg, step, host, weights, dev, stream, args, dist, ring=4):
     (stream 2) and reads every output back (one device->host copy of the
     output span, stream 3).  A ring of `ring` device buffer sets lets step
     k+1 upload and step k-1 download while step k computes; events order
-    each set's reuse.  (Measured on GB300 for the 70B prefill step: 12.8 ms
-    a step with a ring of 2 or 4, 19.1 ms with 3; the same copies alone,
-    both directions at once, take 12.4 ms.)"""
+    each set's reuse.  (Measured on GB300 for the 70B prefill step: either
+    ~12.6 ms a step or 16-18 ms, from run to run, whatever the ring depth;
+    the same copies alone, both directions at once, take 12.4 ms.)"""
     if sorted(w.op for w in step) != ["norm", "silu"]:
         return None
     sets = [PackedSet(torch, step, host, weights, dev) for _ in range(ring)]
