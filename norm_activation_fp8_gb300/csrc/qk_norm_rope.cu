@@ -72,17 +72,20 @@ __global__ void __launch_bounds__(512) qk_norm_rope_kernel(const QkArgs a) {
     prefetch_l2(a.qkv + t * a.row + (int64_t)h0 * D, 2u * (uint32_t)(nh * D));
   }
   pdl_wait();
-  const int64_t pos = a.pos[t];
-  const bool live = h < a.nh && pos >= 0 && pos < a.max_pos;  // same for the head's lanes
-  if (h < a.nh && !live && l == 0) atomicOr(&g_rope_status, kErrBadPosition);
-  uint16_t *head = a.qkv + t * a.row + (live ? (int64_t)h * D : 0);
+  // The head's loads do not depend on the token's position, so they go out
+  // together with it (a head with a bad position is loaded but not stored);
+  // only the cos/sin row waits for the position.
+  const bool in_head = h < a.nh;
+  uint16_t *head = a.qkv + t * a.row + (in_head ? (int64_t)h * D : 0);
   const uint16_t *w = h < a.hq ? a.qw : a.kw;
-
+  const int64_t pos = a.pos[t];
   // chunk 0 of the lane: l (first half of the head), chunk 1: l + G
-  const uint4 xa = live ? ld_stream(head + l * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
-  const uint4 xb = live ? ld_stream(head + (l + G) * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
-  const uint4 wa = live ? ld_keep(w + l * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
-  const uint4 wb = live ? ld_keep(w + (l + G) * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
+  const uint4 xa = in_head ? ld_stream(head + l * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
+  const uint4 xb = in_head ? ld_stream(head + (l + G) * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
+  const uint4 wa = in_head ? ld_keep(w + l * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
+  const uint4 wb = in_head ? ld_keep(w + (l + G) * kElemsPerChunk) : make_uint4(0, 0, 0, 0);
+  const bool live = in_head && pos >= 0 && pos < a.max_pos;  // same for the head's lanes
+  if (in_head && !live && l == 0) atomicOr(&g_rope_status, kErrBadPosition);
   pdl_launch_dependents();
   float2 ta[4], tb[4];
   float cmax;
