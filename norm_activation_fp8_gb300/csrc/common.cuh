@@ -16,7 +16,14 @@ constexpr float kE4M3Max = 448.0f;   // largest finite OCP E4M3FN value
 constexpr float kAmaxFloor = 1e-10f; // floor on a dynamic amax (no 0/0 on zero rows)
 constexpr int kElemsPerChunk = 8;    // bf16 elements per 16-byte vector
 
-
+// max(a, b, c) by PTX's three-operand max (sm_100 and later); a NaN operand
+// is ignored, so the result is NaN only when all three are.  Amaxes over
+// pairs take one of these instead of two two-operand maxes.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 
 // ------------------------------------------------------------------ bf16
 

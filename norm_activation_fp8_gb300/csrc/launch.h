@@ -147,7 +147,7 @@ struct MlaArgs {
 // vpt == 0: the warp-per-token kernel (block/32 tokens per CTA);
 // otherwise the warp-group kernel (rpc tokens per CTA).
 struct MlaPlan {
-  bool stage = false;  // warp kernel: the token's chunks staged in shared memory
+  bool spread = false;  // warp kernel: tokens dealt out across one wave of CTAs
   int vpt;
   int thr[2];
   int rpc;

@@ -235,17 +235,22 @@ __device__ __forceinline__ void cp_async_wait_all() {
 // wide, known at compile time, so no chunk needs a bounds check or a
 // run-time choice of row (DeepSeek's 1536 + 512 is KQ = 6).  KQ = 0: any
 // widths that fit, with `kq` q chunks per lane at run time.
-// STAGE: the token's chunks go to shared memory by asynchronous copies and
-// both passes read them there, instead of 32 registers a lane holding them
-// from the loads to the stores, so that more warps fit on an SM.
-template <bool QFP8, int KQ, bool STAGE = false>
-__global__ void __launch_bounds__(256, STAGE ? 5 : (QFP8 && KQ > 0 ? 3 : 4))
+// STAGE (DeepSeek's widths): the token's chunks go to shared memory by
+// asynchronous copies and both passes read them there, instead of 32
+// registers a lane holding them from the loads to the stores, so that more
+// warps fit on an SM (five CTAs instead of four).
+// Warp w of CTA b takes token b * 8 + w, or with SPREAD (one wave of CTAs,
+// every resident slot filled) token b + w * grid, so that the tokens of a
+// single wave are dealt evenly over the SMs.
+template <bool QFP8, int KQ, bool STAGE, bool SPREAD>
+__global__ void __launch_bounds__(256, STAGE ? 5 : 4)
     mla_dual_norm_warp_kernel(const MlaArgs a, const int kq_rt) {
   const int kq = KQ > 0 ? KQ : kq_rt;
   __shared__ float4 ws[kMlaWeightChunks * 2];  // both weights as fp32: q chunks, then kv; two planes
   __shared__ uint4 xs[STAGE ? 8 : 1][kMlaWarpChunks][32];  // STAGE: per warp, per chunk, per lane
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t row = SPREAD ? (int64_t)blockIdx.x + (int64_t)(threadIdx.x >> 5) * gridDim.x
+                             : (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const bool live = row < a.T;  // warp-uniform
   // (side is a run-time value of the unrolled index: selects, not indexing,
   // keep everything in registers)
@@ -365,6 +370,12 @@ __global__ void __launch_bounds__(256, STAGE ? 5 : (QFP8 && KQ > 0 ? 3 : 4))
     pass2(std::false_type{});
 }
 
+template <int KQ, bool STAGE, bool SPREAD>
+cudaError_t launch_warp(const MlaArgs &a, bool q_fp8, dim3 g, dim3 b, cudaStream_t s, int kq) {
+  return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, KQ, STAGE, SPREAD>, g, b, 0, s, a, kq)
+               : launch_pdl(mla_dual_norm_warp_kernel<false, KQ, STAGE, SPREAD>, g, b, 0, s, a, kq);
+}
+
 template <int VPT, bool BIG>
 cudaError_t launch_vpt(const MlaArgs &a, bool q_fp8, const MlaPlan &p, cudaStream_t s) {
   const dim3 g((unsigned)p.grid), b((unsigned)p.block);
@@ -395,15 +406,11 @@ cudaError_t launch_mla_dual_norm(MlaArgs a, bool q_fp8, const MlaPlan &p, cudaSt
   const dim3 g((unsigned)p.grid), b((unsigned)p.block);
   if (p.vpt == 0) {  // one warp per token
     const int kq = (a.nch[0] + 31) / 32;
-    if (a.nch[0] == 6 * 32 && a.nch[1] == 2 * 32) {  // DeepSeek's latent widths
-      if (p.stage)
-        return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, 6, true>, g, b, 0, s, a, kq)
-                     : launch_pdl(mla_dual_norm_warp_kernel<false, 6, true>, g, b, 0, s, a, kq);
-      return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, 6>, g, b, 0, s, a, kq)
-                   : launch_pdl(mla_dual_norm_warp_kernel<false, 6>, g, b, 0, s, a, kq);
-    }
-    return q_fp8 ? launch_pdl(mla_dual_norm_warp_kernel<true, 0>, g, b, 0, s, a, kq)
-                 : launch_pdl(mla_dual_norm_warp_kernel<false, 0>, g, b, 0, s, a, kq);
+    if (a.nch[0] == 6 * 32 && a.nch[1] == 2 * 32)  // DeepSeek's latent widths
+      return p.spread ? launch_warp<6, true, true>(a, q_fp8, g, b, s, kq)
+                      : launch_warp<6, true, false>(a, q_fp8, g, b, s, kq);
+    return p.spread ? launch_warp<0, false, true>(a, q_fp8, g, b, s, kq)
+                    : launch_warp<0, false, false>(a, q_fp8, g, b, s, kq);
   }
   switch (p.vpt) {
     case 1: return launch_vpt<1, false>(a, q_fp8, p, s);

@@ -53,7 +53,7 @@ __device__ __forceinline__ uint4 pass1_chunk(const uint4 &xv, const uint4 &rv, c
       acc.ss = f2_fma(r, r, acc.ss);
     }
     t[i] = f2_mul(r, wf[i]);
-    m = fmaxf(m, fmaxf(fabsf(t[i].x), fabsf(t[i].y)));
+    m = fmax3(m, fabsf(t[i].x), fabsf(t[i].y));
   }
   cmax = m;
   return make_uint4(ow[0], ow[1], ow[2], ow[3]);

@@ -130,7 +130,7 @@ __device__ __forceinline__ int pow2_exponent(double amax) {
 __device__ __forceinline__ float amax8(const float (&v)[8]) {
   float m = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  for (int i = 0; i < 8; i += 2) m = fmax3(m, fabsf(v[i]), fabsf(v[i + 1]));
   return m;
 }
 

@@ -210,7 +210,7 @@ bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, T
 }
 
 // MLA dual norm.  Many tokens whose two rows fit eight chunks per lane of a
-// warp (DeepSeek's 1536 + 512 exactly): one warp per token, eight tokens per
+// warp (DeepSeek's 1536 + 512 exactly): one warp per token, eight warps per
 // CTA -- the fewest instructions per element, but about 6 us of latency per
 // token, so it pays from about 13 tokens per SM (measured: from T ~ 2048 on
 // 152 SMs).  Otherwise a token's rows spread over a warp group: one token
@@ -221,17 +221,29 @@ bool plan_norm_tma(int64_t T, int H, bool res, int mode, int ngroups, int sms, T
 MlaPlan plan_mla(int64_t T, int nq, int nkv, bool q_fp8, int sms) {
   MlaPlan p;
   if ((nq + 31) / 32 + (nkv + 31) / 32 <= 8 && T >= 13LL * sms) {
-    // The token's chunks go through shared memory (DeepSeek's widths): for
-    // bf16 at every T here, for an fp8 q from 40 tokens per SM.  Measured
-    // on GB300: bf16 0.41 -> 0.46 (T = 2048), 0.71 -> 0.81 (8192), 0.89 ->
-    // 0.99 (32768), equal at 4096; fp8 0.58 -> 0.58 (8192), 0.68 -> 0.71
-    // (32768), but 0.47 -> 0.44 at 4096.
-    p.stage = !q_fp8 || T >= 40LL * sms;
+    // DeepSeek's widths have instances with the token's chunks staged in
+    // shared memory (five CTAs per SM); other widths hold them in registers
+    // (four CTAs per SM).  Measured on GB300, staged against registers:
+    // bf16 0.71 -> 0.81 (T = 8192), 0.89 -> 0.99 (32768); fp8 0.68 -> 0.71
+    // (32768).
+    const bool fixed = nq == 6 * 32 && nkv == 2 * 32;
     p.vpt = 0;
     p.thr[0] = p.thr[1] = 0;
     p.rpc = 8;
     p.block = 256;
     p.grid = (T + 7) / 8;
+    // Up to one full wave, consecutive 8-token CTAs would leave some SMs a
+    // whole CTA more than others (4096 tokens: 32 on 56 SMs, 24 on the
+    // rest); instead every resident CTA slot gets a CTA and the tokens are
+    // dealt out across them, warp by warp (at most one token apart per CTA).
+    // Every CTA of such a wave prefetches its tokens into L2.  Measured on
+    // GB300: T = 4096 bf16 0.54 -> 0.67, fp8 0.50 -> 0.53; T = 2048 bf16
+    // 0.47 -> 0.48, fp8 0.33 -> 0.39.
+    const int64_t wave = (int64_t)sms * (fixed ? 5 : 4);
+    if (T < 8 * wave) {
+      p.spread = true;
+      p.grid = wave;
+    }
     return p;
   }
   p.vpt = T >= 4LL * sms ? 2 : 1;
@@ -294,6 +306,7 @@ vg_status mla_dual_norm(uint16_t *q_out, uint8_t *q_fp8, float *q_scale, uint16_
   a.inv_n[0] = 1.0f / (float)q_dim;
   a.inv_n[1] = 1.0f / (float)kv_dim;
   const MlaPlan p = plan_mla(T, a.nch[0], a.nch[1], fp8, sms);
+  if (p.spread) a.pf_ctas = (int32_t)p.grid;  // a single wave: every CTA prefetches
   return launch_mla_dual_norm(a, fp8, p, (cudaStream_t)stream) == cudaSuccess ? VG_OK
                                                                                : VG_ERR_CUDA;
 }

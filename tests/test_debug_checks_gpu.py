@@ -35,8 +35,8 @@ def _silu(T, I, mode, G=128):
     return lambda: parity.gpu_silu(d["gate_up"], mode, G, scale=0.1)
 
 
-def _mla(T, fp8):
-    d = gen.mla_inputs(T, gen.MLA_Q_DIM, gen.MLA_KV_DIM, seed=T)
+def _mla(T, fp8, q_dim=gen.MLA_Q_DIM, kv_dim=gen.MLA_KV_DIM):
+    d = gen.mla_inputs(T, q_dim, kv_dim, seed=T)
     return lambda: parity.gpu_mla(d["q_c"], d["q_weight"], d["kv_c"], d["kv_weight"], 1e-6, 1e-6, fp8)
 
 
@@ -80,7 +80,9 @@ CASES = {
     "silu-group-ue8m0-colmajor-400x14336": _silu(400, 14336, PG | OPT),
     "silu-nvfp4-400x14336": _nvfp4_silu(400, 14336),
     "mla-bf16-64": _mla(64, False),
-    "mla-fp8-2048": _mla(2048, True),
+    "mla-fp8-2048-wave": _mla(2048, True),
+    "mla-fp8-2100-registers-wave": _mla(2100, True, 1024, 512),
+    "mla-bf16-5000-registers": _mla(5000, False, 1024, 512),
     "mla-bf16-7400-staged": _mla(7400, False),
     "mla-fp8-7400-staged": _mla(7400, True),
     "qk-neox-64": _qk(64),

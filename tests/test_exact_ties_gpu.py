@@ -66,9 +66,14 @@ def test_norm_exact_ties(T, H, mode, G, eps):
 
 
 @pytest.mark.parametrize("eps", [0.0, 1e-5], ids=["no-direction", "direction"])
-@pytest.mark.parametrize("T", [64, 2048, 7400], ids=["group-kernel", "warp-registers", "warp-staged"])
-def test_mla_fp8_exact_ties(T, eps):
-    q_dim, kv_dim = gen.MLA_Q_DIM, gen.MLA_KV_DIM
+@pytest.mark.parametrize("T,q_dim,kv_dim", [
+    (64, gen.MLA_Q_DIM, gen.MLA_KV_DIM),    # warp-group kernel
+    (2048, gen.MLA_Q_DIM, gen.MLA_KV_DIM),  # warp kernel, staged, tokens dealt over one wave
+    (7400, gen.MLA_Q_DIM, gen.MLA_KV_DIM),  # warp kernel, staged, eight tokens per CTA
+    (2100, 1024, 512),                      # warp kernel in registers, one wave
+    (5000, 1024, 512),                      # warp kernel in registers, eight tokens per CTA
+], ids=["group-kernel", "warp-staged-wave", "warp-staged", "warp-registers-wave", "warp-registers"])
+def test_mla_fp8_exact_ties(T, q_dim, kv_dim, eps):
     d = {"q_c": tie_rows(T, q_dim, seed=T), "kv_c": gen.mla_inputs(T, 8, kv_dim, seed=T)["kv_c"],
          "q_weight": tie_weight(q_dim, q_dim, seed=1), "kv_weight": tie_weight(kv_dim, kv_dim, seed=2)}
     g = parity.gpu_mla(d["q_c"], d["q_weight"], d["kv_c"], d["kv_weight"], eps, 1e-6, True)

@@ -47,7 +47,8 @@ def test_mla_deepseek_shapes(T, q_fp8):
     (1280, 768, 8, 8, 2100),      # the warp kernel: 5 + 3 (too wide for a pair)
     (1000, 400, 8, 24, 2100),     # the warp kernel: ragged 2 + 1 chunks per lane
     (1536, 512, 0, 64, 4099),     # the fixed-layout warp kernel, strided rows, ragged T
-    (1536, 512, 0, 64, 6081),     # the same, more tokens
+    (1536, 512, 0, 64, 6081),     # the same, more tokens than one wave of CTAs
+    (1024, 1016, 8, 8, 5000),     # the warp kernel in registers, more than one wave
 ])
 def test_mla_shapes_and_strides(q_dim, kv_dim, q_pad, kv_pad, T, q_fp8):
     run(T, q_dim, kv_dim, q_fp8, seed=q_dim + kv_dim + T, q_pad=q_pad, kv_pad=kv_pad)

@@ -71,7 +71,7 @@ def test_qk_norm_rope_twice_in_place(T):
 
 
 @pytest.mark.parametrize("fp8", [False, True], ids=["bf16", "fp8"])
-@pytest.mark.parametrize("T", [64, 2048, 7400], ids=["group", "warp", "staged"])
+@pytest.mark.parametrize("T", [64, 2048, 7400], ids=["group", "warp-wave", "warp"])
 def test_mla_after_a_rewrite_of_its_input(T, fp8):
     import torch
     q_dim, kv_dim, rope = gen.MLA_Q_DIM, gen.MLA_KV_DIM, 64
