@@ -224,13 +224,15 @@ __device__ __noinline__ void nvfp4_silu_settle(const uint16_t *gate_up, uint8_t 
 // CTA.
 // OPT: per-group with scale options (UE8M0 and/or column-major), an
 // instance of its own so that plain per-group code stays as it is.
-// DENSE: row-segment rows (per-group, scale options, NVFP4) of at most two
-// chunks a thread in 32 registers, four CTAs per SM: more row segments in
-// flight per SM (measured on GB300 from two rows per SM: per-group
-// 2048 x 14336 0.94 -> 1.00, 32768 x 28672 0.93 -> 0.99; NVFP4
+// DENSE: row-segment rows (static, per-group, scale options, NVFP4) of at
+// most two chunks a thread in 32 registers, four CTAs per SM: more row
+// segments in flight per SM (measured on GB300 from two rows per SM:
+// per-group 2048 x 14336 0.94 -> 1.00, 32768 x 28672 0.93 -> 0.99; NVFP4
 // 32768 x 28672 0.88 -> 0.93; UE8M0 column-major 32768 x 14336 0.92 ->
-// 0.96; below two rows per SM, a single partial wave, three CTAs' larger
-// register budget is faster).
+// 0.96; static, against four chunks a thread at three CTAs, 2048 x 14336
+// 0.94 -> 1.01, 512 x 14336 0.68 -> 0.81, 4096 x 14336 0.99 -> 1.01,
+// 32768 x 14336 1.04 -> 1.03; below two rows per SM, a single partial
+// wave, three CTAs' larger register budget is faster).
 template <int VPT, int MODE, int GCH, bool BIG, bool OPT = false, bool DENSE = false>
 __global__ void __launch_bounds__(BIG ? 1024 : 512, BIG ? 1 : (MODE == kPerToken ? 2 : (DENSE ? 4 : 3)))
     silu_fp8_kernel(const SiluArgs a) {
@@ -541,7 +543,10 @@ template <int VPT>
 cudaError_t launch_mode(const SiluArgs &a, int mode, const RowPlan &p, cudaStream_t s) {
   const dim3 g((unsigned)p.grid, (unsigned)p.segs), b((unsigned)p.block());
   switch (mode) {
-    case kStatic: return launch_pdl(silu_fp8_kernel<VPT, kStatic, 1, false>, g, b, 0, s, a);
+    case kStatic:
+      if constexpr (VPT <= 2)
+        if (p.dense) return launch_pdl(silu_fp8_kernel<VPT, kStatic, 1, false, false, true>, g, b, 0, s, a);
+      return launch_pdl(silu_fp8_kernel<VPT, kStatic, 1, false>, g, b, 0, s, a);
     case kNvfp4:  // the per-group plan: at most two chunks a thread
       if constexpr (VPT <= 2)
         return p.dense ? launch_pdl(silu_fp8_kernel<VPT, kNvfp4, 2, false, false, true>, g, b, 0, s, a)

@@ -127,11 +127,12 @@ RowPlan plan_rows(int64_t T, int nch, int min_vpt, int sms) {
 }
 
 // SiLU.  Static / per-group keep no row state: a row is cut into column
-// segments of at most 448 threads x VPT chunks (static four chunks a
-// thread, per-group two), each an independent CTA; rows of <= 64 chunks go
-// one warp per row, eight rows per CTA.  Per-token needs the row in one CTA:
-// four chunks a thread, up to 1024 threads (fewer chunks when that still
-// fits 448 threads).
+// segments of at most 448 threads x VPT chunks (two chunks a thread; static
+// four below two rows per SM), each an independent CTA; from two rows per
+// SM these run the dense instance (four CTAs per SM).  Rows of <= 64 chunks
+// go one warp per row, eight rows per CTA.  Per-token needs the row in one
+// CTA: four chunks a thread, up to 1024 threads (fewer chunks when that
+// still fits 448 threads).
 RowPlan plan_silu(int64_t T, int nch, int mode, int sms) {
   RowPlan p;
   p.rpc = 1;
@@ -146,9 +147,9 @@ RowPlan plan_silu(int64_t T, int nch, int mode, int sms) {
     p.grid = (T + p.rpc - 1) / p.rpc;
     return p;
   } else {
-    p.vpt = mode == VG_SCALE_STATIC ? 4 : 2;
+    p.dense = T >= 2LL * sms;
+    p.vpt = (mode == VG_SCALE_STATIC && !p.dense) ? 4 : 2;
     p.segs = (nch + 448 * p.vpt - 1) / (448 * p.vpt);
-    p.dense = mode == VG_SCALE_PER_GROUP && T >= 2LL * sms;
   }
   const int per = (nch + p.segs * p.vpt - 1) / (p.segs * p.vpt);
   p.ntr = (per + 31) / 32 * 32;

@@ -73,6 +73,7 @@ CASES = {
     "norm-nvfp4-700x8192": _nvfp4_norm(700, 8192),
     "norm-pad-700x2880": _pad(700),
     "silu-static-300x14336": _silu(300, 14336, ST),
+    "silu-static-400x14336-dense": _silu(400, 14336, ST),
     "silu-group-64x14336": _silu(64, 14336, PG),
     "silu-group-400x14336-dense": _silu(400, 14336, PG),
     "silu-token-256x14336": _silu(256, 14336, PT),

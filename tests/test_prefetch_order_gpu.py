@@ -112,7 +112,7 @@ def test_mla_after_a_rewrite_of_its_input(T, fp8):
     _run_both_ways(torch, lambda: [t.fill_(0) for t in outputs()], run, outputs)
 
 
-@pytest.mark.parametrize("mode", [gen.PER_GROUP, gen.PER_TOKEN], ids=["per_group", "per_token"])
+@pytest.mark.parametrize("mode", [gen.STATIC, gen.PER_GROUP, gen.PER_TOKEN], ids=["static", "per_group", "per_token"])
 @pytest.mark.parametrize("T", [64, 400], ids=["register", "dense"])
 def test_silu_after_a_rewrite_of_its_input(T, mode):
     import torch
@@ -121,11 +121,12 @@ def test_silu_after_a_rewrite_of_its_input(T, mode):
     srcs = [torch.from_numpy(gen.silu_inputs(T, I, seed=T + k)["gate_up"].view(np.int16)).to(dev)
             for k in range(2)]
     gu = torch.empty_like(srcs[0])
+    static = torch.full((1,), 0.1, dtype=torch.float32, device=dev)  # an input, not rewritten
     outs = []
     for _ in srcs:
         q = torch.empty((T, I), dtype=torch.uint8, device=dev)
-        s = torch.empty((T,) if mode == gen.PER_TOKEN else (T, I // 128), dtype=torch.float32,
-                        device=dev)
+        s = static if mode == gen.STATIC else torch.empty(
+            (T,) if mode == gen.PER_TOKEN else (T, I // 128), dtype=torch.float32, device=dev)
         outs.append((q, s))
 
     def run(sync):
@@ -136,6 +137,6 @@ def test_silu_after_a_rewrite_of_its_input(T, mode):
                 torch.cuda.synchronize()
 
     def outputs():
-        return [t for o in outs for t in o]
+        return [t for o in outs for t in o if t is not static]
 
     _run_both_ways(torch, lambda: [t.fill_(0) for t in outputs()], run, outputs)
