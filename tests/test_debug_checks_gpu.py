@@ -111,7 +111,8 @@ def test_debug_build_matches_and_reports_nothing(case, monkeypatch):
 
 
 SHRUNK = ["norm-token-256x4096", "norm-group-1000x4096-tma", "silu-token-400x14336-tma",
-          "silu-group-400x14336-dense", "mla-fp8-7400-staged", "qk-neox-64"]
+          "silu-group-400x14336-dense", "silu-static-400x14336-dense", "mla-fp8-7400-staged",
+          "mla-fp8-2048-wave", "mla-bf16-5000-registers", "qk-neox-64"]
 
 
 @pytest.mark.parametrize("case", SHRUNK)
