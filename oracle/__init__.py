@@ -33,7 +33,12 @@ Parity status per function (each pin lives in ``tests/test_oracle_pins.py``):
   qk_norm_rope .............. pinned (identity and quarter-turn rotations
                               against the pinned bf16 rms_norm, V untouched,
                               neox/gptj by permutation, exact rationals)
-  NaN / Inf inputs .......... parity unpinned (no workload contains them)
+  NaN / Inf inputs, FP8 norm and SiLU ... pinned (the IEEE consequences:
+                              NaN rows, an infinite residual, silu(-inf),
+                              saturation under a static scale, against
+                              values fixed by that reading)
+  NaN / Inf in the NVFP4, padded, MLA and QK paths ... parity unpinned
+                              (no workload contains them)
 """
 from __future__ import annotations
 
